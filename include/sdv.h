@@ -1,0 +1,212 @@
+/*
+ * sdv.h -- C ABI of libsdv, the GB300 (sm_103a) kernels of the verify forward
+ * of greedy speculative decoding.
+ *
+ * The operations and where they are defined:
+ *
+ *  - per-block-32 absmax symmetric int8 / int4 weight quantisation:
+ *    "Riding Apple's pipelined GPU engine -- 3.5x over a hand-rolled loop, zero
+ *    custom kernels", section "Quantization on the GPU delegate" (int8 linear
+ *    per-block-32 is the ship configuration; q4_0 is per-block-32 absmax
+ *    symmetric int4; big-vocabulary heads use plain absmax, never clipping);
+ *  - the verify forward over a static window of S = K+1 rows:
+ *    "Spec-decode on GDN hybrids (Qwen3.5/3.6 family) -- static-S verify
+ *    design", section "Verify graph = STATIC S=K+1 + chunked GDN scan", and
+ *    "Stream C -- Speculative decoding: feasibility verdict + implementation
+ *    plan", section "TL;DR" (a K-token verify forward costs about one decode
+ *    step: it is bound by reading the weights once);
+ *  - the batched on-GPU argmax [S, vocab] -> [S] and the greedy accept rule:
+ *    "Stream C ...", section "The delta -- new ENGINE work for greedy n-gram
+ *    spec-decode", and "Spec-decode on GDN hybrids ...", section "Hybrid state
+ *    discipline" (a0 is committed first; the row after the last accepted draft
+ *    becomes the next a0; pad drafts are never accepted);
+ *  - only the sampled ids cross back to the host: "Riding Apple's pipelined GPU
+ *    engine", section "Why hand-rolled per-token loops lose ~3x";
+ *  - the fused SwiGLU MLP: "Flagship dramatic-speedup plan -- the full stackable
+ *    tuning set", section "Axis 4 -- kernel micro-opts";
+ *  - gathered routed experts (top-8 of 256): same page, section "Baseline byte
+ *    model".
+ *
+ * Conventions for every entry point:
+ *  - Tensor pointers are DEVICE pointers owned by the caller; the library never
+ *    allocates, frees or keeps state between calls.  Row-major everywhere.
+ *  - fp16 values (activations, scales, h) are passed as IEEE binary16 bit
+ *    patterns (uint16_t).
+ *  - Every call is asynchronous on `stream` (a cudaStream_t; NULL = the legacy
+ *    default stream).  Results are valid once the stream has been synchronised.
+ *  - Arguments are validated on the host before any launch; an invalid argument
+ *    returns an error and launches nothing.  Errors are returned, never thrown,
+ *    and the library never exits the process.
+ *  - Weight code and scale pointers, activation pointers and workspaces must be
+ *    16-byte aligned (weights are read by the Tensor Memory Accelerator).
+ *  - Workspaces ("ws") are caller-owned device scratch of at least
+ *    sdv_workspace_bytes(...) bytes, ZERO-FILLED before their first use
+ *    (sdv_workspace_init does it).  Every completed call leaves the workspace's
+ *    counters back at zero, so one workspace serves any number of calls issued
+ *    in stream order.  Calls that overlap on the GPU must not share a workspace.
+ */
+#ifndef SDV_H
+#define SDV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define SDV_API __attribute__((visibility("default")))
+#else
+#define SDV_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A cudaStream_t (the runtime's stream handle), declared without CUDA headers. */
+typedef struct CUstream_st* sdv_stream_t;
+
+typedef enum {
+  SDV_OK = 0,
+  SDV_ERR_INVALID_ARG = 1, /* null/misaligned pointer, bad size, n_valid out of range */
+  SDV_ERR_UNSUPPORTED = 2, /* valid but outside what the kernels handle (e.g. S > 32) */
+  SDV_ERR_CUDA = 3,        /* a CUDA runtime error while launching */
+  SDV_ERR_TIMEOUT = 4,     /* a bounded device-side wait gave up (see sdv_device_status) */
+  SDV_ERR_WORKSPACE = 5    /* workspace null, misaligned or smaller than required */
+} sdv_status;
+
+typedef enum { SDV_Q8 = 8, SDV_Q4 = 4 } sdv_qtype;
+
+/* Operation ids for sdv_workspace_bytes. */
+typedef enum {
+  SDV_OP_QLINEAR = 1,
+  SDV_OP_QLINEAR_SWIGLU = 2,
+  SDV_OP_VERIFY_HEAD = 3,
+  SDV_OP_MOE = 4
+} sdv_op;
+
+/*
+ * A per-block-32 quantised weight W[n, k] (n output rows, reduction length k,
+ * k % 32 == 0).  Block b of row r covers W[r, 32b .. 32b+31] and has one fp16
+ * scale s[r, b]; the weight is q * s with q in [-127, 127] (Q8) or [-7, 7] (Q4).
+ *   Q8: codes = int8  [n][k]    (one two's-complement byte per weight)
+ *   Q4: codes = uint8 [n][k/2]  (two's-complement nibbles; byte i of a row holds
+ *                                 weight 2i in bits 0-3 and weight 2i+1 in bits 4-7)
+ *   scales = fp16 [n][k/32]
+ */
+typedef struct {
+  int32_t qtype;          /* SDV_Q8 or SDV_Q4 */
+  int32_t n;              /* output rows, >= 1 */
+  int32_t k;              /* reduction length, >= 32, multiple of 32 */
+  const void* codes;      /* device, 16-byte aligned */
+  const uint16_t* scales; /* device, 16-byte aligned */
+} sdv_qweight;
+
+/*
+ * Quantise fp32 w[n][k] per block of 32 along k:  s32 = max|w| / Q (IEEE fp32
+ * division), s = fp16(s32) rounded to nearest even, q = clamp(rint(w / s), -Q, Q)
+ * (IEEE fp32 division, ties to even); s == 0 gives q = 0.  Q = 127 (SDV_Q8) or
+ * 7 (SDV_Q4).  Writes `codes` in the sdv_qweight layout of `qtype` and `scales`
+ * fp16 [n][k/32].  No workspace.
+ */
+SDV_API sdv_status sdv_quantize_block32(const float* w, int32_t n, int32_t k, int32_t qtype,
+                                void* codes, uint16_t* scales, sdv_stream_t stream);
+
+/*
+ * Dequantised skinny GEMM:  y[s][r] = sum_h x[s][h] * q[r][h] * s[r][h/32]
+ * for s < S, r < w->n; fp16 activations, fp32 accumulation, fp32 output.
+ *   x: fp16 [S][w->k];  y: fp32 [S][w->n];  1 <= S <= 32.
+ */
+SDV_API sdv_status sdv_qlinear(const sdv_qweight* w, const uint16_t* x, int32_t S, float* y,
+                       void* ws, size_t ws_bytes, sdv_stream_t stream);
+
+/*
+ * Fused SwiGLU gate/up projection: h[s][r] = fp16( SiLU(g) * u ) with
+ * g = (x G^T)[s][r], u = (x U^T)[s][r] accumulated in fp32 and
+ * SiLU(t) = t / (1 + exp(-t)); the result is rounded once to fp16 (nearest even).
+ * gate and up must have equal n, k and qtype.   x: fp16 [S][k];  h: fp16 [S][n].
+ */
+SDV_API sdv_status sdv_qlinear_swiglu(const sdv_qweight* gate, const sdv_qweight* up,
+                              const uint16_t* x, int32_t S, uint16_t* h,
+                              void* ws, size_t ws_bytes, sdv_stream_t stream);
+
+/*
+ * The verify head over one window [a0, d_1 .. d_{S-1}]:
+ *   logits[s][v] = sum_h x[s][h] * q[v][h] * s[v][h/32]        (fp32 accumulate)
+ *   argmax[s]    = the lowest v with logits[s][v] == max_v' logits[s][v']
+ *   accepted     = the largest j <= n_valid with drafts[i] == argmax[i] for all i < j
+ *   next_a0      = argmax[accepted]   (the correction on a miss, the bonus token
+ *                                       when all n_valid drafts were accepted)
+ * head: the quantised lm_head, n = vocabulary size, k = hidden size.
+ * x: fp16 [S][k] hidden states of the window rows (row 0 = the row of a0).
+ * drafts: int32 [S-1], drafts[i] = the token at window position i+1; entries at
+ *   i >= n_valid are pad and never accepted.  May be NULL when n_valid == 0.
+ * n_valid: 0 <= n_valid <= S-1.
+ * logits_or_null: fp32 [S][n] written when non-NULL (parity/debug; the hot path
+ *   passes NULL and the full logits never leave the chip).
+ * argmax: int32 [S];  accepted, next_a0: int32 [1] each.
+ * One kernel launch: a persistent dequant GEMM whose epilogue reduces each
+ * CTA's vocabulary slab to per-row (max, index) partials in `ws`; the last CTA
+ * to finish reduces the partials and runs the accept.
+ */
+SDV_API sdv_status sdv_verify_head(const sdv_qweight* head, const uint16_t* x, int32_t S,
+                           const int32_t* drafts, int32_t n_valid, float* logits_or_null,
+                           int32_t* argmax, int32_t* accepted, int32_t* next_a0,
+                           void* ws, size_t ws_bytes, sdv_stream_t stream);
+
+/*
+ * The greedy accept rule alone, on a given argmax[S] (device, int32), with the
+ * same definition and outputs as sdv_verify_head.  No workspace.
+ */
+SDV_API sdv_status sdv_greedy_accept(const int32_t* argmax, int32_t S, const int32_t* drafts,
+                             int32_t n_valid, int32_t* accepted, int32_t* next_a0,
+                             sdv_stream_t stream);
+
+/*
+ * Gathered-expert SwiGLU MoE over the window rows:
+ *   route:   per row s, the top_k experts by router_logits[s][e] (ties to the
+ *            lower id), weights w = softmax over the top_k selected logits;
+ *   experts: for each selected (s, e): h = SiLU(x[s] G_e^T) * (x[s] U_e^T),
+ *            y = h D_e^T;
+ *   combine: out[s] = sum_j w[s][j] * y(s, e_j).
+ * gate, up: stacked [E*I][H] (expert e owns rows e*I .. e*I+I-1);
+ * down: stacked [E*H][I] (expert e owns rows e*H .. e*H+H-1); all the same qtype.
+ * x: fp16 [S][H]; router_logits: fp32 [S][E]; out: fp32 [S][H].
+ * topk_ids_or_null (int32 [S][top_k]) and topk_w_or_null (fp32 [S][top_k]) are
+ * written, in selection order, when non-NULL.
+ */
+SDV_API sdv_status sdv_moe_gather_qmm(const sdv_qweight* gate, const sdv_qweight* up,
+                              const sdv_qweight* down, int32_t E, int32_t I, int32_t H,
+                              int32_t top_k, const uint16_t* x, const float* router_logits,
+                              int32_t S, float* out, int32_t* topk_ids_or_null,
+                              float* topk_w_or_null, void* ws, size_t ws_bytes,
+                              sdv_stream_t stream);
+
+/*
+ * Workspace bytes an operation needs on the current device.
+ * `op` is an sdv_op; n, k are the weight's (for SDV_OP_MOE: n = I, k = H);
+ * S the window rows; E, top_k for SDV_OP_MOE (ignored otherwise).
+ * Returns 0 for invalid arguments; the operation itself reports them.
+ */
+SDV_API size_t sdv_workspace_bytes(int32_t op, int32_t n, int32_t k, int32_t S, int32_t E,
+                           int32_t top_k);
+
+/* Zero-fill a workspace (cudaMemsetAsync on `stream`). */
+SDV_API sdv_status sdv_workspace_init(void* ws, size_t ws_bytes, sdv_stream_t stream);
+
+/*
+ * Synchronise `stream`, then read and clear the device status word a kernel
+ * leaves in `ws`: SDV_OK, or SDV_ERR_TIMEOUT if a bounded wait for an
+ * asynchronous copy gave up (the outputs of that call are then undefined).
+ */
+SDV_API sdv_status sdv_device_status(void* ws, sdv_stream_t stream);
+
+/* A static, human-readable name of a status code. */
+SDV_API const char* sdv_status_string(sdv_status status);
+
+/* Library version (major * 10000 + minor * 100 + patch). */
+SDV_API int32_t sdv_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SDV_H */

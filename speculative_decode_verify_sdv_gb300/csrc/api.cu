@@ -1,0 +1,268 @@
+// C ABI of libsdv (declared in include/sdv.h): argument validation, TMA
+// descriptor encoding, launch configuration and workspace layout.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "sdv.h"
+#include "sdv_kernels.h"
+
+namespace {
+
+using sdv::GemmArgs;
+
+constexpr size_t kWsHeader = 256;  // status word, ticket counter, reserved
+constexpr int kMaxS = 32;
+constexpr int kMaxDepth = 8;
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+sdv_status cuda_status(cudaError_t e) { return e == cudaSuccess ? SDV_OK : SDV_ERR_CUDA; }
+
+// cuTensorMapEncodeTiled, fetched from the driver once (no link-time libcuda).
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+int device_sms() {
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  return sms;
+}
+
+int device_smem_optin() {
+  int dev = 0, v = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (cudaDeviceGetAttribute(&v, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess) return 0;
+  return v;
+}
+
+bool valid_weight(const sdv_qweight* w) {
+  if (w == nullptr || w->codes == nullptr || w->scales == nullptr) return false;
+  if (w->qtype != SDV_Q8 && w->qtype != SDV_Q4) return false;
+  if (w->n < 1 || w->k < 32 || (w->k % 32) != 0) return false;
+  if (!aligned16(w->codes) || !aligned16(w->scales)) return false;
+  return true;
+}
+
+// Codes: uint8 [n][row_bytes], box 128 bytes x 16 rows, 128-byte swizzle.
+// Scales: fp16 [n][k/32], box 8 x (16 * mt) rows (only when k % 256 == 0).
+sdv_status encode_maps(const sdv_qweight* w, int mt, CUtensorMap* tc, CUtensorMap* tsc, int* scales_tma) {
+  auto enc = encode_fn();
+  if (enc == nullptr) return SDV_ERR_CUDA;
+  const uint64_t row_bytes = (w->qtype == SDV_Q8) ? (uint64_t)w->k : (uint64_t)w->k / 2;
+  {
+    cuuint64_t dims[2] = {row_bytes, (cuuint64_t)w->n};
+    cuuint64_t strides[1] = {row_bytes};
+    cuuint32_t box[2] = {128, 16};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(tc, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(w->codes), dims, strides,
+                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return SDV_ERR_CUDA;
+  }
+  *scales_tma = (w->k % 256) == 0 ? 1 : 0;
+  std::memset(tsc, 0, sizeof(*tsc));
+  if (*scales_tma) {
+    cuuint64_t dims[2] = {(cuuint64_t)(w->k / 32), (cuuint64_t)w->n};
+    cuuint64_t strides[1] = {(cuuint64_t)(w->k / 32) * 2};
+    cuuint32_t box[2] = {8, (cuuint32_t)(16 * mt)};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(tsc, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<uint16_t*>(w->scales), dims,
+                     strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                     CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return SDV_ERR_CUDA;
+  }
+  return SDV_OK;
+}
+
+// Largest ring depth whose shared-memory plan fits; 0 if none >= 2 does.
+int pick_depth(int qbits, int S, int k_len, int* smem) {
+  const int limit = device_smem_optin();
+  for (int d = kMaxDepth; d >= 2; --d) {
+    const int b = sdv::gemm_smem_bytes(qbits, S, k_len, d);
+    if (b <= limit) {
+      *smem = b;
+      return d;
+    }
+  }
+  return 0;
+}
+
+int gemm_grid(int n) {
+  const int tiles = (n + 15) / 16;
+  const int w = sdv::gemm_warps_per_cta();
+  int grid = (tiles + w - 1) / w;
+  const int sms = device_sms();
+  if (grid > sms) grid = sms;
+  return grid < 1 ? 1 : grid;
+}
+
+size_t head_ws_bytes(int S) {
+  const int sms = device_sms();
+  return kWsHeader + (size_t)(sms > 0 ? sms : 1024) * (size_t)S * 8;
+}
+
+// Common part of the weight-streaming GEMM launches.
+sdv_status run_gemm(const sdv_qweight* w, const uint16_t* x, int S, int mode, GemmArgs& a, void* ws,
+                    cudaStream_t st) {
+  const int mt = sdv::gemm_tile_mt(w->qtype);
+  CUtensorMap tc, tsc;
+  int scales_tma = 0;
+  sdv_status s = encode_maps(w, mt, &tc, &tsc, &scales_tma);
+  if (s != SDV_OK) return s;
+  int smem = 0;
+  const int depth = pick_depth(w->qtype, S, w->k, &smem);
+  if (depth == 0) return SDV_ERR_UNSUPPORTED;
+  a.x = reinterpret_cast<const __half*>(x);
+  a.scales = w->scales;
+  a.S = S;
+  a.N = w->n;
+  a.K = w->k;
+  a.k_begin = 0;
+  a.k_len = w->k;
+  a.m16_tiles = (w->n + 15) / 16;
+  a.depth = depth;
+  a.scales_tma = scales_tma;
+  a.status = static_cast<int*>(ws);
+  a.ticket = reinterpret_cast<unsigned*>(static_cast<char*>(ws) + 4);
+  const int grid = gemm_grid(w->n);
+  return cuda_status(sdv::launch_dq_gemm(w->qtype, mode, tc, tsc, a, grid, smem, st));
+}
+
+}  // namespace
+
+extern "C" {
+
+int32_t sdv_version(void) { return 100; }
+
+const char* sdv_status_string(sdv_status s) {
+  switch (s) {
+    case SDV_OK: return "SDV_OK";
+    case SDV_ERR_INVALID_ARG: return "SDV_ERR_INVALID_ARG";
+    case SDV_ERR_UNSUPPORTED: return "SDV_ERR_UNSUPPORTED";
+    case SDV_ERR_CUDA: return "SDV_ERR_CUDA";
+    case SDV_ERR_TIMEOUT: return "SDV_ERR_TIMEOUT";
+    case SDV_ERR_WORKSPACE: return "SDV_ERR_WORKSPACE";
+  }
+  return "SDV_ERR_UNKNOWN";
+}
+
+size_t sdv_workspace_bytes(int32_t op, int32_t n, int32_t k, int32_t S, int32_t E, int32_t top_k) {
+  (void)n; (void)k; (void)E; (void)top_k;
+  if (S < 1 || S > kMaxS) return 0;
+  switch (op) {
+    case SDV_OP_QLINEAR:
+    case SDV_OP_QLINEAR_SWIGLU: return kWsHeader;
+    case SDV_OP_VERIFY_HEAD: return head_ws_bytes(S);
+    case SDV_OP_MOE: return kWsHeader;
+  }
+  return 0;
+}
+
+sdv_status sdv_workspace_init(void* ws, size_t ws_bytes, sdv_stream_t stream) {
+  if (ws == nullptr || ws_bytes < kWsHeader) return SDV_ERR_WORKSPACE;
+  return cuda_status(cudaMemsetAsync(ws, 0, ws_bytes, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+sdv_status sdv_device_status(void* ws, sdv_stream_t stream) {
+  if (ws == nullptr) return SDV_ERR_WORKSPACE;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(st) != cudaSuccess) return SDV_ERR_CUDA;
+  int word = 0;
+  if (cudaMemcpy(&word, ws, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return SDV_ERR_CUDA;
+  if (word == 0) return SDV_OK;
+  const int zero = 0;
+  if (cudaMemcpy(ws, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess) return SDV_ERR_CUDA;
+  return SDV_ERR_TIMEOUT;
+}
+
+sdv_status sdv_quantize_block32(const float* w, int32_t n, int32_t k, int32_t qtype, void* codes,
+                                uint16_t* scales, sdv_stream_t stream) {
+  if (w == nullptr || codes == nullptr || scales == nullptr) return SDV_ERR_INVALID_ARG;
+  if (n < 1 || k < 32 || (k % 32) != 0) return SDV_ERR_INVALID_ARG;
+  if (qtype != SDV_Q8 && qtype != SDV_Q4) return SDV_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(w) & 3u) || (reinterpret_cast<uintptr_t>(scales) & 1u))
+    return SDV_ERR_INVALID_ARG;
+  return cuda_status(sdv::launch_quantize(w, n, k, qtype, codes, scales,
+                                          reinterpret_cast<cudaStream_t>(stream)));
+}
+
+sdv_status sdv_qlinear(const sdv_qweight* w, const uint16_t* x, int32_t S, float* y, void* ws,
+                       size_t ws_bytes, sdv_stream_t stream) {
+  if (!valid_weight(w) || x == nullptr || y == nullptr || !aligned16(x)) return SDV_ERR_INVALID_ARG;
+  if (S < 1) return SDV_ERR_INVALID_ARG;
+  if (S > kMaxS) return SDV_ERR_UNSUPPORTED;
+  if (ws == nullptr || !aligned16(ws) || ws_bytes < sdv_workspace_bytes(SDV_OP_QLINEAR, w->n, w->k, S, 0, 0))
+    return SDV_ERR_WORKSPACE;
+  GemmArgs a{};
+  a.y = y;
+  return run_gemm(w, x, S, sdv::kModeY, a, ws, reinterpret_cast<cudaStream_t>(stream));
+}
+
+sdv_status sdv_verify_head(const sdv_qweight* head, const uint16_t* x, int32_t S, const int32_t* drafts,
+                           int32_t n_valid, float* logits_or_null, int32_t* argmax, int32_t* accepted,
+                           int32_t* next_a0, void* ws, size_t ws_bytes, sdv_stream_t stream) {
+  if (!valid_weight(head) || x == nullptr || !aligned16(x)) return SDV_ERR_INVALID_ARG;
+  if (argmax == nullptr || accepted == nullptr || next_a0 == nullptr) return SDV_ERR_INVALID_ARG;
+  if (S < 1) return SDV_ERR_INVALID_ARG;
+  if (S > kMaxS) return SDV_ERR_UNSUPPORTED;
+  if (n_valid < 0 || n_valid > S - 1) return SDV_ERR_INVALID_ARG;
+  if (n_valid > 0 && drafts == nullptr) return SDV_ERR_INVALID_ARG;
+  const size_t need = sdv_workspace_bytes(SDV_OP_VERIFY_HEAD, head->n, head->k, S, 0, 0);
+  if (ws == nullptr || !aligned16(ws) || ws_bytes < need) return SDV_ERR_WORKSPACE;
+  const int grid = gemm_grid(head->n);
+  GemmArgs a{};
+  a.y = logits_or_null;
+  a.drafts = drafts;
+  a.n_valid = n_valid;
+  a.argmax = argmax;
+  a.accepted = accepted;
+  a.next_a0 = next_a0;
+  a.part_v = reinterpret_cast<float*>(static_cast<char*>(ws) + kWsHeader);
+  a.part_i = reinterpret_cast<int*>(static_cast<char*>(ws) + kWsHeader + (size_t)grid * S * 4);
+  return run_gemm(head, x, S, sdv::kModeHead, a, ws, reinterpret_cast<cudaStream_t>(stream));
+}
+
+sdv_status sdv_greedy_accept(const int32_t* argmax, int32_t S, const int32_t* drafts, int32_t n_valid,
+                             int32_t* accepted, int32_t* next_a0, sdv_stream_t stream) {
+  if (argmax == nullptr || accepted == nullptr || next_a0 == nullptr) return SDV_ERR_INVALID_ARG;
+  if (S < 1 || n_valid < 0 || n_valid > S - 1) return SDV_ERR_INVALID_ARG;
+  if (n_valid > 0 && drafts == nullptr) return SDV_ERR_INVALID_ARG;
+  return cuda_status(sdv::launch_greedy_accept(argmax, S, drafts, n_valid, accepted, next_a0,
+                                               reinterpret_cast<cudaStream_t>(stream)));
+}
+
+sdv_status sdv_qlinear_swiglu(const sdv_qweight* gate, const sdv_qweight* up, const uint16_t* x,
+                              int32_t S, uint16_t* h, void* ws, size_t ws_bytes, sdv_stream_t stream) {
+  (void)gate; (void)up; (void)x; (void)S; (void)h; (void)ws; (void)ws_bytes; (void)stream;
+  return SDV_ERR_UNSUPPORTED;
+}
+
+sdv_status sdv_moe_gather_qmm(const sdv_qweight* gate, const sdv_qweight* up, const sdv_qweight* down,
+                              int32_t E, int32_t I, int32_t H, int32_t top_k, const uint16_t* x,
+                              const float* router_logits, int32_t S, float* out,
+                              int32_t* topk_ids_or_null, float* topk_w_or_null, void* ws,
+                              size_t ws_bytes, sdv_stream_t stream) {
+  (void)gate; (void)up; (void)down; (void)E; (void)I; (void)H; (void)top_k; (void)x;
+  (void)router_logits; (void)S; (void)out; (void)topk_ids_or_null; (void)topk_w_or_null; (void)ws;
+  (void)ws_bytes; (void)stream;
+  return SDV_ERR_UNSUPPORTED;
+}
+
+}  // extern "C"

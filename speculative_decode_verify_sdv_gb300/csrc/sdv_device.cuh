@@ -1,0 +1,163 @@
+// Device-side building blocks shared by the libsdv kernels: mbarriers, TMA
+// (cp.async.bulk.tensor) loads with bounded waits, exact integer-code -> fp16
+// conversions, the m16n8k16 tensor-core MMA and the (value, index) argmax order.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_fp16.h>
+
+namespace sdv {
+
+// Device status word bits (first word of every workspace).
+constexpr int kDevErrTimeout = 1;
+
+// Give up on an asynchronous copy after this long (nanoseconds).
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t global_timer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_barrier_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Wait for phase `parity` of an mbarrier, giving up after `limit_ns`.
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
+                                                  uint64_t limit_ns = kWaitLimitNs) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  for (;;) {
+#pragma unroll 1
+    for (int i = 0; i < 32; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (global_timer_ns() - t0 > limit_ns) return false;
+  }
+}
+
+// L2 policy for data read exactly once (weights): evict first.
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+__device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(map) : "memory");
+}
+
+// 2-D tiled TMA load of the box at (x = inner element, y = row) into shared
+// memory, completing on `bar` (transaction bytes).
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y,
+                                            uint32_t bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+      "l"(map), "r"(x), "r"(y), "r"(bar), "l"(policy)
+      : "memory");
+}
+
+__device__ __forceinline__ uint2 lds64(uint32_t addr) {
+  uint2 v;
+  asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
+  return v;
+}
+__device__ __forceinline__ uint32_t lds32(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr));
+  return v;
+}
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(addr));
+  return v;
+}
+
+__device__ __forceinline__ uint32_t h2_as_u32(__half2 h) { return *reinterpret_cast<uint32_t*>(&h); }
+__device__ __forceinline__ __half2 u32_as_h2(uint32_t u) { return *reinterpret_cast<__half2*>(&u); }
+
+// Four signed int8 codes e0..e3 (e0 in bits 0-7) -> exact fp16 pairs
+// lo = (e0, e2), hi = (e1, e3).  Each byte, xor 0x80, is placed in the mantissa
+// of 1024 (1024 + e + 128 is exact for e in [-128, 127]) and the bias removed.
+__device__ __forceinline__ void i8x4_to_h2x2(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  const __half2 bias = u32_as_h2(0x64806480u);  // (1152, 1152)
+  const uint32_t t0 = (w & 0x00FF00FFu) ^ 0x64806480u;
+  const uint32_t t1 = ((w >> 8) & 0x00FF00FFu) ^ 0x64806480u;
+  lo = h2_as_u32(__hsub2(u32_as_h2(t0), bias));
+  hi = h2_as_u32(__hsub2(u32_as_h2(t1), bias));
+}
+
+// Eight signed int4 codes n0..n7 (n0 in bits 0-3) -> exact fp16 pairs
+// p0 = (n0, n4), p1 = (n1, n5), p2 = (n2, n6), p3 = (n3, n7).
+// Nibbles at bits 0-3 of each 16-bit half land as 1024 + (n + 8); nibbles at
+// bits 4-7 land as 1024 + 16 (n + 8) and are rescaled by 1/16 (exact).
+__device__ __forceinline__ void i4x8_to_h2x4(uint32_t w, uint32_t& p0, uint32_t& p1, uint32_t& p2,
+                                             uint32_t& p3) {
+  const __half2 b_lo = u32_as_h2(0x64086408u);       // (1032, 1032)
+  const __half2 sixteenth = u32_as_h2(0x2C002C00u);  // (1/16, 1/16)
+  const __half2 b_hi = u32_as_h2(0xD480D480u);       // (-72, -72)
+  const uint32_t y = w >> 8;
+  const uint32_t t0 = (w & 0x000F000Fu) ^ 0x64086408u;
+  const uint32_t t1 = (w & 0x00F000F0u) ^ 0x64806480u;
+  const uint32_t t2 = (y & 0x000F000Fu) ^ 0x64086408u;
+  const uint32_t t3 = (y & 0x00F000F0u) ^ 0x64806480u;
+  p0 = h2_as_u32(__hsub2(u32_as_h2(t0), b_lo));
+  p1 = h2_as_u32(__hfma2(u32_as_h2(t1), sixteenth, b_hi));
+  p2 = h2_as_u32(__hsub2(u32_as_h2(t2), b_lo));
+  p3 = h2_as_u32(__hfma2(u32_as_h2(t3), sixteenth, b_hi));
+}
+
+// D = A * B + C, m16n8k16, fp16 inputs, fp32 accumulate.
+__device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                          uint32_t a3, uint32_t b0, uint32_t b1, const float (&c)[4]) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%10,%11,%12,%13};"
+      : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(c[0]), "f"(c[1]), "f"(c[2]),
+        "f"(c[3]));
+}
+
+// Total order for the argmax: larger value first, then lower index.
+__device__ __forceinline__ bool better(float va, int ia, float vb, int ib) {
+  return va > vb || (va == vb && ia < ib);
+}
+
+__device__ __forceinline__ void argmax_merge(float& v, int& i, float ov, int oi) {
+  if (better(ov, oi, v, i)) {
+    v = ov;
+    i = oi;
+  }
+}
+
+}  // namespace sdv

@@ -1,0 +1,47 @@
+// Internal interface between the C-ABI layer (api.cu) and the kernels.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <cstdint>
+
+namespace sdv {
+
+constexpr int kModeY = 0;     // write fp32 Y [S][N]
+constexpr int kModeHead = 1;  // verify head: argmax partials + last-CTA reduce + accept
+
+struct GemmArgs {
+  const __half* x;          // fp16 [S][K]
+  const uint16_t* scales;   // fp16 [N][K/32] (read directly when scales_tma == 0)
+  int S, N, K;              // window rows, weight rows, reduction length
+  int k_begin, k_len;       // reduction range of this launch (k_begin % 256 == 0)
+  int m16_tiles;            // ceil(N / 16)
+  int depth;                // TMA ring stages per warp
+  int scales_tma;           // 1: scales staged by TMA (needs K % 256 == 0)
+  float* y;                 // fp32 [S][N]: Y (kModeY) or optional logits (kModeHead)
+  // verify head
+  const int32_t* drafts;
+  int n_valid;
+  int32_t* argmax;
+  int32_t* accepted;
+  int32_t* next_a0;
+  float* part_v;            // [grid][S]
+  int* part_i;              // [grid][S]
+  unsigned* ticket;
+  int* status;
+};
+
+int gemm_tile_mt(int qbits);
+int gemm_smem_bytes(int qbits, int S, int k_len, int depth);
+int gemm_warps_per_cta();
+cudaError_t launch_dq_gemm(int qbits, int mode, const CUtensorMap& tm_codes,
+                           const CUtensorMap& tm_scales, const GemmArgs& a, int grid, int smem,
+                           cudaStream_t st);
+
+cudaError_t launch_quantize(const float* w, int n, int k, int qbits, void* codes, uint16_t* scales,
+                            cudaStream_t st);
+cudaError_t launch_greedy_accept(const int32_t* argmax, int S, const int32_t* drafts, int n_valid,
+                                 int32_t* accepted, int32_t* next_a0, cudaStream_t st);
+
+}  // namespace sdv

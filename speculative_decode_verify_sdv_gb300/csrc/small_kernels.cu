@@ -1,0 +1,85 @@
+// Small kernels of the verify path: the per-block-32 quantiser and the
+// stand-alone greedy accept.
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "sdv_kernels.h"
+
+namespace sdv {
+
+namespace {
+
+// One warp per block of 32 weights ("Riding Apple's pipelined GPU engine",
+// section "Quantization on the GPU delegate": per-block-32 absmax symmetric).
+// s32 = max|w| / Q (IEEE fp32 division), s16 = fp16(s32) round-to-nearest-even,
+// q = clamp(rint(w / s16), -Q, Q) with rint ties-to-even; s16 == 0 gives q = 0.
+template <int QB>
+__global__ void quantize_block32_kernel(const float* __restrict__ w, long nblocks, int k,
+                                        uint8_t* __restrict__ codes, __half* __restrict__ scales) {
+  constexpr float kQ = (QB == 8) ? 127.f : 7.f;
+  const int lane = threadIdx.x & 31;
+  const long warps = (long)gridDim.x * (blockDim.x >> 5);
+  const int kb = k / 32;
+  for (long b = (long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); b < nblocks; b += warps) {
+    const long row = b / kb, blk = b - row * kb;
+    const float v = w[row * k + blk * 32 + lane];
+    float m = fabsf(v);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+    const __half s16 = __float2half_rn(__fdiv_rn(m, kQ));
+    const float sf = __half2float(s16);
+    int q = 0;
+    if (sf != 0.f) {
+      const float r = rintf(__fdiv_rn(v, sf));
+      q = (int)fminf(fmaxf(r, -kQ), kQ);
+    }
+    if (QB == 8) {
+      codes[row * k + blk * 32 + lane] = (uint8_t)(int8_t)q;
+    } else {
+      const int hi = __shfl_down_sync(0xffffffffu, q, 1);
+      if ((lane & 1) == 0)
+        codes[row * (k / 2) + blk * 16 + lane / 2] = (uint8_t)((q & 0xF) | ((hi & 0xF) << 4));
+    }
+    if (lane == 0) scales[row * kb + blk] = s16;
+  }
+}
+
+// Greedy longest-prefix accept ("Stream C -- Speculative decoding: feasibility
+// verdict + implementation plan", section "The delta"): accept d_i while
+// d_i == argmax[i] for i < n_valid; the next a0 is argmax[accepted].
+__global__ void greedy_accept_kernel(const int32_t* __restrict__ argmax, const int32_t* __restrict__ drafts,
+                                     int n_valid, int32_t* accepted, int32_t* next_a0) {
+  if (threadIdx.x != 0) return;
+  int j = 0;
+  while (j < n_valid && drafts[j] == argmax[j]) ++j;
+  *accepted = j;
+  *next_a0 = argmax[j];
+}
+
+}  // namespace
+
+cudaError_t launch_quantize(const float* w, int n, int k, int qbits, void* codes, uint16_t* scales,
+                            cudaStream_t st) {
+  const long nblocks = (long)n * (k / 32);
+  const int threads = 256;
+  long grid = (nblocks + 7) / 8;
+  if (grid > 65535L * 16) grid = 65535L * 16;
+  if (qbits == 8)
+    quantize_block32_kernel<8><<<(unsigned)grid, threads, 0, st>>>(
+        w, nblocks, k, static_cast<uint8_t*>(codes), reinterpret_cast<__half*>(scales));
+  else
+    quantize_block32_kernel<4><<<(unsigned)grid, threads, 0, st>>>(
+        w, nblocks, k, static_cast<uint8_t*>(codes), reinterpret_cast<__half*>(scales));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_greedy_accept(const int32_t* argmax, int S, const int32_t* drafts, int n_valid,
+                                 int32_t* accepted, int32_t* next_a0, cudaStream_t st) {
+  (void)S;
+  greedy_accept_kernel<<<1, 32, 0, st>>>(argmax, drafts, n_valid, accepted, next_a0);
+  return cudaGetLastError();
+}
+
+}  // namespace sdv

@@ -1,0 +1,208 @@
+"""Thin Python binding of libsdv (include/sdv.h): argument marshalling only.
+
+Every function has the name of the C entry point it calls and takes torch
+tensors where the C function takes device pointers.  All arithmetic happens
+in the library's CUDA kernels; there is no Python or CPU fallback: if the
+shared library is missing or a GPU is absent the calls raise.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libsdv.so")
+
+SDV_OK, SDV_ERR_INVALID_ARG, SDV_ERR_UNSUPPORTED, SDV_ERR_CUDA, SDV_ERR_TIMEOUT, SDV_ERR_WORKSPACE = range(6)
+SDV_Q8, SDV_Q4 = 8, 4
+SDV_OP_QLINEAR, SDV_OP_QLINEAR_SWIGLU, SDV_OP_VERIFY_HEAD, SDV_OP_MOE = 1, 2, 3, 4
+
+EXPORTED = (
+    "sdv_quantize_block32", "sdv_qlinear", "sdv_qlinear_swiglu", "sdv_verify_head",
+    "sdv_greedy_accept", "sdv_moe_gather_qmm", "sdv_workspace_bytes", "sdv_workspace_init",
+    "sdv_device_status", "sdv_status_string", "sdv_version",
+)
+
+
+class SdvError(RuntimeError):
+    def __init__(self, fn: str, status: int, text: str):
+        super().__init__(f"{fn} failed: {text} ({status})")
+        self.status = status
+
+
+class sdv_qweight(ctypes.Structure):
+    _fields_ = [("qtype", ctypes.c_int32), ("n", ctypes.c_int32), ("k", ctypes.c_int32),
+                ("codes", ctypes.c_void_p), ("scales", ctypes.c_void_p)]
+
+
+_lib = None
+
+
+def load() -> ctypes.CDLL:
+    """Load libsdv.so (built in-tree by ``build.build()``); raise if absent."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(f"libsdv.so not found at {LIB_PATH}; run __graft_entry__.build() first")
+    lib = ctypes.CDLL(LIB_PATH)
+    vp, i32, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_size_t
+    qw = ctypes.POINTER(sdv_qweight)
+    sig = {
+        "sdv_quantize_block32": ([vp, i32, i32, i32, vp, vp, vp], i32),
+        "sdv_qlinear": ([qw, vp, i32, vp, vp, sz, vp], i32),
+        "sdv_qlinear_swiglu": ([qw, qw, vp, i32, vp, vp, sz, vp], i32),
+        "sdv_verify_head": ([qw, vp, i32, vp, i32, vp, vp, vp, vp, vp, sz, vp], i32),
+        "sdv_greedy_accept": ([vp, i32, vp, i32, vp, vp, vp], i32),
+        "sdv_moe_gather_qmm": ([qw, qw, qw, i32, i32, i32, i32, vp, vp, i32, vp, vp, vp, vp, sz, vp], i32),
+        "sdv_workspace_bytes": ([i32, i32, i32, i32, i32, i32], sz),
+        "sdv_workspace_init": ([vp, sz, vp], i32),
+        "sdv_device_status": ([vp, vp], i32),
+        "sdv_status_string": ([i32], ctypes.c_char_p),
+        "sdv_version": ([], i32),
+    }
+    for name, (args, res) in sig.items():
+        f = getattr(lib, name)
+        f.argtypes = args
+        f.restype = res
+    _lib = lib
+    return lib
+
+
+def _check(fn: str, status: int) -> None:
+    if status != SDV_OK:
+        raise SdvError(fn, status, load().sdv_status_string(status).decode())
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("expected a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError("expected a contiguous tensor")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _want(t, dtype, name):
+    if t is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+
+
+def _stream(stream):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+class QWeight:
+    """A per-block-32 quantised weight: codes (int8 [n, k] or uint8 [n, k/2]),
+    fp16 scales [n, k/32], on the GPU."""
+
+    def __init__(self, codes: torch.Tensor, scales: torch.Tensor, bits: int, n: int, k: int):
+        self.codes, self.scales, self.bits, self.n, self.k = codes, scales, bits, n, k
+
+    def c(self) -> sdv_qweight:
+        return sdv_qweight(self.bits, self.n, self.k, _ptr(self.codes), _ptr(self.scales))
+
+
+def sdv_version() -> int:
+    return int(load().sdv_version())
+
+
+def sdv_status_string(status: int) -> str:
+    return load().sdv_status_string(status).decode()
+
+
+def sdv_workspace_bytes(op: int, n: int, k: int, S: int, E: int = 0, top_k: int = 0) -> int:
+    return int(load().sdv_workspace_bytes(op, n, k, S, E, top_k))
+
+
+def sdv_workspace_init(ws: torch.Tensor, stream=None) -> None:
+    _check("sdv_workspace_init", load().sdv_workspace_init(_ptr(ws), ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def sdv_device_status(ws: torch.Tensor, stream=None) -> int:
+    """Synchronise and return (and clear) the workspace's device status."""
+    return int(load().sdv_device_status(_ptr(ws), _stream(stream)))
+
+
+def sdv_quantize_block32(w: torch.Tensor, bits: int, codes: torch.Tensor, scales: torch.Tensor,
+                         stream=None) -> None:
+    _want(w, torch.float32, "w")
+    _want(scales, torch.float16, "scales")
+    n, k = w.shape
+    _check("sdv_quantize_block32", load().sdv_quantize_block32(
+        _ptr(w), n, k, bits, _ptr(codes), _ptr(scales), _stream(stream)))
+
+
+def sdv_qlinear(w: QWeight, x: torch.Tensor, S: int, y: torch.Tensor, ws: torch.Tensor, stream=None) -> None:
+    _want(x, torch.float16, "x")
+    _want(y, torch.float32, "y")
+    cw = w.c()
+    _check("sdv_qlinear", load().sdv_qlinear(ctypes.byref(cw), _ptr(x), S, _ptr(y), _ptr(ws),
+                                             ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def sdv_qlinear_swiglu(gate: QWeight, up: QWeight, x: torch.Tensor, S: int, h: torch.Tensor,
+                       ws: torch.Tensor, stream=None) -> None:
+    _want(x, torch.float16, "x")
+    _want(h, torch.float16, "h")
+    cg, cu = gate.c(), up.c()
+    _check("sdv_qlinear_swiglu", load().sdv_qlinear_swiglu(
+        ctypes.byref(cg), ctypes.byref(cu), _ptr(x), S, _ptr(h), _ptr(ws),
+        ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def sdv_verify_head(head: QWeight, x: torch.Tensor, S: int, drafts, n_valid: int, logits,
+                    argmax: torch.Tensor, accepted: torch.Tensor, next_a0: torch.Tensor,
+                    ws: torch.Tensor, stream=None) -> None:
+    _want(x, torch.float16, "x")
+    _want(drafts, torch.int32, "drafts")
+    _want(logits, torch.float32, "logits")
+    for t, nm in ((argmax, "argmax"), (accepted, "accepted"), (next_a0, "next_a0")):
+        _want(t, torch.int32, nm)
+    cw = head.c()
+    _check("sdv_verify_head", load().sdv_verify_head(
+        ctypes.byref(cw), _ptr(x), S, _ptr(drafts), n_valid, _ptr(logits), _ptr(argmax),
+        _ptr(accepted), _ptr(next_a0), _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def sdv_greedy_accept(argmax: torch.Tensor, S: int, drafts, n_valid: int, accepted: torch.Tensor,
+                      next_a0: torch.Tensor, stream=None) -> None:
+    for t, nm in ((argmax, "argmax"), (drafts, "drafts"), (accepted, "accepted"), (next_a0, "next_a0")):
+        _want(t, torch.int32, nm)
+    _check("sdv_greedy_accept", load().sdv_greedy_accept(
+        _ptr(argmax), S, _ptr(drafts), n_valid, _ptr(accepted), _ptr(next_a0), _stream(stream)))
+
+
+def sdv_moe_gather_qmm(gate: QWeight, up: QWeight, down: QWeight, E: int, I: int, H: int, top_k: int,
+                       x: torch.Tensor, router_logits: torch.Tensor, S: int, out: torch.Tensor,
+                       topk_ids, topk_w, ws: torch.Tensor, stream=None) -> None:
+    _want(x, torch.float16, "x")
+    _want(router_logits, torch.float32, "router_logits")
+    _want(out, torch.float32, "out")
+    cg, cu, cd = gate.c(), up.c(), down.c()
+    _check("sdv_moe_gather_qmm", load().sdv_moe_gather_qmm(
+        ctypes.byref(cg), ctypes.byref(cu), ctypes.byref(cd), E, I, H, top_k, _ptr(x),
+        _ptr(router_logits), S, _ptr(out), _ptr(topk_ids), _ptr(topk_w), _ptr(ws),
+        ws.numel() * ws.element_size(), _stream(stream)))
+
+
+# ---- small allocation helpers (torch owns the memory) ---------------------------
+
+def workspace(op: int, n: int, k: int, S: int, E: int = 0, top_k: int = 0, device="cuda") -> torch.Tensor:
+    """A zero-filled workspace of the size the operation needs."""
+    nbytes = max(sdv_workspace_bytes(op, n, k, S, E, top_k), 256)
+    return torch.zeros(nbytes, dtype=torch.uint8, device=device)
+
+
+def quantize(w: torch.Tensor, bits: int) -> QWeight:
+    """Quantise an fp32 [n, k] CUDA tensor with sdv_quantize_block32."""
+    n, k = w.shape
+    codes = torch.empty((n, k if bits == 8 else k // 2), dtype=torch.int8 if bits == 8 else torch.uint8,
+                        device=w.device)
+    scales = torch.empty((n, k // 32), dtype=torch.float16, device=w.device)
+    sdv_quantize_block32(w.contiguous(), bits, codes, scales)
+    return QWeight(codes, scales, bits, n, k)
