@@ -104,13 +104,49 @@ int pick_depth(int qbits, int S, int k_len, int* smem) {
   return 0;
 }
 
-int gemm_grid(int n) {
-  const int tiles = (n + 15) / 16;
-  const int w = sdv::gemm_warps_per_cta();
-  int grid = (tiles + w - 1) / w;
+struct GemmPlan {
+  int splits = 0, k_chunk = 0, depth = 0, smem = 0, grid = 0;
+};
+
+// Launch plan of the weight-streaming GEMM.  Without split-K (the verify head,
+// whose argmax needs complete logits) one CTA per SM covers the full reduction.
+// With split-K the reduction is cut into 256-multiples until every warp has a
+// few 16-row tiles and the window rows of one split fit in shared memory.
+GemmPlan plan_gemm(int qbits, int n, int k, int S, bool allow_split) {
+  GemmPlan pl;
   const int sms = device_sms();
-  if (grid > sms) grid = sms;
-  return grid < 1 ? 1 : grid;
+  if (sms <= 0) return pl;
+  const int tiles = (n + 15) / 16;
+  const int warps_total = sms * sdv::gemm_warps_per_cta();
+  const int kst = (k + 255) / 256;
+  int splits = 1;
+  if (allow_split) {
+    splits = (4 * warps_total + tiles - 1) / tiles;
+    if (splits > kst) splits = kst;
+    if (splits < 1) splits = 1;
+  }
+  for (;;) {
+    int k_chunk = k;
+    if (splits > 1) {
+      k_chunk = ((k + splits - 1) / splits + 255) / 256 * 256;
+      splits = (k + k_chunk - 1) / k_chunk;
+    }
+    int smem = 0;
+    const int depth = pick_depth(qbits, S, k_chunk, &smem);
+    if (depth >= 3 || (depth == 2 && (!allow_split || splits >= kst))) {
+      pl.splits = splits;
+      pl.k_chunk = k_chunk;
+      pl.depth = depth;
+      pl.smem = smem;
+      int grid = (tiles + sdv::gemm_warps_per_cta() - 1) / sdv::gemm_warps_per_cta();
+      const int per_split = (sms + splits - 1) / splits;
+      if (grid > per_split) grid = per_split;
+      pl.grid = grid < 1 ? 1 : grid;
+      return pl;
+    }
+    if (!allow_split || splits >= kst) return GemmPlan{};
+    ++splits;
+  }
 }
 
 size_t head_ws_bytes(int S) {
@@ -118,31 +154,50 @@ size_t head_ws_bytes(int S) {
   return kWsHeader + (size_t)(sms > 0 ? sms : 1024) * (size_t)S * 8;
 }
 
-// Common part of the weight-streaming GEMM launches.
+size_t qlinear_ws_bytes(int qbits, int n, int k, int S) {
+  const GemmPlan pl = plan_gemm(qbits, n, k, S, true);
+  if (pl.splits == 0) return kWsHeader;
+  return kWsHeader + (pl.splits > 1 ? (size_t)pl.splits * S * n * sizeof(float) : 0);
+}
+
+// Common part of the weight-streaming GEMM launches.  For kModeY the output
+// `y_final` receives Y (through split-K partials in ws when the plan splits).
 sdv_status run_gemm(const sdv_qweight* w, const uint16_t* x, int S, int mode, GemmArgs& a, void* ws,
-                    cudaStream_t st) {
+                    size_t ws_bytes, float* y_final, cudaStream_t st) {
   const int mt = sdv::gemm_tile_mt(w->qtype);
   CUtensorMap tc, tsc;
   int scales_tma = 0;
   sdv_status s = encode_maps(w, mt, &tc, &tsc, &scales_tma);
   if (s != SDV_OK) return s;
-  int smem = 0;
-  const int depth = pick_depth(w->qtype, S, w->k, &smem);
-  if (depth == 0) return SDV_ERR_UNSUPPORTED;
+  const GemmPlan pl = plan_gemm(w->qtype, w->n, w->k, S, mode == sdv::kModeY);
+  if (pl.splits == 0) return SDV_ERR_UNSUPPORTED;
   a.x = reinterpret_cast<const __half*>(x);
   a.scales = w->scales;
   a.S = S;
   a.N = w->n;
   a.K = w->k;
-  a.k_begin = 0;
-  a.k_len = w->k;
+  a.k_chunk = pl.k_chunk;
+  a.splits = pl.splits;
   a.m16_tiles = (w->n + 15) / 16;
-  a.depth = depth;
+  a.depth = pl.depth;
   a.scales_tma = scales_tma;
   a.status = static_cast<int*>(ws);
   a.ticket = reinterpret_cast<unsigned*>(static_cast<char*>(ws) + 4);
-  const int grid = gemm_grid(w->n);
-  return cuda_status(sdv::launch_dq_gemm(w->qtype, mode, tc, tsc, a, grid, smem, st));
+  float* part = nullptr;
+  if (mode == sdv::kModeY) {
+    if (pl.splits > 1) {
+      const size_t need = kWsHeader + (size_t)pl.splits * S * w->n * sizeof(float);
+      if (ws_bytes < need) return SDV_ERR_WORKSPACE;
+      part = reinterpret_cast<float*>(static_cast<char*>(ws) + kWsHeader);
+      a.y = part;
+    } else {
+      a.y = y_final;
+    }
+  }
+  cudaError_t e = sdv::launch_dq_gemm(w->qtype, mode, tc, tsc, a, pl.grid, pl.smem, st);
+  if (e == cudaSuccess && part != nullptr)
+    e = sdv::launch_splitk_reduce(part, pl.splits, (long)S * w->n, y_final, st);
+  return cuda_status(e);
 }
 
 }  // namespace
@@ -167,7 +222,10 @@ size_t sdv_workspace_bytes(int32_t op, int32_t n, int32_t k, int32_t S, int32_t 
   (void)n; (void)k; (void)E; (void)top_k;
   if (S < 1 || S > kMaxS) return 0;
   switch (op) {
-    case SDV_OP_QLINEAR:
+    case SDV_OP_QLINEAR: {  // the larger of the two weight types' plans
+      const size_t a = qlinear_ws_bytes(8, n, k, S), b = qlinear_ws_bytes(4, n, k, S);
+      return a > b ? a : b;
+    }
     case SDV_OP_QLINEAR_SWIGLU: return kWsHeader;
     case SDV_OP_VERIFY_HEAD: return head_ws_bytes(S);
     case SDV_OP_MOE: return kWsHeader;
@@ -208,11 +266,9 @@ sdv_status sdv_qlinear(const sdv_qweight* w, const uint16_t* x, int32_t S, float
   if (!valid_weight(w) || x == nullptr || y == nullptr || !aligned16(x)) return SDV_ERR_INVALID_ARG;
   if (S < 1) return SDV_ERR_INVALID_ARG;
   if (S > kMaxS) return SDV_ERR_UNSUPPORTED;
-  if (ws == nullptr || !aligned16(ws) || ws_bytes < sdv_workspace_bytes(SDV_OP_QLINEAR, w->n, w->k, S, 0, 0))
-    return SDV_ERR_WORKSPACE;
+  if (ws == nullptr || !aligned16(ws) || ws_bytes < kWsHeader) return SDV_ERR_WORKSPACE;
   GemmArgs a{};
-  a.y = y;
-  return run_gemm(w, x, S, sdv::kModeY, a, ws, reinterpret_cast<cudaStream_t>(stream));
+  return run_gemm(w, x, S, sdv::kModeY, a, ws, ws_bytes, y, reinterpret_cast<cudaStream_t>(stream));
 }
 
 sdv_status sdv_verify_head(const sdv_qweight* head, const uint16_t* x, int32_t S, const int32_t* drafts,
@@ -226,7 +282,9 @@ sdv_status sdv_verify_head(const sdv_qweight* head, const uint16_t* x, int32_t S
   if (n_valid > 0 && drafts == nullptr) return SDV_ERR_INVALID_ARG;
   const size_t need = sdv_workspace_bytes(SDV_OP_VERIFY_HEAD, head->n, head->k, S, 0, 0);
   if (ws == nullptr || !aligned16(ws) || ws_bytes < need) return SDV_ERR_WORKSPACE;
-  const int grid = gemm_grid(head->n);
+  const GemmPlan pl = plan_gemm(head->qtype, head->n, head->k, S, false);
+  if (pl.splits == 0) return SDV_ERR_UNSUPPORTED;
+  const int grid = pl.grid;
   GemmArgs a{};
   a.y = logits_or_null;
   a.drafts = drafts;
@@ -236,7 +294,7 @@ sdv_status sdv_verify_head(const sdv_qweight* head, const uint16_t* x, int32_t S
   a.next_a0 = next_a0;
   a.part_v = reinterpret_cast<float*>(static_cast<char*>(ws) + kWsHeader);
   a.part_i = reinterpret_cast<int*>(static_cast<char*>(ws) + kWsHeader + (size_t)grid * S * 4);
-  return run_gemm(head, x, S, sdv::kModeHead, a, ws, reinterpret_cast<cudaStream_t>(stream));
+  return run_gemm(head, x, S, sdv::kModeHead, a, ws, ws_bytes, nullptr, reinterpret_cast<cudaStream_t>(stream));
 }
 
 sdv_status sdv_greedy_accept(const int32_t* argmax, int32_t S, const int32_t* drafts, int32_t n_valid,

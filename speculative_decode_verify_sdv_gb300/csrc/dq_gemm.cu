@@ -43,11 +43,6 @@ namespace {
 constexpr int kWarps = 4;
 constexpr int kStageK = 256;  // reduction elements per stage (8 scale blocks)
 
-__device__ __forceinline__ uint16_t lds16(uint32_t addr) {
-  uint16_t v;
-  asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(addr));
-  return v;
-}
 
 __device__ __forceinline__ void sts128(uint32_t addr, uint4 v) {
   asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z),
@@ -100,12 +95,16 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, c = lane & 3;
-  const SmemPlan sp = make_plan(QB, MT, p.S, p.k_len, p.depth);
+  // reduction range of this CTA (split-K over gridDim.y)
+  const int k_begin = blockIdx.y * p.k_chunk;
+  const int k_len = min(p.k_chunk, p.K - k_begin);
+  const SmemPlan sp = make_plan(QB, MT, p.S, p.k_chunk, p.depth);
   const int depth = sp.depth;
 
   const uint32_t codes_ring = base + sp.codes_off + warp * depth * sp.code_slot;
   const uint32_t sc_ring = base + sp.sc_off + warp * depth * sp.sc_slot;
   const uint32_t xs = base + sp.x_off;
+  const uint8_t* const xsp = sbase + sp.x_off;
   const uint32_t bars = base + sp.bar_off + warp * depth * 8;
   float* const best_v = reinterpret_cast<float*>(sbase + sp.best_off);
   int* const best_i = reinterpret_cast<int*>(sbase + sp.best_off + kWarps * 32 * 4);
@@ -119,10 +118,10 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
   const int tile_hi = (int)((gw + 1) * p.m16_tiles / total_warps);
   const int ntiles = tile_hi - tile_lo;
   const int nunits = (ntiles + MT - 1) / MT;
-  const int kst = (p.k_len + kStageK - 1) / kStageK;
+  const int kst = (k_len + kStageK - 1) / kStageK;
   const int nstages = nunits * kst;
-  const int kbyte0 = (QB == 8) ? p.k_begin : p.k_begin / 2;
-  const int kbyte_end = (QB == 8) ? p.k_begin + p.k_len : (p.k_begin + p.k_len) / 2;
+  const int kbyte0 = (QB == 8) ? k_begin : k_begin / 2;
+  const int kbyte_end = (QB == 8) ? k_begin + k_len : (k_begin + k_len) / 2;
 
   if (lane == 0) {
     for (int d = 0; d < depth; ++d) mbar_init(bars + 8 * d, 1);
@@ -156,7 +155,7 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
           tma_load_2d(cdst + (mt * L::kBoxes + bx) * 2048, &tm_codes, xb + 128 * bx, row0 + mt * 16,
                       bar, policy);
     if (p.scales_tma)
-      tma_load_2d(sc_ring + slot * sp.sc_slot, &tm_scales, p.k_begin / 32 + ks * 8, row0, bar,
+      tma_load_2d(sc_ring + slot * sp.sc_slot, &tm_scales, k_begin / 32 + ks * 8, row0, bar,
                   policy);
   };
 
@@ -168,10 +167,10 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
 
   // ---- stage X (window rows) with the reduction index permuted ---------------
   {
-    const int v8 = p.k_len / 8;
+    const int v8 = k_len / 8;
     for (int v = threadIdx.x; v < p.S * v8; v += blockDim.x) {
       const int s = v / v8, k8 = (v - s * v8) * 8;
-      const uint4 in = *reinterpret_cast<const uint4*>(p.x + (size_t)s * p.K + p.k_begin + k8);
+      const uint4 in = *reinterpret_cast<const uint4*>(p.x + (size_t)s * p.K + k_begin + k8);
       uint4 o;
       if (QB == 8) {  // per 4 elements: (k0, k2, k1, k3)
         o.x = __byte_perm(in.x, in.y, 0x5410);
@@ -189,7 +188,7 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
   }
   __syncthreads();
 
-  const int nblk_total = p.k_len / 32;
+  const int nblk_total = k_len / 32;
   const int ks_per_row = p.K / 32;  // scale entries per weight row
   bool dead = false;
 
@@ -222,73 +221,97 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
         dead = true;
         break;
       }
-      const uint32_t cbase = codes_ring + slot * sp.code_slot;
-      const uint32_t sbase_sc = sc_ring + slot * sp.sc_slot;
+      const uint8_t* const cbase = sbase + (codes_ring - base) + slot * sp.code_slot;
+      const uint8_t* const scbase = sbase + (sc_ring - base) + slot * sp.sc_slot;
       const int nblk = min(8, nblk_total - ks * 8);
-#pragma unroll
-      for (int blk = 0; blk < 8; ++blk) {
-        if (blk >= nblk) break;
-        const int kb = ks * 8 + blk;  // block index within this launch's K range
-        uint4 bf[NT];
+
+      // operands of one 32-block, loaded one block ahead of their use
+      constexpr int AW = (QB == 8) ? 2 : 1;  // 32-bit code words per row per block
+      struct Ops {
+        uint32_t a[MT][2][AW];
+        float s[MT][2];
+        uint4 b[NT];
+      };
+      auto load_ops = [&](int blk, Ops& o) {
+        const int kb = ks * 8 + blk;
 #pragma unroll
         for (int t = 0; t < NT; ++t) {
           const int n = 8 * t + g;
-          if (n < p.S)
-            bf[t] = lds128(xs + n * sp.xpitch + (kb * 32 + 8 * c) * 2);
-          else
-            bf[t] = make_uint4(0u, 0u, 0u, 0u);
+          o.b[t] = (n < p.S) ? *reinterpret_cast<const uint4*>(xsp + n * sp.xpitch + (kb * 32 + 8 * c) * 2)
+                             : make_uint4(0u, 0u, 0u, 0u);
         }
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt) {
-          if (mt >= mt_cnt) break;
-          // codes of rows g and g+8 of tile mt
-          uint32_t a_s0[4], a_s1[4];
-          if (QB == 8) {
-            const int bx = blk >> 2, bb = blk & 3;
-            const uint32_t tb = cbase + (mt * 2 + bx) * 2048;
-            const uint32_t chunk = 2 * bb + (c >> 1);
-            const uint2 wg = lds64(tb + g * 128 + ((chunk ^ g) << 4) + 8 * (c & 1));
-            const uint2 wh = lds64(tb + (g + 8) * 128 + ((chunk ^ g) << 4) + 8 * (c & 1));
-            uint32_t lo, hi, lo8, hi8;
-            i8x4_to_h2x2(wg.x, lo, hi);
-            i8x4_to_h2x2(wh.x, lo8, hi8);
-            a_s0[0] = lo; a_s0[1] = lo8; a_s0[2] = hi; a_s0[3] = hi8;
-            i8x4_to_h2x2(wg.y, lo, hi);
-            i8x4_to_h2x2(wh.y, lo8, hi8);
-            a_s1[0] = lo; a_s1[1] = lo8; a_s1[2] = hi; a_s1[3] = hi8;
-          } else {
-            const uint32_t tb = cbase + mt * 2048;
-            const uint32_t wg = lds32(tb + g * 128 + ((blk ^ g) << 4) + 4 * c);
-            const uint32_t wh = lds32(tb + (g + 8) * 128 + ((blk ^ g) << 4) + 4 * c);
-            uint32_t p0, p1, p2, p3, q0, q1, q2, q3;
-            i4x8_to_h2x4(wg, p0, p1, p2, p3);
-            i4x8_to_h2x4(wh, q0, q1, q2, q3);
-            a_s0[0] = p0; a_s0[1] = q0; a_s0[2] = p1; a_s0[3] = q1;
-            a_s1[0] = p2; a_s1[1] = q2; a_s1[2] = p3; a_s1[3] = q3;
-          }
-          float sg, sh;
-          if (p.scales_tma) {
-            sg = __half2float(__ushort_as_half(lds16(sbase_sc + (mt * 16 + g) * 16 + blk * 2)));
-            sh = __half2float(__ushort_as_half(lds16(sbase_sc + (mt * 16 + g + 8) * 16 + blk * 2)));
-          } else {
-            const int rg = row0 + mt * 16 + g, rh = rg + 8;
-            const int col = p.k_begin / 32 + kb;
-            sg = rg < p.N ? __half2float(__ushort_as_half(__ldg(p.scales + (size_t)rg * ks_per_row + col))) : 0.f;
-            sh = rh < p.N ? __half2float(__ushort_as_half(__ldg(p.scales + (size_t)rh * ks_per_row + col))) : 0.f;
-          }
-          const float zero4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-          for (int t = 0; t < NT; ++t) {
-            if (8 * t >= p.S) break;
-            float tmp[4];
-            mma_16816(tmp, a_s0[0], a_s0[1], a_s0[2], a_s0[3], bf[t].x, bf[t].y, zero4);
-            mma_16816(tmp, a_s1[0], a_s1[1], a_s1[2], a_s1[3], bf[t].z, bf[t].w, tmp);
-            acc[mt][t][0] = fmaf(sg, tmp[0], acc[mt][t][0]);
-            acc[mt][t][1] = fmaf(sg, tmp[1], acc[mt][t][1]);
-            acc[mt][t][2] = fmaf(sh, tmp[2], acc[mt][t][2]);
-            acc[mt][t][3] = fmaf(sh, tmp[3], acc[mt][t][3]);
+          for (int hr = 0; hr < 2; ++hr) {
+            const int r = g + 8 * hr;
+            if (QB == 8) {
+              const int bx = blk >> 2, bb = blk & 3;
+              const int chunk = (2 * bb + (c >> 1)) ^ g;
+              const uint2 w = *reinterpret_cast<const uint2*>(cbase + (mt * 2 + bx) * 2048 + r * 128 +
+                                                              chunk * 16 + 8 * (c & 1));
+              o.a[mt][hr][0] = w.x;
+              o.a[mt][hr][AW - 1] = w.y;
+            } else {
+              o.a[mt][hr][0] = *reinterpret_cast<const uint32_t*>(cbase + mt * 2048 + r * 128 +
+                                                                  ((blk ^ g) << 4) + 4 * c);
+            }
+            if (p.scales_tma) {
+              o.s[mt][hr] = __half2float(*reinterpret_cast<const __half*>(scbase + (mt * 16 + r) * 16 + blk * 2));
+            } else {
+              const int row = row0 + mt * 16 + r;
+              o.s[mt][hr] = row < p.N ? __half2float(__ushort_as_half(__ldg(
+                                            p.scales + (size_t)row * ks_per_row + k_begin / 32 + kb)))
+                                      : 0.f;
+            }
           }
         }
+      };
+      auto compute = [&](const Ops& o) {
+        uint32_t a0[MT][4], a1[MT][4];
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt) {
+          if (QB == 8) {
+            i8x4_to_h2x2(o.a[mt][0][0], a0[mt][0], a0[mt][2]);
+            i8x4_to_h2x2(o.a[mt][1][0], a0[mt][1], a0[mt][3]);
+            i8x4_to_h2x2(o.a[mt][0][AW - 1], a1[mt][0], a1[mt][2]);
+            i8x4_to_h2x2(o.a[mt][1][AW - 1], a1[mt][1], a1[mt][3]);
+          } else {
+            i4x8_to_h2x4(o.a[mt][0][0], a0[mt][0], a0[mt][2], a1[mt][0], a1[mt][2]);
+            i4x8_to_h2x4(o.a[mt][1][0], a0[mt][1], a0[mt][3], a1[mt][1], a1[mt][3]);
+          }
+        }
+        float tmp[MT][NT][4];
+        const float zero4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+          for (int t = 0; t < NT; ++t)
+            mma_16816(tmp[mt][t], a0[mt][0], a0[mt][1], a0[mt][2], a0[mt][3], o.b[t].x, o.b[t].y, zero4);
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+          for (int t = 0; t < NT; ++t)
+            mma_16816(tmp[mt][t], a1[mt][0], a1[mt][1], a1[mt][2], a1[mt][3], o.b[t].z, o.b[t].w, tmp[mt][t]);
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+          for (int t = 0; t < NT; ++t) {
+            acc[mt][t][0] = fmaf(o.s[mt][0], tmp[mt][t][0], acc[mt][t][0]);
+            acc[mt][t][1] = fmaf(o.s[mt][0], tmp[mt][t][1], acc[mt][t][1]);
+            acc[mt][t][2] = fmaf(o.s[mt][1], tmp[mt][t][2], acc[mt][t][2]);
+            acc[mt][t][3] = fmaf(o.s[mt][1], tmp[mt][t][3], acc[mt][t][3]);
+          }
+      };
+
+      Ops cur, nxt;
+      load_ops(0, cur);
+#pragma unroll
+      for (int blk = 0; blk < 8; ++blk) {
+        if (blk >= nblk) break;
+        if (blk + 1 < nblk) load_ops(blk + 1, nxt);
+        compute(cur);
+        cur = nxt;
       }
       __syncwarp();
       if (lane == 0 && i_stage + depth < nstages) issue(i_stage + depth);
@@ -296,7 +319,7 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
     if (dead) break;
 
     // ---- epilogue of this unit -------------------------------------------------
-    float* const yout = p.y;
+    float* const yout = p.y == nullptr ? nullptr : p.y + (size_t)blockIdx.y * p.S * p.N;
     if (yout != nullptr) {
 #pragma unroll
       for (int mt = 0; mt < MT; ++mt) {
@@ -410,7 +433,7 @@ cudaError_t launch_t(const CUtensorMap& tc, const CUtensorMap& tsc, const GemmAr
   auto k = dq_gemm_kernel<QB, NT, MT, MODE>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  k<<<grid, kWarps * 32, smem, st>>>(tc, tsc, a);
+  k<<<dim3(grid, a.splits), kWarps * 32, smem, st>>>(tc, tsc, a);
   return cudaGetLastError();
 }
 
@@ -426,7 +449,24 @@ cudaError_t launch_nt(int nt, const CUtensorMap& tc, const CUtensorMap& tsc, con
   return cudaErrorInvalidValue;
 }
 
+// y[s][n] = sum over splits of part[split][s][n], in split order (deterministic).
+__global__ void splitk_reduce_kernel(const float* __restrict__ part, int splits, long count,
+                                     float* __restrict__ y) {
+  for (long i = (long)blockIdx.x * blockDim.x + threadIdx.x; i < count; i += (long)gridDim.x * blockDim.x) {
+    float v = part[i];
+    for (int sp = 1; sp < splits; ++sp) v += part[(long)sp * count + i];
+    y[i] = v;
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_splitk_reduce(const float* part, int splits, long count, float* y, cudaStream_t st) {
+  long grid = (count + 255) / 256;
+  if (grid > 4096) grid = 4096;
+  splitk_reduce_kernel<<<(unsigned)grid, 256, 0, st>>>(part, splits, count, y);
+  return cudaGetLastError();
+}
 
 int gemm_tile_mt(int qbits) { return qbits == 8 ? 2 : 4; }
 

@@ -15,11 +15,13 @@ struct GemmArgs {
   const __half* x;          // fp16 [S][K]
   const uint16_t* scales;   // fp16 [N][K/32] (read directly when scales_tma == 0)
   int S, N, K;              // window rows, weight rows, reduction length
-  int k_begin, k_len;       // reduction range of this launch (k_begin % 256 == 0)
+  int k_chunk;              // reduction length per split (multiple of 256 unless splits == 1)
+  int splits;               // gridDim.y; split s covers [s * k_chunk, min(K, (s+1) * k_chunk))
   int m16_tiles;            // ceil(N / 16)
   int depth;                // TMA ring stages per warp
   int scales_tma;           // 1: scales staged by TMA (needs K % 256 == 0)
-  float* y;                 // fp32 [S][N]: Y (kModeY) or optional logits (kModeHead)
+  float* y;                 // fp32 [splits][S][N]: Y or its split-K partials (kModeY),
+                            // or the optional logits (kModeHead, splits == 1)
   // verify head
   const int32_t* drafts;
   int n_valid;
@@ -38,6 +40,8 @@ int gemm_warps_per_cta();
 cudaError_t launch_dq_gemm(int qbits, int mode, const CUtensorMap& tm_codes,
                            const CUtensorMap& tm_scales, const GemmArgs& a, int grid, int smem,
                            cudaStream_t st);
+
+cudaError_t launch_splitk_reduce(const float* part, int splits, long count, float* y, cudaStream_t st);
 
 cudaError_t launch_quantize(const float* w, int n, int k, int qbits, void* codes, uint16_t* scales,
                             cudaStream_t st);

@@ -54,7 +54,8 @@ def test_greedy_accept_random_windows(sdv):
 
 @pytest.mark.parametrize("bits", [8, 4])
 @pytest.mark.parametrize("n,k,S", [(5120, 1024, 1), (5120, 1024, 9), (5120, 1024, 17), (777, 288, 5),
-                                   (64, 4096, 32), (17408, 512, 17)])
+                                   (64, 4096, 32), (17408, 512, 17), (300, 8192, 17), (5120, 17408, 17),
+                                   (100, 352, 3)])
 def test_qlinear(sdv, bits, n, k, S):
     w = G.normal(G.stream_seed(910, n, k, bits), (n, k), 0.02)
     codes, scales, stored = oracle_weight(w, bits)
