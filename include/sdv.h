@@ -153,6 +153,30 @@ SDV_API sdv_status sdv_verify_head(const sdv_qweight* head, const uint16_t* x, i
                            void* ws, size_t ws_bytes, sdv_stream_t stream);
 
 /*
+ * sdv_verify_head without a workspace, for callers that cannot allocate device
+ * memory: code that only receives a stream and tensors from a host framework
+ * which owns all device memory and forbids side allocations, or that runs in a
+ * latency-critical loop where cudaMalloc (which may synchronise the device) is
+ * not allowed.  The pages have no counterpart of this entry point.
+ * Same arguments, outputs and definition as sdv_verify_head minus ws/ws_bytes.
+ * Its scratch (status word, last-CTA ticket, per-CTA argmax partials) is a
+ * fixed 65,792-byte device array inside the library, resident on every GPU that
+ * loads the library until the process exits.  Limit: the scratch the call needs
+ * (256 + 8 * S * number-of-SMs bytes) must fit, else SDV_ERR_WORKSPACE; on a
+ * 152-SM GB300 every S <= 32 fits.  The first call on a device looks up the
+ * array's device address (cudaGetSymbolAddress) with that device current, so
+ * make that first call before any stream capture.  Each call clears the
+ * status word and ticket on `stream` first; every call shares the one array, so
+ * calls that overlap on the GPU (other streams, other host threads) race and
+ * must be serialised by the caller.  sdv_device_status does not apply.
+ * Allocates nothing: no cudaMalloc, cudaFree or allocating library routine.
+ */
+SDV_API sdv_status sdv_verify_head_noalloc(const sdv_qweight* head, const uint16_t* x, int32_t S,
+                                   const int32_t* drafts, int32_t n_valid,
+                                   float* logits_or_null, int32_t* argmax, int32_t* accepted,
+                                   int32_t* next_a0, sdv_stream_t stream);
+
+/*
  * The greedy accept rule alone, on a given argmax[S] (device, int32), with the
  * same definition and outputs as sdv_verify_head.  No workspace.
  */

@@ -22,7 +22,7 @@ SDV_OP_QLINEAR, SDV_OP_QLINEAR_SWIGLU, SDV_OP_VERIFY_HEAD, SDV_OP_MOE = 1, 2, 3,
 EXPORTED = (
     "sdv_quantize_block32", "sdv_qlinear", "sdv_qlinear_swiglu", "sdv_verify_head",
     "sdv_greedy_accept", "sdv_moe_gather_qmm", "sdv_workspace_bytes", "sdv_workspace_init",
-    "sdv_device_status", "sdv_status_string", "sdv_version",
+    "sdv_device_status", "sdv_status_string", "sdv_version", "sdv_verify_head_noalloc",
 )
 
 
@@ -55,6 +55,7 @@ def load() -> ctypes.CDLL:
         "sdv_qlinear": ([qw, vp, i32, vp, vp, sz, vp], i32),
         "sdv_qlinear_swiglu": ([qw, qw, vp, i32, vp, vp, sz, vp], i32),
         "sdv_verify_head": ([qw, vp, i32, vp, i32, vp, vp, vp, vp, vp, sz, vp], i32),
+        "sdv_verify_head_noalloc": ([qw, vp, i32, vp, i32, vp, vp, vp, vp, vp], i32),
         "sdv_greedy_accept": ([vp, i32, vp, i32, vp, vp, vp], i32),
         "sdv_moe_gather_qmm": ([qw, qw, qw, i32, i32, i32, i32, vp, vp, i32, vp, vp, vp, vp, sz, vp], i32),
         "sdv_workspace_bytes": ([i32, i32, i32, i32, i32, i32], sz),
@@ -167,6 +168,21 @@ def sdv_verify_head(head: QWeight, x: torch.Tensor, S: int, drafts, n_valid: int
     _check("sdv_verify_head", load().sdv_verify_head(
         ctypes.byref(cw), _ptr(x), S, _ptr(drafts), n_valid, _ptr(logits), _ptr(argmax),
         _ptr(accepted), _ptr(next_a0), _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def sdv_verify_head_noalloc(head: QWeight, x: torch.Tensor, S: int, drafts, n_valid: int, logits,
+                            argmax: torch.Tensor, accepted: torch.Tensor, next_a0: torch.Tensor,
+                            stream=None) -> None:
+    """sdv_verify_head with the library's own fixed device scratch (no workspace)."""
+    _want(x, torch.float16, "x")
+    _want(drafts, torch.int32, "drafts")
+    _want(logits, torch.float32, "logits")
+    for t, nm in ((argmax, "argmax"), (accepted, "accepted"), (next_a0, "next_a0")):
+        _want(t, torch.int32, nm)
+    cw = head.c()
+    _check("sdv_verify_head_noalloc", load().sdv_verify_head_noalloc(
+        ctypes.byref(cw), _ptr(x), S, _ptr(drafts), n_valid, _ptr(logits), _ptr(argmax),
+        _ptr(accepted), _ptr(next_a0), _stream(stream)))
 
 
 def sdv_greedy_accept(argmax: torch.Tensor, S: int, drafts, n_valid: int, accepted: torch.Tensor,
