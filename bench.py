@@ -196,6 +196,7 @@ def run_sdv(args, wl, S, world, rank, local):
 
     build.build()
     sdv.load()
+    sdv.sdv_set_gemm_path({"auto": 0, "mma": 1, "tc": 2, "tc16": 3}[args.path])
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
 
@@ -303,7 +304,7 @@ def run_sdv(args, wl, S, world, rank, local):
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "weight_gbs": achieved, "hbm_frac": achieved / peak,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                     "traffic": None, "peak_kind": kind, "kernel": "dq_gemm_kernel (verify head)",
+                     "traffic": None, "peak_kind": kind, "kernel": f"verify-head GEMM ({args.path} path)",
                      "kernel_ms": kernel_ms},
         "cpu_baseline": {"value": cpu_rate, "unit": "windows/s", "cores": os.cpu_count(), "kind": "oracle",
                          "sample": cpu_desc},
@@ -326,6 +327,8 @@ def main(argv=None):
     ap.add_argument("--S", type=int, default=0)
     ap.add_argument("--windows", type=int, default=200)
     ap.add_argument("--cpu-budget", type=float, default=10.0)
+    ap.add_argument("--path", choices=["auto", "mma", "tc", "tc16"], default="auto",
+                    help="GEMM implementation (auto: tcgen05 where its plan fits)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3

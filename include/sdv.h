@@ -223,6 +223,18 @@ SDV_API sdv_status sdv_workspace_init(void* ws, size_t ws_bytes, sdv_stream_t st
  */
 SDV_API sdv_status sdv_device_status(void* ws, sdv_stream_t stream);
 
+/*
+ * Select the implementation of the weight-streaming GEMM behind sdv_qlinear and
+ * sdv_verify_head (process-wide; for measurement and tests):
+ *   0 = automatic: the tcgen05 path (tensor-memory accumulators, 128-row tiles)
+ *       whenever its shared-memory plan fits, else the mma.sync path;
+ *   1 = the mma.sync path (m16n8k16 tensor-core MMA from registers);
+ *   2 = the tcgen05 path only (SDV_ERR_UNSUPPORTED where its plan does not fit);
+ *   3 = as 2 with twice the converter warps per CTA (16 instead of 8).
+ * Returns the previous selection, or -1 for an invalid value (nothing changes).
+ */
+SDV_API int32_t sdv_set_gemm_path(int32_t path);
+
 /* A static, human-readable name of a status code. */
 SDV_API const char* sdv_status_string(sdv_status status);
 

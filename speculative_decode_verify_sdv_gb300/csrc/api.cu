@@ -6,6 +6,7 @@
 
 #include <cstdint>
 #include <cstring>
+#include <atomic>
 #include <mutex>
 
 #include "sdv.h"
@@ -60,16 +61,17 @@ bool valid_weight(const sdv_qweight* w) {
   return true;
 }
 
-// Codes: uint8 [n][row_bytes], box 128 bytes x 16 rows, 128-byte swizzle.
-// Scales: fp16 [n][k/32], box 8 x (16 * mt) rows (only when k % 256 == 0).
-sdv_status encode_maps(const sdv_qweight* w, int mt, CUtensorMap* tc, CUtensorMap* tsc, int* scales_tma) {
+// Codes: uint8 [n][row_bytes], box 128 bytes x code_rows rows, 128-byte swizzle.
+// Scales: fp16 [n][k/32], box 8 x sc_rows rows (only when k % 256 == 0).
+sdv_status encode_maps(const sdv_qweight* w, int code_rows, int sc_rows, CUtensorMap* tc, CUtensorMap* tsc,
+                       int* scales_tma) {
   auto enc = encode_fn();
   if (enc == nullptr) return SDV_ERR_CUDA;
   const uint64_t row_bytes = (w->qtype == SDV_Q8) ? (uint64_t)w->k : (uint64_t)w->k / 2;
   {
     cuuint64_t dims[2] = {row_bytes, (cuuint64_t)w->n};
     cuuint64_t strides[1] = {row_bytes};
-    cuuint32_t box[2] = {128, 16};
+    cuuint32_t box[2] = {128, (cuuint32_t)code_rows};
     cuuint32_t estr[2] = {1, 1};
     CUresult r = enc(tc, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(w->codes), dims, strides,
                      box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -81,7 +83,7 @@ sdv_status encode_maps(const sdv_qweight* w, int mt, CUtensorMap* tc, CUtensorMa
   if (*scales_tma) {
     cuuint64_t dims[2] = {(cuuint64_t)(w->k / 32), (cuuint64_t)w->n};
     cuuint64_t strides[1] = {(cuuint64_t)(w->k / 32) * 2};
-    cuuint32_t box[2] = {8, (cuuint32_t)(16 * mt)};
+    cuuint32_t box[2] = {8, (cuuint32_t)sc_rows};
     cuuint32_t estr[2] = {1, 1};
     CUresult r = enc(tsc, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<uint16_t*>(w->scales), dims,
                      strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
@@ -106,6 +108,7 @@ int pick_depth(int qbits, int S, int k_len, int* smem) {
 
 struct GemmPlan {
   int splits = 0, k_chunk = 0, depth = 0, smem = 0, grid = 0;
+  bool tc = false;  // tcgen05 path
 };
 
 // Launch plan of the weight-streaming GEMM.  Without split-K (the verify head,
@@ -149,28 +152,95 @@ GemmPlan plan_gemm(int qbits, int n, int k, int S, bool allow_split) {
   }
 }
 
+// GEMM implementation: 0 = choose (tcgen05 when its plan fits), 1 = the
+// mma.sync path, 2 = the tcgen05 path only.
+std::atomic<int> g_gemm_path{0};
+
+// tcgen05 path plan: 128-row tiles, one CTA per SM; split-K (Y only) until the
+// tiles cover the SMs and the window rows of one split fit next to a ring of at
+// least three stages.
+GemmPlan plan_tc(int qbits, int n, int k, int S, bool allow_split) {
+  GemmPlan pl;
+  const int sms = device_sms();
+  const int limit = device_smem_optin();
+  if (sms <= 0 || limit <= 0) return pl;
+  const int tiles = (n + 127) / 128;
+  const int kst = (k + 255) / 256;
+  int splits = 1;
+  if (allow_split) {
+    splits = (sms + tiles - 1) / tiles;
+    if (splits > kst) splits = kst;
+  }
+  for (;;) {
+    int k_chunk = k;
+    if (splits > 1) {
+      k_chunk = ((k + splits - 1) / splits + 255) / 256 * 256;
+      splits = (k + k_chunk - 1) / k_chunk;
+    }
+    for (int d = kMaxDepth; d >= 3; --d) {
+      const int b = sdv::tc_smem_bytes(qbits, S, k_chunk, d);
+      if (b <= limit && sdv::tc_plan_valid(qbits, S, k_chunk, d)) {
+        pl.splits = splits;
+        pl.k_chunk = k_chunk;
+        pl.depth = d;
+        // at least half the SM's shared memory: one CTA (one 512-column tensor
+        // memory allocation) per SM
+        pl.smem = b > limit / 2 + 1024 ? b : limit / 2 + 1024;
+        int grid = (sms + splits - 1) / splits;
+        if (grid > tiles) grid = tiles;
+        pl.grid = grid < 1 ? 1 : grid;
+        pl.tc = true;
+        return pl;
+      }
+    }
+    if (!allow_split || splits >= kst) return GemmPlan{};
+    ++splits;
+  }
+}
+
+GemmPlan choose_plan(int qbits, int n, int k, int S, bool allow_split) {
+  const int path = g_gemm_path.load();
+  if (path != 1) {
+    const GemmPlan t = plan_tc(qbits, n, k, S, allow_split);
+    if (t.splits != 0 || path >= 2) return t;
+  }
+  return plan_gemm(qbits, n, k, S, allow_split);
+}
+
 size_t head_ws_bytes(int S) {
   const int sms = device_sms();
   return kWsHeader + (size_t)(sms > 0 ? sms : 1024) * (size_t)S * 8;
 }
 
 size_t qlinear_ws_bytes(int qbits, int n, int k, int S) {
-  const GemmPlan pl = plan_gemm(qbits, n, k, S, true);
-  if (pl.splits == 0) return kWsHeader;
-  return kWsHeader + (pl.splits > 1 ? (size_t)pl.splits * S * n * sizeof(float) : 0);
+  size_t need = kWsHeader;
+  for (const GemmPlan& pl : {plan_gemm(qbits, n, k, S, true), plan_tc(qbits, n, k, S, true)}) {
+    if (pl.splits > 1) {
+      const size_t b = kWsHeader + (size_t)pl.splits * S * n * sizeof(float);
+      if (b > need) need = b;
+    }
+  }
+  return need;
 }
 
 // Common part of the weight-streaming GEMM launches.  For kModeY the output
 // `y_final` receives Y (through split-K partials in ws when the plan splits).
 sdv_status run_gemm(const sdv_qweight* w, const uint16_t* x, int S, int mode, GemmArgs& a, void* ws,
                     size_t ws_bytes, float* y_final, cudaStream_t st) {
-  const int mt = sdv::gemm_tile_mt(w->qtype);
+  const GemmPlan pl = choose_plan(w->qtype, w->n, w->k, S, mode == sdv::kModeY);
+  if (pl.splits == 0) return SDV_ERR_UNSUPPORTED;
+  if (mode == sdv::kModeHead) {
+    a.part_v = reinterpret_cast<float*>(static_cast<char*>(ws) + kWsHeader);
+    a.part_i = reinterpret_cast<int*>(static_cast<char*>(ws) + kWsHeader + (size_t)pl.grid * S * 4);
+  }
   CUtensorMap tc, tsc;
   int scales_tma = 0;
-  sdv_status s = encode_maps(w, mt, &tc, &tsc, &scales_tma);
+  // box heights: the tcgen05 path moves whole 128-row tiles, the mma.sync path
+  // 16-row tiles (scales for its MT tiles at once)
+  const int code_rows = pl.tc ? 128 : 16;
+  const int sc_rows = pl.tc ? 128 : 16 * sdv::gemm_tile_mt(w->qtype);
+  sdv_status s = encode_maps(w, code_rows, sc_rows, &tc, &tsc, &scales_tma);
   if (s != SDV_OK) return s;
-  const GemmPlan pl = plan_gemm(w->qtype, w->n, w->k, S, mode == sdv::kModeY);
-  if (pl.splits == 0) return SDV_ERR_UNSUPPORTED;
   a.x = reinterpret_cast<const __half*>(x);
   a.scales = w->scales;
   a.S = S;
@@ -194,7 +264,8 @@ sdv_status run_gemm(const sdv_qweight* w, const uint16_t* x, int S, int mode, Ge
       a.y = y_final;
     }
   }
-  cudaError_t e = sdv::launch_dq_gemm(w->qtype, mode, tc, tsc, a, pl.grid, pl.smem, st);
+  cudaError_t e = pl.tc ? sdv::launch_tc_gemm(w->qtype, mode, tc, tsc, a, pl.grid, pl.smem, st)
+                        : sdv::launch_dq_gemm(w->qtype, mode, tc, tsc, a, pl.grid, pl.smem, st);
   if (e == cudaSuccess && part != nullptr)
     e = sdv::launch_splitk_reduce(part, pl.splits, (long)S * w->n, y_final, st);
   return cuda_status(e);
@@ -205,6 +276,12 @@ sdv_status run_gemm(const sdv_qweight* w, const uint16_t* x, int S, int mode, Ge
 extern "C" {
 
 int32_t sdv_version(void) { return 100; }
+
+int32_t sdv_set_gemm_path(int32_t path) {
+  if (path < 0 || path > 3) return -1;
+  sdv::g_tc_groups = path == 3 ? 4 : 2;
+  return g_gemm_path.exchange(path);
+}
 
 const char* sdv_status_string(sdv_status s) {
   switch (s) {
@@ -282,9 +359,6 @@ sdv_status sdv_verify_head(const sdv_qweight* head, const uint16_t* x, int32_t S
   if (n_valid > 0 && drafts == nullptr) return SDV_ERR_INVALID_ARG;
   const size_t need = sdv_workspace_bytes(SDV_OP_VERIFY_HEAD, head->n, head->k, S, 0, 0);
   if (ws == nullptr || !aligned16(ws) || ws_bytes < need) return SDV_ERR_WORKSPACE;
-  const GemmPlan pl = plan_gemm(head->qtype, head->n, head->k, S, false);
-  if (pl.splits == 0) return SDV_ERR_UNSUPPORTED;
-  const int grid = pl.grid;
   GemmArgs a{};
   a.y = logits_or_null;
   a.drafts = drafts;
@@ -292,8 +366,6 @@ sdv_status sdv_verify_head(const sdv_qweight* head, const uint16_t* x, int32_t S
   a.argmax = argmax;
   a.accepted = accepted;
   a.next_a0 = next_a0;
-  a.part_v = reinterpret_cast<float*>(static_cast<char*>(ws) + kWsHeader);
-  a.part_i = reinterpret_cast<int*>(static_cast<char*>(ws) + kWsHeader + (size_t)grid * S * 4);
   return run_gemm(head, x, S, sdv::kModeHead, a, ws, ws_bytes, nullptr, reinterpret_cast<cudaStream_t>(stream));
 }
 

@@ -1,0 +1,512 @@
+// Weight-streaming dequantised skinny GEMM on the 5th-generation tensor cores
+// (tcgen05, tensor memory), sm_103a.
+//
+// Same operation and epilogues as dq_gemm.cu (the verify forward reads every
+// weight byte once for all S window rows: "Stream C -- Speculative decoding:
+// feasibility verdict + implementation plan", section "TL;DR"; per-block-32
+// int8/int4 weights: "Riding Apple's pipelined GPU engine", section
+// "Quantization on the GPU delegate").
+//
+// One CTA per SM, warp roles:
+//   warp 0        TMA producer: 128-row x 256-element stages of codes (128-byte
+//                 swizzled boxes) and their fp16 scales into a shared-memory ring;
+//   warp 1        allocates tensor memory and issues every tcgen05.mma (one
+//                 thread), committing completion to mbarriers;
+//   warps 2-5     tile epilogue, one per tensor-memory lane quarter;
+//   warps 6..     4*G converter warps: group g (warps 6+4g .. 9+4g) converts blocks
+//                 [8g/G, 8(g+1)/G) of every stage; warp w serves tensor-memory lane
+//                 quarter w % 4 (rows 32q..32q+31 of the tile) and each thread owns
+//                 one weight row.  Codes become exact fp16 integers, are multiplied
+//                 by the block's fp16 scale (one rounding: q*s to fp16) and stored
+//                 into tensor memory as the A operand (M = 128 rows, K = 16 per
+//                 MMA).  The window rows are the B operand (N = 16 or 32), staged
+//                 once in shared memory in the K-major core-matrix layout with the
+//                 reduction index permuted like the converted codes.
+//   The MMAs of a 128-row tile accumulate in fp32 tensor memory (double-buffered
+//   across tiles); the epilogue warps load the result (tcgen05.ld) while the next
+//   tile streams and write Y, or reduce the verify head's per-row
+//   (max, lowest index) through shared memory.  The MMA warp runs a
+//   warp-uniform loop and one elected lane issues each MMA.
+// Tensor memory: columns 0-255 hold A (2 stage buffers x 8 blocks x 16 columns),
+// columns 256.. two tile buffers of 4 accumulators (N columns each): the MMAs of
+// a tile rotate over the 4 so that consecutive MMAs do not depend on each other,
+// and the epilogue adds the 4.
+#include <cuda.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include <cfloat>
+#include <climits>
+#include <cstdint>
+
+#include "sdv_device.cuh"
+#include "sdv_kernels.h"
+
+namespace sdv {
+
+namespace {
+
+constexpr int kTileRows = 128;
+constexpr uint32_t kTmemCols = 512;
+constexpr int kAcc = 4;  // independent accumulators per tile (MMA m -> m % kAcc)
+
+template <int G>
+struct TcRoles {
+  static constexpr int kConvWarps = 4 * G;
+  static constexpr int kConv0 = 6;  // first converter warp (0 TMA, 1 MMA, 2-5 epilogue)
+  static constexpr int kWarps = kConv0 + kConvWarps;
+  static constexpr int kThreads = 32 * kWarps;
+  static constexpr int kBlocksPerGroup = 8 / G;
+};
+
+struct TcPlan {
+  int depth, nmma, xrows, code_stage, sc_stage;
+  int x_off, ring_off, sc_off, red_off, bar_off, best_off, misc_off, total;
+};
+
+__host__ __device__ inline int rup(int a, int b) { return (a + b - 1) / b * b; }
+
+__host__ __device__ inline TcPlan tc_plan(int qb, int S, int kc, int depth) {
+  TcPlan p;
+  p.depth = depth;
+  p.nmma = S <= 16 ? 16 : 32;
+  p.xrows = rup(S, 8);
+  p.code_stage = kTileRows * 128 * (qb == 8 ? 2 : 1);
+  p.sc_stage = kTileRows * 16;
+  // The window rows come first: when N exceeds the staged rows, the MMA's reads
+  // of the missing 8-row groups land in the ring and only feed discarded columns.
+  p.x_off = 0;
+  p.ring_off = rup(p.xrows * kc * 2, 1024);
+  p.sc_off = p.ring_off + depth * p.code_stage;
+  p.red_off = p.sc_off + depth * p.sc_stage;           // epilogue: [4 warps][S][33] floats
+  p.bar_off = rup(p.red_off + 4 * S * 33 * 4, 16);
+  p.best_off = p.bar_off + (2 * depth + 2 * 4 * 2 + 4) * 8;
+  p.misc_off = p.best_off + 4 * 32 * 8;
+  p.total = p.misc_off + 32 * 4 + 16;
+  return p;
+}
+
+template <int QB, int MODE, int G>
+__global__ void __launch_bounds__(TcRoles<G>::kThreads, 1)
+    tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_codes,
+                   const __grid_constant__ CUtensorMap tm_scales, const GemmArgs p) {
+  using R = TcRoles<G>;
+  constexpr int BPG = R::kBlocksPerGroup;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_addr(smem_raw);
+  const uint32_t base = (raw_addr + 1023u) & ~1023u;
+  uint8_t* const sb = smem_raw + (base - raw_addr);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int k_begin = blockIdx.y * p.k_chunk;
+  const int k_len = min(p.k_chunk, p.K - k_begin);
+  const TcPlan pl = tc_plan(QB, p.S, p.k_chunk, p.depth);
+  const int depth = pl.depth;
+  const int NM = pl.nmma;
+
+  const uint32_t x_base = base + pl.x_off;
+  const uint32_t ring = base + pl.ring_off;
+  const uint32_t sc_ring = base + pl.sc_off;
+  const uint32_t bars = base + pl.bar_off;
+  const uint32_t bar_full = bars, bar_empty = bars + 8 * depth;
+  const uint32_t bar_afull = bars + 16 * depth;  // [g][buf], g < 4
+  const uint32_t bar_afree = bar_afull + 8 * 8;  // [g][buf]
+  const uint32_t bar_tfull = bar_afree + 8 * 8;  // [tile buf]
+  const uint32_t bar_tfree = bar_tfull + 2 * 8;  // [tile buf]
+  float* const best_v = reinterpret_cast<float*>(sb + pl.best_off);
+  int* const best_i = reinterpret_cast<int*>(sb + pl.best_off + 4 * 32 * 4);
+  uint32_t* const s_tmem = reinterpret_cast<uint32_t*>(sb + pl.misc_off);
+  volatile int* const s_dead = reinterpret_cast<volatile int*>(sb + pl.misc_off + 4);
+  int* const s_flag = reinterpret_cast<int*>(sb + pl.misc_off + 8);
+  int* const s_am = reinterpret_cast<int*>(sb + pl.misc_off + 16);
+
+  // tiles of this CTA and the stage sequence
+  const int tiles = (p.N + kTileRows - 1) / kTileRows;
+  const int tile_lo = (int)((long)blockIdx.x * tiles / gridDim.x);
+  const int tile_hi = (int)((long)(blockIdx.x + 1) * tiles / gridDim.x);
+  const int ntile = tile_hi - tile_lo;
+  const int kst = (k_len + 255) / 256;
+  const int nblk_total = k_len / 32;
+  const int nstages = ntile * kst;
+  const int kbyte0 = (QB == 8) ? k_begin : k_begin / 2;
+  const int kbyte_end = (QB == 8) ? k_begin + k_len : (k_begin + k_len) / 2;
+
+  auto wait = [&](uint32_t bar, uint32_t parity) -> bool {
+    if (*s_dead) return false;
+    if (mbar_wait_bounded(bar, parity)) return true;
+    *s_dead = 1;
+    atomicOr(p.status, kDevErrTimeout);
+    return false;
+  };
+  // all 32 lanes wait (each acquires the phase), then agree, so that the
+  // warp-wide tcgen05.ld / tcgen05.st that follow run converged
+  auto wait_warp = [&](uint32_t bar, uint32_t parity) -> bool {
+    const bool ok = wait(bar, parity);
+    return __all_sync(0xffffffffu, ok) != 0;
+  };
+  auto group_blocks = [&](int i, int g) -> int {  // valid 32-blocks of group g in stage i
+    const int ks = i % kst;
+    return max(0, min(BPG, nblk_total - ks * 8 - BPG * g));
+  };
+  uint64_t policy = 0;
+  auto issue = [&](int i) {  // TMA of stage i into ring slot i % depth
+    const int slot = i % depth;
+    const int t = i / kst, ks = i - (i / kst) * kst;
+    const int row0 = (tile_lo + t) * kTileRows;
+    const int boxes = (QB == 8) ? 2 : 1;
+    const int xb = kbyte0 + ks * 128 * boxes;
+    uint32_t bytes = p.scales_tma ? kTileRows * 16 : 0;
+    for (int bx = 0; bx < boxes; ++bx)
+      if (xb + 128 * bx < kbyte_end) bytes += kTileRows * 128;
+    const uint32_t fb = bar_full + 8 * slot;
+    mbar_arrive_expect_tx(fb, bytes);
+    for (int bx = 0; bx < boxes; ++bx)
+      if (xb + 128 * bx < kbyte_end)
+        tma_load_2d(ring + slot * pl.code_stage + bx * kTileRows * 128, &tm_codes, xb + 128 * bx, row0, fb,
+                    policy);
+    if (p.scales_tma)
+      tma_load_2d(sc_ring + slot * pl.sc_stage, &tm_scales, k_begin / 32 + ks * 8, row0, fb, policy);
+  };
+
+  if (threadIdx.x == 0) {
+    for (int d = 0; d < depth; ++d) {
+      mbar_init(bar_full + 8 * d, 1);
+      mbar_init(bar_empty + 8 * d, R::kConvWarps);
+    }
+    for (int j = 0; j < 8; ++j) {
+      mbar_init(bar_afull + 8 * j, 4);
+      mbar_init(bar_afree + 8 * j, 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(bar_tfull + 8 * b, 1);
+      mbar_init(bar_tfree + 8 * b, 4);
+    }
+    *s_dead = 0;
+    fence_barrier_init();
+    // start streaming weights before the window rows are staged
+    policy = l2_policy_evict_first();
+    tma_prefetch_desc(&tm_codes);
+    if (p.scales_tma) tma_prefetch_desc(&tm_scales);
+    for (int i = 0; i < depth && i < nstages; ++i) issue(i);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_addr(s_tmem), kTmemCols);
+    tmem_relinquish();
+  }
+  if (threadIdx.x < 4 * 32) {
+    best_v[threadIdx.x] = -FLT_MAX;
+    best_i[threadIdx.x] = INT_MAX;
+  }
+
+  // ---- stage the window rows: K-major core matrices (8 rows x 8 elements) -------
+  {
+    const int g8n = k_len / 8;       // 8-element groups along K
+    const int sbo = p.k_chunk * 16;  // bytes between 8-row groups
+    const int total = pl.xrows * g8n;
+#pragma unroll 4
+    for (int v = threadIdx.x; v < total; v += blockDim.x) {
+      const int n = v / g8n, g8 = v - n * g8n;
+      uint4 in = make_uint4(0u, 0u, 0u, 0u);
+      if (n < p.S) in = *reinterpret_cast<const uint4*>(p.x + (size_t)n * p.K + k_begin + 8 * g8);
+      uint4 o;
+      if (QB == 8) {  // per 4 elements: (k0, k2, k1, k3)
+        o.x = __byte_perm(in.x, in.y, 0x5410);
+        o.y = __byte_perm(in.x, in.y, 0x7632);
+        o.z = __byte_perm(in.z, in.w, 0x5410);
+        o.w = __byte_perm(in.z, in.w, 0x7632);
+      } else {  // per 8 elements: (k0, k4, k1, k5, k2, k6, k3, k7)
+        o.x = __byte_perm(in.x, in.z, 0x5410);
+        o.y = __byte_perm(in.x, in.z, 0x7632);
+        o.z = __byte_perm(in.y, in.w, 0x5410);
+        o.w = __byte_perm(in.y, in.w, 0x7632);
+      }
+      *reinterpret_cast<uint4*>(sb + pl.x_off + (n >> 3) * sbo + g8 * 128 + (n & 7) * 16) = o;
+    }
+  }
+  fence_proxy_async_smem();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *s_tmem;
+
+  if (warp == 0) {
+    // ---------------- TMA producer -------------------------------------------------
+    if (lane == 0) {
+      for (int i = depth; i < nstages; ++i) {
+        if (!wait(bar_empty + 8 * (i % depth), ((i / depth) - 1) & 1)) break;
+        issue(i);
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer (warp-uniform loop, one elected lane issues) ------
+    const uint32_t idesc = idesc_f16_f32(kTileRows, NM);
+    const uint32_t sbo = (uint32_t)p.k_chunk * 16u;
+    for (int i = 0; i < nstages; ++i) {
+      const int t = i / kst, ks = i % kst, tb = t & 1;
+      if (ks == 0 && t >= 2 && !wait_warp(bar_tfree + 8 * tb, ((t >> 1) - 1) & 1)) break;
+      const uint32_t d0 = tmem + (uint32_t)(256 + tb * kAcc * NM);
+      bool ok = true;
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        if (!wait_warp(bar_afull + 8 * (2 * g + (i & 1)), (i >> 1) & 1)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const int nb = group_blocks(i, g);
+#pragma unroll
+        for (int blk = 0; blk < BPG; ++blk) {
+          if (blk < nb) {
+#pragma unroll
+            for (int s = 0; s < 2; ++s) {
+              // MMA m of the tile goes to accumulator m % kAcc (independent chains)
+              const int m = ((ks * 8 + BPG * g + blk) << 1) + s;
+              const int k = m * 16;
+              const uint64_t bdesc = smem_desc_kmajor(x_base + (uint32_t)k * 16u, 128u, sbo);
+              const uint32_t a = tmem + (uint32_t)((i & 1) * 128 + (BPG * g + blk) * 16 + s * 8);
+              tc_mma_f16_ta_elect(d0 + (uint32_t)((m & (kAcc - 1)) * NM), a, bdesc, idesc, m >= kAcc ? 1u : 0u);
+            }
+          }
+        }
+        tc_commit_elect(bar_afree + 8 * (2 * g + (i & 1)));
+      }
+      if (!ok) break;
+      if (ks == kst - 1) tc_commit_elect(bar_tfull + 8 * tb);
+    }
+  } else if (warp < R::kConv0) {
+    // ---------------- tile epilogue (one warp per tensor-memory lane quarter) --------
+    const int q = warp & 3;
+    const int r = 32 * q + lane;
+    const uint32_t lane_base = (uint32_t)(32 * q) << 16;
+    float* const red = reinterpret_cast<float*>(sb + pl.red_off) + q * p.S * 33;  // [S][33]
+    float run_v = -FLT_MAX;  // running best of column n = lane
+    int run_i = INT_MAX;
+    const int nacc = min(kAcc, 2 * nblk_total);  // accumulators a tile writes
+    for (int t = 0; t < ntile; ++t) {
+      const int tb = t & 1;
+      if (!wait_warp(bar_tfull + 8 * tb, (t >> 1) & 1)) break;
+      tc_fence_after();
+      float acc[32];
+#pragma unroll
+      for (int n = 0; n < 32; ++n) acc[n] = 0.f;
+#pragma unroll
+      for (int j = 0; j < kAcc; ++j) {
+        if (j < nacc) {
+          const uint32_t col = (uint32_t)(256 + (tb * kAcc + j) * NM);
+          uint32_t v[16];
+          tmem_ld16(tmem + lane_base + col, v);
+          tmem_wait_ld();
+#pragma unroll
+          for (int n = 0; n < 16; ++n) acc[n] += __uint_as_float(v[n]);
+          if (NM == 32) {
+            tmem_ld16(tmem + lane_base + col + 16, v);
+            tmem_wait_ld();
+#pragma unroll
+            for (int n = 0; n < 16; ++n) acc[16 + n] += __uint_as_float(v[n]);
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_tfree + 8 * tb);
+      const int row = (tile_lo + t) * kTileRows + r;
+      const bool valid = row < p.N;
+      if (p.y != nullptr && valid) {
+        float* const yo = p.y + (size_t)blockIdx.y * p.S * p.N;
+#pragma unroll
+        for (int n = 0; n < 32; ++n)
+          if (n < p.S) yo[(size_t)n * p.N + row] = acc[n];
+      }
+      if (MODE == kModeHead) {
+        // columns through shared memory: lane n then scans the warp's 32 rows
+#pragma unroll
+        for (int n = 0; n < 32; ++n)
+          if (n < p.S) red[n * 33 + lane] = valid ? acc[n] : -FLT_MAX;
+        __syncwarp();
+        if (lane < p.S) {
+          const int row0 = (tile_lo + t) * kTileRows + 32 * q;
+          for (int j = 0; j < 32; ++j) {
+            const float v = red[lane * 33 + j];
+            if (row0 + j < p.N) argmax_merge(run_v, run_i, v, row0 + j);
+          }
+        }
+        __syncwarp();
+      }
+    }
+    if (MODE == kModeHead && lane < p.S) {
+      best_v[q * 32 + lane] = run_v;
+      best_i[q * 32 + lane] = run_i;
+    }
+  } else {
+    // ---------------- converters ------------------------------------------------------
+    const int cw = warp - R::kConv0;
+    const int q = warp & 3;
+    const int g = cw >> 2;
+    const int r = 32 * q + lane;  // row within the tile (= TMEM lane)
+    const uint32_t lane_base = (uint32_t)(32 * q) << 16;
+    const int ks_per_row = p.K / 32;
+    for (int i = 0; i < nstages; ++i) {
+      const int slot = i % depth;
+      const int ab = i & 1;
+      const int nb = group_blocks(i, g);
+      bool ok = wait_warp(bar_full + 8 * slot, (i / depth) & 1);
+      if (ok && i >= 2) ok = wait_warp(bar_afree + 8 * (2 * g + ab), ((i >> 1) - 1) & 1);
+      if (ok) {
+        tc_fence_after();
+        const uint8_t* const cb = sb + pl.ring_off + slot * pl.code_stage;
+        const int sw = r & 7;
+        // fp16 scales of this group's blocks (row r)
+        uint32_t sc_h[4];
+        if (p.scales_tma) {
+          const uint8_t* const sp = sb + pl.sc_off + slot * pl.sc_stage + r * 16 + BPG * g * 2;
+          if (BPG == 4) {
+            const uint2 sv = *reinterpret_cast<const uint2*>(sp);
+            sc_h[0] = sv.x & 0xFFFFu; sc_h[1] = sv.x >> 16; sc_h[2] = sv.y & 0xFFFFu; sc_h[3] = sv.y >> 16;
+          } else {
+            const uint32_t sv = *reinterpret_cast<const uint32_t*>(sp);
+            sc_h[0] = sv & 0xFFFFu; sc_h[1] = sv >> 16; sc_h[2] = 0u; sc_h[3] = 0u;
+          }
+        } else {
+          const int row = (tile_lo + i / kst) * kTileRows + r;
+          const int ks = i % kst;
+#pragma unroll
+          for (int blk = 0; blk < 4; ++blk)
+            sc_h[blk] = (blk < nb && row < p.N)
+                            ? (uint32_t)__ldg(p.scales + (size_t)row * ks_per_row + k_begin / 32 + ks * 8 + BPG * g + blk)
+                            : 0u;
+        }
+#pragma unroll
+        for (int blk = 0; blk < BPG; ++blk) {
+          if (blk >= nb) break;
+          const __half2 s2 = u32_as_h2(sc_h[blk] | (sc_h[blk] << 16));
+          const int sblk = BPG * g + blk;  // block within the stage
+          uint32_t cols[16];
+          if (QB == 8) {
+            const uint8_t* const row_p = cb + (sblk >> 2) * kTileRows * 128 + r * 128;
+            const uint4 w0 = *reinterpret_cast<const uint4*>(row_p + (((2 * (sblk & 3)) ^ sw) << 4));
+            const uint4 w1 = *reinterpret_cast<const uint4*>(row_p + (((2 * (sblk & 3) + 1) ^ sw) << 4));
+            const uint32_t wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+#pragma unroll
+            for (int j = 0; j < 8; ++j) i8x4_to_h2x2(wv[j], cols[2 * j], cols[2 * j + 1]);
+          } else {
+            const uint8_t* const row_p = cb + r * 128;
+            const uint4 w = *reinterpret_cast<const uint4*>(row_p + ((sblk ^ sw) << 4));
+            const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              i4x8_to_h2x4(wv[j], cols[4 * j], cols[4 * j + 1], cols[4 * j + 2], cols[4 * j + 3]);
+          }
+#pragma unroll
+          for (int j = 0; j < 16; ++j) cols[j] = h2_as_u32(__hmul2(u32_as_h2(cols[j]), s2));
+          tmem_st16(tmem + lane_base + (uint32_t)(ab * 128 + sblk * 16), cols);
+        }
+        tmem_wait_st();
+        tc_fence_before();
+      }
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(bar_afull + 8 * (2 * g + ab));
+        mbar_arrive(bar_empty + 8 * slot);
+      }
+    }
+  }
+
+  // ---- teardown ------------------------------------------------------------------
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) {
+    __syncwarp();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+
+  if (MODE != kModeHead) return;
+  if (threadIdx.x < p.S) {
+    const int col = threadIdx.x;
+    float bv = best_v[col];
+    int bi = best_i[col];
+    for (int q = 1; q < 4; ++q) argmax_merge(bv, bi, best_v[q * 32 + col], best_i[q * 32 + col]);
+    __stcg(p.part_v + (size_t)blockIdx.x * p.S + col, bv);
+    __stcg(p.part_i + (size_t)blockIdx.x * p.S + col, bi);
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    const unsigned tk = atomicAdd(p.ticket, 1u);
+    *s_flag = (tk == gridDim.x - 1) ? 1 : 0;
+  }
+  __syncthreads();
+  if (*s_flag == 0) return;
+  __threadfence();
+  for (int col = warp; col < p.S; col += R::kWarps) {
+    float bv = -FLT_MAX;
+    int bi = INT_MAX;
+    for (int j = lane; j < (int)gridDim.x; j += 32)
+      argmax_merge(bv, bi, __ldcg(p.part_v + (size_t)j * p.S + col), __ldcg(p.part_i + (size_t)j * p.S + col));
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
+      const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
+      argmax_merge(bv, bi, ov, oi);
+    }
+    if (lane == 0) {
+      s_am[col] = bi;
+      p.argmax[col] = bi;
+    }
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int j = 0;
+    while (j < p.n_valid && p.drafts[j] == s_am[j]) ++j;
+    *p.accepted = j;
+    *p.next_a0 = s_am[j];
+    *p.ticket = 0u;
+  }
+}
+
+template <int QB, int MODE, int G>
+cudaError_t tc_launch_t(const CUtensorMap& tc, const CUtensorMap& tsc, const GemmArgs& a, int grid,
+                        int smem, cudaStream_t st) {
+  auto k = tc_gemm_kernel<QB, MODE, G>;
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  k<<<dim3(grid, a.splits), TcRoles<G>::kThreads, smem, st>>>(tc, tsc, a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+int tc_smem_bytes(int qbits, int S, int k_chunk, int depth) {
+  return tc_plan(qbits, S, k_chunk, depth).total + 1024;
+}
+
+// The aliased 8-row groups of N read up to one group stride past the staged
+// rows; the ring behind them must be at least that long.
+bool tc_plan_valid(int qbits, int S, int k_chunk, int depth) {
+  const TcPlan p = tc_plan(qbits, S, k_chunk, depth);
+  const int ring_bytes = depth * p.code_stage;
+  const int over = (p.nmma - p.xrows) * k_chunk * 2;  // bytes of missing groups
+  return over <= ring_bytes;
+}
+
+// Converter groups per CTA (4 or 8 converter warps ... 16): settable for measurement.
+int g_tc_groups = 2;
+
+cudaError_t launch_tc_gemm(int qbits, int mode, const CUtensorMap& tm_codes, const CUtensorMap& tm_scales,
+                           const GemmArgs& a, int grid, int smem, cudaStream_t st) {
+  const bool head = mode == kModeHead;
+  if (g_tc_groups == 4) {
+    if (qbits == 8)
+      return head ? tc_launch_t<8, kModeHead, 4>(tm_codes, tm_scales, a, grid, smem, st)
+                  : tc_launch_t<8, kModeY, 4>(tm_codes, tm_scales, a, grid, smem, st);
+    return head ? tc_launch_t<4, kModeHead, 4>(tm_codes, tm_scales, a, grid, smem, st)
+                : tc_launch_t<4, kModeY, 4>(tm_codes, tm_scales, a, grid, smem, st);
+  }
+  if (qbits == 8)
+    return head ? tc_launch_t<8, kModeHead, 2>(tm_codes, tm_scales, a, grid, smem, st)
+                : tc_launch_t<8, kModeY, 2>(tm_codes, tm_scales, a, grid, smem, st);
+  return head ? tc_launch_t<4, kModeHead, 2>(tm_codes, tm_scales, a, grid, smem, st)
+              : tc_launch_t<4, kModeY, 2>(tm_codes, tm_scales, a, grid, smem, st);
+}
+
+}  // namespace sdv

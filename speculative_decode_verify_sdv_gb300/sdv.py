@@ -22,7 +22,7 @@ SDV_OP_QLINEAR, SDV_OP_QLINEAR_SWIGLU, SDV_OP_VERIFY_HEAD, SDV_OP_MOE = 1, 2, 3,
 EXPORTED = (
     "sdv_quantize_block32", "sdv_qlinear", "sdv_qlinear_swiglu", "sdv_verify_head",
     "sdv_greedy_accept", "sdv_moe_gather_qmm", "sdv_workspace_bytes", "sdv_workspace_init",
-    "sdv_device_status", "sdv_status_string", "sdv_version", "sdv_verify_head_noalloc",
+    "sdv_device_status", "sdv_status_string", "sdv_version", "sdv_verify_head_noalloc", "sdv_set_gemm_path",
 )
 
 
@@ -63,6 +63,7 @@ def load() -> ctypes.CDLL:
         "sdv_device_status": ([vp, vp], i32),
         "sdv_status_string": ([i32], ctypes.c_char_p),
         "sdv_version": ([], i32),
+        "sdv_set_gemm_path": ([i32], i32),
     }
     for name, (args, res) in sig.items():
         f = getattr(lib, name)
@@ -110,6 +111,17 @@ class QWeight:
 
 def sdv_version() -> int:
     return int(load().sdv_version())
+
+
+SDV_PATH_AUTO, SDV_PATH_MMA_SYNC, SDV_PATH_TCGEN05 = 0, 1, 2
+
+
+def sdv_set_gemm_path(path: int) -> int:
+    """Select the GEMM implementation (0 auto, 1 mma.sync, 2 tcgen05); returns the previous one."""
+    prev = int(load().sdv_set_gemm_path(path))
+    if prev < 0:
+        raise ValueError(f"invalid GEMM path {path}")
+    return prev
 
 
 def sdv_status_string(status: int) -> str:

@@ -67,6 +67,25 @@ def check_head_outputs(ref: dict, am: np.ndarray, acc: int, nxt: int):
     return int(elig.sum())
 
 
+PATHS = {"mma": 1, "tc": 2, "tc16": 3}
+
+
+class gemm_path:
+    """Context manager selecting the GEMM implementation (sdv_set_gemm_path)."""
+
+    def __init__(self, name: str):
+        self.path = PATHS[name] if isinstance(name, str) else int(name)
+
+    def __enter__(self):
+        from speculative_decode_verify_sdv_gb300 import sdv
+        self.prev = sdv.sdv_set_gemm_path(self.path)
+        return self
+
+    def __exit__(self, *a):
+        from speculative_decode_verify_sdv_gb300 import sdv
+        sdv.sdv_set_gemm_path(self.prev)
+
+
 def run_head(head, x: np.ndarray, drafts: np.ndarray, n_valid: int, want_logits=True, ws=None):
     from speculative_decode_verify_sdv_gb300 import sdv
     S = x.shape[0]

@@ -8,7 +8,7 @@ import torch
 
 from oracle import verify
 from synth import generator as G
-from tests.helpers import assert_gemm_close, device_weight, oracle_weight, to_dev, to_dev_f16
+from tests.helpers import assert_gemm_close, device_weight, gemm_path, oracle_weight, to_dev, to_dev_f16
 
 pytestmark = pytest.mark.gpu
 
@@ -19,6 +19,13 @@ def sdv():
     build.build()
     _sdv.load()
     return _sdv
+
+
+@pytest.fixture(params=["mma", "tc", "tc16"])
+def path(request, sdv):
+    """Run the test on each GEMM implementation (mma.sync and tcgen05)."""
+    with gemm_path(request.param):
+        yield request.param
 
 
 def test_greedy_accept_exhaustive_small(sdv):
@@ -56,7 +63,7 @@ def test_greedy_accept_random_windows(sdv):
 @pytest.mark.parametrize("n,k,S", [(5120, 1024, 1), (5120, 1024, 9), (5120, 1024, 17), (777, 288, 5),
                                    (64, 4096, 32), (17408, 512, 17), (300, 8192, 17), (5120, 17408, 17),
                                    (100, 352, 3)])
-def test_qlinear(sdv, bits, n, k, S):
+def test_qlinear(sdv, path, bits, n, k, S):
     w = G.normal(G.stream_seed(910, n, k, bits), (n, k), 0.02)
     codes, scales, stored = oracle_weight(w, bits)
     qw = device_weight(stored, scales, bits, n, k)
@@ -68,7 +75,7 @@ def test_qlinear(sdv, bits, n, k, S):
     assert_gemm_close(y.cpu().numpy(), verify.dequant_gemm(x, codes, scales), k, "Y")
 
 
-def test_qlinear_integer_case_exact(sdv):
+def test_qlinear_integer_case_exact(sdv, path):
     # unit scales, small integer activations: the result is an exact integer GEMM
     n, k, S = 300, 512, 9
     rng = np.random.default_rng(1)

@@ -13,8 +13,8 @@ import torch
 from oracle import quant, verify
 from synth import generator as G
 from synth import workloads as W
-from tests.helpers import (GAP, assert_gemm_close, check_head_outputs, device_weight, oracle_weight,
-                           run_head, to_dev)
+from tests.helpers import (GAP, assert_gemm_close, check_head_outputs, device_weight, gemm_path,
+                           oracle_weight, run_head, to_dev)
 
 pytestmark = pytest.mark.gpu
 
@@ -25,6 +25,18 @@ def sdv():
     build.build()
     _sdv.load()
     return _sdv
+
+
+_CURRENT = {"path": None}
+
+
+@pytest.fixture(params=["mma", "tc", "tc16"])
+def path(request, sdv):
+    """Run the test on each GEMM implementation (mma.sync and tcgen05)."""
+    with gemm_path(request.param):
+        _CURRENT["path"] = request.param
+        yield request.param
+        _CURRENT["path"] = None
 
 
 def _synthetic_head(n, k, bits, seed):
@@ -46,13 +58,18 @@ def _window(sdv, head, codes, scales, x, seed, k):
     drafts[:j] = ref0["argmax"][:j]
     n_valid = S - 1
     ref = verify.verify_head(x, codes, scales, drafts, n_valid)
-    logits, am, acc, nxt = run_head(head, x, drafts, n_valid)
+    try:
+        logits, am, acc, nxt = run_head(head, x, drafts, n_valid)
+    except sdv.SdvError as e:
+        if e.status == sdv.SDV_ERR_UNSUPPORTED and _CURRENT["path"] in ("tc", "tc16"):
+            pytest.skip("window rows x reduction length do not fit the tcgen05 plan")
+        raise
     assert_gemm_close(logits, ref["logits"], k, "logits")
     check_head_outputs(ref, am, acc, nxt)
     return ref, am, acc, nxt
 
 
-def test_tiny_head_all_windows(sdv):
+def test_tiny_head_all_windows(sdv, path):
     wl = W.TINY
     w = W.head_weights(wl)
     codes, scales, stored = oracle_weight(w, 8)
@@ -77,7 +94,7 @@ def test_tiny_head_all_windows(sdv):
 
 @pytest.mark.parametrize("bits", [8, 4])
 @pytest.mark.parametrize("S", [1, 2, 3, 8, 9, 16, 17, 24, 25, 32])
-def test_window_sizes(sdv, bits, S):
+def test_window_sizes(sdv, path, bits, S):
     n, k = 1000, 512
     codes, scales, stored = _synthetic_head(n, k, bits, S)
     head = device_weight(stored, scales, bits, n, k)
@@ -86,14 +103,14 @@ def test_window_sizes(sdv, bits, S):
 
 @pytest.mark.parametrize("bits", [8, 4])
 @pytest.mark.parametrize("n,k", [(1, 32), (17, 64), (4097, 96), (2000, 288), (3001, 800), (640, 2560)])
-def test_ragged_shapes(sdv, bits, n, k):
+def test_ragged_shapes(sdv, path, bits, n, k):
     codes, scales, stored = _synthetic_head(n, k, bits, 1)
     head = device_weight(stored, scales, bits, n, k)
     for S in (1, 9, 17):
         _window(sdv, head, codes, scales, _x(S, k, n + S), n + S, k)
 
 
-def test_planted_ties_and_tail_maximum(sdv):
+def test_planted_ties_and_tail_maximum(sdv, path):
     # rows with identical codes and scales give identical logits: lowest index wins;
     # a dominant row in the last (ragged) tile must be found
     n, k, S = 4099, 256, 9
@@ -118,7 +135,7 @@ def test_planted_ties_and_tail_maximum(sdv):
     assert np.all(ref["argmax"] == 4098) and np.all(am == 4098)
 
 
-def test_accept_paths_on_device(sdv):
+def test_accept_paths_on_device(sdv, path):
     # all drafts equal the argmax -> bonus; first mismatch at 0; pads never accepted
     n, k, S = 2048, 256, 9
     codes, scales, stored = _synthetic_head(n, k, 8, 3)
@@ -143,7 +160,7 @@ def test_accept_paths_on_device(sdv):
     assert acc == 0 and nxt == am_ref[0]
 
 
-def test_workspace_reused_across_calls(sdv):
+def test_workspace_reused_across_calls(sdv, path):
     n, k, S = 3000, 512, 9
     codes, scales, stored = _synthetic_head(n, k, 4, 9)
     head = device_weight(stored, scales, 4, n, k)
@@ -190,10 +207,10 @@ def _full_size(sdv, wl, S, windows):
         assert (acc2, nxt2) == (acc, nxt)
 
 
-def test_full_size_q4b_head(sdv):
+def test_full_size_q4b_head(sdv, path):
     _full_size(sdv, W.Q4B, 9, [0, 1])
 
 
 @pytest.mark.parametrize("S", [1, 2, 9, 17])
-def test_full_size_a3b_head(sdv, S):
+def test_full_size_a3b_head(sdv, path, S):
     _full_size(sdv, W.A3B, S, [0])
