@@ -196,7 +196,7 @@ def run_sdv(args, wl, S, world, rank, local):
 
     build.build()
     sdv.load()
-    sdv.sdv_set_gemm_path({"auto": 0, "mma": 1, "tc": 2, "tc16": 3}[args.path])
+    sdv.sdv_set_gemm_path({"auto": 0, "mma": 1, "tc": 2}[args.path])
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
 
@@ -327,7 +327,7 @@ def main(argv=None):
     ap.add_argument("--S", type=int, default=0)
     ap.add_argument("--windows", type=int, default=200)
     ap.add_argument("--cpu-budget", type=float, default=10.0)
-    ap.add_argument("--path", choices=["auto", "mma", "tc", "tc16"], default="auto",
+    ap.add_argument("--path", choices=["auto", "mma", "tc"], default="auto",
                     help="GEMM implementation (auto: tcgen05 where its plan fits)")
     args = ap.parse_args(argv)
     if args.warmup < 3:

@@ -229,8 +229,7 @@ SDV_API sdv_status sdv_device_status(void* ws, sdv_stream_t stream);
  *   0 = automatic: the tcgen05 path (tensor-memory accumulators, 128-row tiles)
  *       whenever its shared-memory plan fits, else the mma.sync path;
  *   1 = the mma.sync path (m16n8k16 tensor-core MMA from registers);
- *   2 = the tcgen05 path only (SDV_ERR_UNSUPPORTED where its plan does not fit);
- *   3 = as 2 with twice the converter warps per CTA (16 instead of 8).
+ *   2 = the tcgen05 path only (SDV_ERR_UNSUPPORTED where its plan does not fit).
  * Returns the previous selection, or -1 for an invalid value (nothing changes).
  */
 SDV_API int32_t sdv_set_gemm_path(int32_t path);

@@ -278,8 +278,7 @@ extern "C" {
 int32_t sdv_version(void) { return 100; }
 
 int32_t sdv_set_gemm_path(int32_t path) {
-  if (path < 0 || path > 3) return -1;
-  sdv::g_tc_groups = path == 3 ? 4 : 2;
+  if (path < 0 || path > 2) return -1;
   return g_gemm_path.exchange(path);
 }
 

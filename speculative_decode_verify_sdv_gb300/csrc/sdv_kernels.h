@@ -41,7 +41,6 @@ cudaError_t launch_dq_gemm(int qbits, int mode, const CUtensorMap& tm_codes,
                            const CUtensorMap& tm_scales, const GemmArgs& a, int grid, int smem,
                            cudaStream_t st);
 
-extern int g_tc_groups;  // converter warp groups of the tcgen05 path (2 or 4)
 int tc_smem_bytes(int qbits, int S, int k_chunk, int depth);
 bool tc_plan_valid(int qbits, int S, int k_chunk, int depth);
 cudaError_t launch_tc_gemm(int qbits, int mode, const CUtensorMap& tm_codes,

@@ -48,12 +48,13 @@ namespace {
 
 constexpr int kTileRows = 128;
 constexpr uint32_t kTmemCols = 512;
-constexpr int kAcc = 4;  // independent accumulators per tile (MMA m -> m % kAcc)
+constexpr int kABufs = 3;        // A operand stage buffers in tensor memory
+constexpr int kACols = kABufs * 128;
 
-template <int G>
 struct TcRoles {
+  static constexpr int G = 2;                // converter groups (blocks 0-3 / 4-7 of a stage)
   static constexpr int kConvWarps = 4 * G;
-  static constexpr int kConv0 = 6;  // first converter warp (0 TMA, 1 MMA, 2-5 epilogue)
+  static constexpr int kConv0 = 6;           // first converter warp (0 TMA, 1 MMA, 2-5 epilogue)
   static constexpr int kWarps = kConv0 + kConvWarps;
   static constexpr int kThreads = 32 * kWarps;
   static constexpr int kBlocksPerGroup = 8 / G;
@@ -86,12 +87,17 @@ __host__ __device__ inline TcPlan tc_plan(int qb, int S, int kc, int depth) {
   return p;
 }
 
-template <int QB, int MODE, int G>
-__global__ void __launch_bounds__(TcRoles<G>::kThreads, 1)
+template <int QB, int MODE, int NM>
+__global__ void __launch_bounds__(TcRoles::kThreads, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_codes,
                    const __grid_constant__ CUtensorMap tm_scales, const GemmArgs p) {
-  using R = TcRoles<G>;
+  using R = TcRoles;
+  constexpr int G = R::G;
   constexpr int BPG = R::kBlocksPerGroup;
+  // independent fp32 accumulators per tile (MMA m of a stage -> m % kAcc), two
+  // tile buffers, in the tensor-memory columns behind the A buffers
+  constexpr int kAcc = (512 - kACols) / (2 * NM);
+  static_assert(kAcc >= 2 && (kAcc & (kAcc - 1)) == 0, "accumulator count");
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_addr(smem_raw);
   const uint32_t base = (raw_addr + 1023u) & ~1023u;
@@ -102,14 +108,13 @@ __global__ void __launch_bounds__(TcRoles<G>::kThreads, 1)
   const int k_len = min(p.k_chunk, p.K - k_begin);
   const TcPlan pl = tc_plan(QB, p.S, p.k_chunk, p.depth);
   const int depth = pl.depth;
-  const int NM = pl.nmma;
 
   const uint32_t x_base = base + pl.x_off;
   const uint32_t ring = base + pl.ring_off;
   const uint32_t sc_ring = base + pl.sc_off;
   const uint32_t bars = base + pl.bar_off;
   const uint32_t bar_full = bars, bar_empty = bars + 8 * depth;
-  const uint32_t bar_afull = bars + 16 * depth;  // [g][buf], g < 4
+  const uint32_t bar_afull = bars + 16 * depth;  // [g][buf], g < 2, buf < kABufs (8 slots)
   const uint32_t bar_afree = bar_afull + 8 * 8;  // [g][buf]
   const uint32_t bar_tfull = bar_afree + 8 * 8;  // [tile buf]
   const uint32_t bar_tfree = bar_tfull + 2 * 8;  // [tile buf]
@@ -144,15 +149,27 @@ __global__ void __launch_bounds__(TcRoles<G>::kThreads, 1)
     const bool ok = wait(bar, parity);
     return __all_sync(0xffffffffu, ok) != 0;
   };
-  auto group_blocks = [&](int i, int g) -> int {  // valid 32-blocks of group g in stage i
-    const int ks = i % kst;
+  auto group_blocks = [&](int ks, int g) -> int {  // valid 32-blocks of group g at stage column ks
     return max(0, min(BPG, nblk_total - ks * 8 - BPG * g));
   };
+  // Stage cursor: position i in the stage sequence and its derived indices,
+  // advanced incrementally (no per-stage integer division).
+  struct Cursor {
+    int i, slot, phase, ks, t, ab, abphase;
+  };
+  auto cursor_at = [&](int i) -> Cursor {
+    return Cursor{i, i % depth, (i / depth) & 1, i % kst, i / kst, i % kABufs, (i / kABufs) & 1};
+  };
+  auto advance = [&](Cursor& c) {
+    ++c.i;
+    if (++c.slot == depth) { c.slot = 0; c.phase ^= 1; }
+    if (++c.ks == kst) { c.ks = 0; ++c.t; }
+    if (++c.ab == kABufs) { c.ab = 0; c.abphase ^= 1; }
+  };
   uint64_t policy = 0;
-  auto issue = [&](int i) {  // TMA of stage i into ring slot i % depth
-    const int slot = i % depth;
-    const int t = i / kst, ks = i - (i / kst) * kst;
-    const int row0 = (tile_lo + t) * kTileRows;
+  auto issue = [&](const Cursor& c) {  // TMA of stage c.i into ring slot c.slot
+    const int slot = c.slot, ks = c.ks;
+    const int row0 = (tile_lo + c.t) * kTileRows;
     const int boxes = (QB == 8) ? 2 : 1;
     const int xb = kbyte0 + ks * 128 * boxes;
     uint32_t bytes = p.scales_tma ? kTileRows * 16 : 0;
@@ -187,7 +204,8 @@ __global__ void __launch_bounds__(TcRoles<G>::kThreads, 1)
     policy = l2_policy_evict_first();
     tma_prefetch_desc(&tm_codes);
     if (p.scales_tma) tma_prefetch_desc(&tm_scales);
-    for (int i = 0; i < depth && i < nstages; ++i) issue(i);
+    Cursor c = cursor_at(0);
+    for (; c.i < depth && c.i < nstages; advance(c)) issue(c);
   }
   if (warp == 1) {
     tmem_alloc(smem_addr(s_tmem), kTmemCols);
@@ -232,43 +250,49 @@ __global__ void __launch_bounds__(TcRoles<G>::kThreads, 1)
   if (warp == 0) {
     // ---------------- TMA producer -------------------------------------------------
     if (lane == 0) {
-      for (int i = depth; i < nstages; ++i) {
-        if (!wait(bar_empty + 8 * (i % depth), ((i / depth) - 1) & 1)) break;
-        issue(i);
+      for (Cursor c = cursor_at(depth); c.i < nstages; advance(c)) {
+        if (!wait(bar_empty + 8 * c.slot, c.phase ^ 1)) break;
+        issue(c);
       }
     }
   } else if (warp == 1) {
     // ---------------- MMA issuer (warp-uniform loop, one elected lane issues) ------
+    // Per stage: uniform bases, then 16 MMAs at compile-time offsets.
     const uint32_t idesc = idesc_f16_f32(kTileRows, NM);
-    const uint32_t sbo = (uint32_t)p.k_chunk * 16u;
-    for (int i = 0; i < nstages; ++i) {
-      const int t = i / kst, ks = i % kst, tb = t & 1;
+    const uint64_t bdesc0 = smem_desc_kmajor(x_base, 128u, (uint32_t)p.k_chunk * 16u);
+    for (Cursor c = cursor_at(0); c.i < nstages; advance(c)) {
+      const int t = c.t, ks = c.ks, tb = t & 1;
+      const int ab = c.ab;
       if (ks == 0 && t >= 2 && !wait_warp(bar_tfree + 8 * tb, ((t >> 1) - 1) & 1)) break;
-      const uint32_t d0 = tmem + (uint32_t)(256 + tb * kAcc * NM);
+      const uint32_t a_stage = tmem + (uint32_t)(ab * 128);
+      const uint32_t d_tile = tmem + (uint32_t)(kACols + tb * kAcc * NM);
+      // descriptor start address advances by k (16-byte units) per reduction element k
+      const uint64_t b_stage = bdesc0 + (uint64_t)(ks * 256);
+      const bool later = ks > 0;
       bool ok = true;
 #pragma unroll
       for (int g = 0; g < G; ++g) {
-        if (!wait_warp(bar_afull + 8 * (2 * g + (i & 1)), (i >> 1) & 1)) {
+        if (!wait_warp(bar_afull + 8 * (kABufs * g + ab), c.abphase)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        const int nb = group_blocks(i, g);
+        const int nb = group_blocks(ks, g);
 #pragma unroll
         for (int blk = 0; blk < BPG; ++blk) {
           if (blk < nb) {
 #pragma unroll
             for (int s = 0; s < 2; ++s) {
-              // MMA m of the tile goes to accumulator m % kAcc (independent chains)
-              const int m = ((ks * 8 + BPG * g + blk) << 1) + s;
-              const int k = m * 16;
-              const uint64_t bdesc = smem_desc_kmajor(x_base + (uint32_t)k * 16u, 128u, sbo);
-              const uint32_t a = tmem + (uint32_t)((i & 1) * 128 + (BPG * g + blk) * 16 + s * 8);
-              tc_mma_f16_ta_elect(d0 + (uint32_t)((m & (kAcc - 1)) * NM), a, bdesc, idesc, m >= kAcc ? 1u : 0u);
+              const int sblk = BPG * g + blk;          // compile-time
+              const int mloc = 2 * sblk + s;           // compile-time, 0..15
+              tc_mma_f16_ta_elect(d_tile + (uint32_t)((mloc & (kAcc - 1)) * NM),
+                                  a_stage + (uint32_t)(sblk * 16 + s * 8),
+                                  b_stage + (uint64_t)(sblk * 32 + s * 16), idesc,
+                                  (later || mloc >= kAcc) ? 1u : 0u);
             }
           }
         }
-        tc_commit_elect(bar_afree + 8 * (2 * g + (i & 1)));
+        tc_commit_elect(bar_afree + 8 * (kABufs * g + ab));
       }
       if (!ok) break;
       if (ks == kst - 1) tc_commit_elect(bar_tfull + 8 * tb);
@@ -292,7 +316,7 @@ __global__ void __launch_bounds__(TcRoles<G>::kThreads, 1)
 #pragma unroll
       for (int j = 0; j < kAcc; ++j) {
         if (j < nacc) {
-          const uint32_t col = (uint32_t)(256 + (tb * kAcc + j) * NM);
+          const uint32_t col = (uint32_t)(kACols + (tb * kAcc + j) * NM);
           uint32_t v[16];
           tmem_ld16(tmem + lane_base + col, v);
           tmem_wait_ld();
@@ -345,36 +369,44 @@ __global__ void __launch_bounds__(TcRoles<G>::kThreads, 1)
     const int r = 32 * q + lane;  // row within the tile (= TMEM lane)
     const uint32_t lane_base = (uint32_t)(32 * q) << 16;
     const int ks_per_row = p.K / 32;
-    for (int i = 0; i < nstages; ++i) {
-      const int slot = i % depth;
-      const int ab = i & 1;
-      const int nb = group_blocks(i, g);
-      bool ok = wait_warp(bar_full + 8 * slot, (i / depth) & 1);
-      if (ok && i >= 2) ok = wait_warp(bar_afree + 8 * (2 * g + ab), ((i >> 1) - 1) & 1);
+    for (Cursor c = cursor_at(0); c.i < nstages; advance(c)) {
+      const int slot = c.slot;
+      const int ab = c.ab;
+      const int nb = group_blocks(c.ks, g);
+      bool ok = wait_warp(bar_full + 8 * slot, c.phase);
+      // codes and scales of this group's blocks (row r) into registers, then the
+      // ring slot goes back to the producer before the conversion
+      constexpr int kWords = (QB == 8) ? 8 : 4;  // 16-byte chunks per row per group
+      uint4 wreg[kWords];
+      uint32_t sc_h[4] = {0u, 0u, 0u, 0u};
       if (ok) {
-        tc_fence_after();
         const uint8_t* const cb = sb + pl.ring_off + slot * pl.code_stage;
         const int sw = r & 7;
-        // fp16 scales of this group's blocks (row r)
-        uint32_t sc_h[4];
+#pragma unroll
+        for (int c = 0; c < kWords; ++c) {
+          // int8: box g holds this group's 128 bytes; int4: chunks 4g..4g+3 of the one box
+          const int chunk = (QB == 8) ? c : 4 * g + c;
+          const uint8_t* const row_p = cb + ((QB == 8) ? g * kTileRows * 128 : 0) + r * 128;
+          wreg[c] = *reinterpret_cast<const uint4*>(row_p + ((chunk ^ sw) << 4));
+        }
         if (p.scales_tma) {
-          const uint8_t* const sp = sb + pl.sc_off + slot * pl.sc_stage + r * 16 + BPG * g * 2;
-          if (BPG == 4) {
-            const uint2 sv = *reinterpret_cast<const uint2*>(sp);
-            sc_h[0] = sv.x & 0xFFFFu; sc_h[1] = sv.x >> 16; sc_h[2] = sv.y & 0xFFFFu; sc_h[3] = sv.y >> 16;
-          } else {
-            const uint32_t sv = *reinterpret_cast<const uint32_t*>(sp);
-            sc_h[0] = sv & 0xFFFFu; sc_h[1] = sv >> 16; sc_h[2] = 0u; sc_h[3] = 0u;
-          }
+          const uint2 sv = *reinterpret_cast<const uint2*>(sb + pl.sc_off + slot * pl.sc_stage + r * 16 + BPG * g * 2);
+          sc_h[0] = sv.x & 0xFFFFu; sc_h[1] = sv.x >> 16; sc_h[2] = sv.y & 0xFFFFu; sc_h[3] = sv.y >> 16;
         } else {
-          const int row = (tile_lo + i / kst) * kTileRows + r;
-          const int ks = i % kst;
+          const int row = (tile_lo + c.t) * kTileRows + r;
+          const int ks = c.ks;
 #pragma unroll
           for (int blk = 0; blk < 4; ++blk)
             sc_h[blk] = (blk < nb && row < p.N)
                             ? (uint32_t)__ldg(p.scales + (size_t)row * ks_per_row + k_begin / 32 + ks * 8 + BPG * g + blk)
                             : 0u;
         }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_empty + 8 * slot);
+      if (ok && c.i >= kABufs) ok = wait_warp(bar_afree + 8 * (kABufs * g + ab), c.abphase ^ 1);
+      if (ok) {
+        tc_fence_after();
 #pragma unroll
         for (int blk = 0; blk < BPG; ++blk) {
           if (blk >= nb) break;
@@ -382,16 +414,12 @@ __global__ void __launch_bounds__(TcRoles<G>::kThreads, 1)
           const int sblk = BPG * g + blk;  // block within the stage
           uint32_t cols[16];
           if (QB == 8) {
-            const uint8_t* const row_p = cb + (sblk >> 2) * kTileRows * 128 + r * 128;
-            const uint4 w0 = *reinterpret_cast<const uint4*>(row_p + (((2 * (sblk & 3)) ^ sw) << 4));
-            const uint4 w1 = *reinterpret_cast<const uint4*>(row_p + (((2 * (sblk & 3) + 1) ^ sw) << 4));
-            const uint32_t wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+            const uint32_t wv[8] = {wreg[2 * blk].x, wreg[2 * blk].y, wreg[2 * blk].z, wreg[2 * blk].w,
+                                    wreg[2 * blk + 1].x, wreg[2 * blk + 1].y, wreg[2 * blk + 1].z, wreg[2 * blk + 1].w};
 #pragma unroll
             for (int j = 0; j < 8; ++j) i8x4_to_h2x2(wv[j], cols[2 * j], cols[2 * j + 1]);
           } else {
-            const uint8_t* const row_p = cb + r * 128;
-            const uint4 w = *reinterpret_cast<const uint4*>(row_p + ((sblk ^ sw) << 4));
-            const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
+            const uint32_t wv[4] = {wreg[blk].x, wreg[blk].y, wreg[blk].z, wreg[blk].w};
 #pragma unroll
             for (int j = 0; j < 4; ++j)
               i4x8_to_h2x4(wv[j], cols[4 * j], cols[4 * j + 1], cols[4 * j + 2], cols[4 * j + 3]);
@@ -404,10 +432,7 @@ __global__ void __launch_bounds__(TcRoles<G>::kThreads, 1)
         tc_fence_before();
       }
       __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(bar_afull + 8 * (2 * g + ab));
-        mbar_arrive(bar_empty + 8 * slot);
-      }
+      if (lane == 0) mbar_arrive(bar_afull + 8 * (kABufs * g + ab));
     }
   }
 
@@ -464,14 +489,21 @@ __global__ void __launch_bounds__(TcRoles<G>::kThreads, 1)
   }
 }
 
-template <int QB, int MODE, int G>
+template <int QB, int MODE, int NM>
 cudaError_t tc_launch_t(const CUtensorMap& tc, const CUtensorMap& tsc, const GemmArgs& a, int grid,
                         int smem, cudaStream_t st) {
-  auto k = tc_gemm_kernel<QB, MODE, G>;
+  auto k = tc_gemm_kernel<QB, MODE, NM>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  k<<<dim3(grid, a.splits), TcRoles<G>::kThreads, smem, st>>>(tc, tsc, a);
+  k<<<dim3(grid, a.splits), TcRoles::kThreads, smem, st>>>(tc, tsc, a);
   return cudaGetLastError();
+}
+
+template <int QB, int MODE>
+cudaError_t tc_launch_nm(const CUtensorMap& tc, const CUtensorMap& tsc, const GemmArgs& a, int grid,
+                         int smem, cudaStream_t st) {
+  return a.S <= 16 ? tc_launch_t<QB, MODE, 16>(tc, tsc, a, grid, smem, st)
+                   : tc_launch_t<QB, MODE, 32>(tc, tsc, a, grid, smem, st);
 }
 
 }  // namespace
@@ -489,24 +521,14 @@ bool tc_plan_valid(int qbits, int S, int k_chunk, int depth) {
   return over <= ring_bytes;
 }
 
-// Converter groups per CTA (4 or 8 converter warps ... 16): settable for measurement.
-int g_tc_groups = 2;
-
 cudaError_t launch_tc_gemm(int qbits, int mode, const CUtensorMap& tm_codes, const CUtensorMap& tm_scales,
                            const GemmArgs& a, int grid, int smem, cudaStream_t st) {
   const bool head = mode == kModeHead;
-  if (g_tc_groups == 4) {
-    if (qbits == 8)
-      return head ? tc_launch_t<8, kModeHead, 4>(tm_codes, tm_scales, a, grid, smem, st)
-                  : tc_launch_t<8, kModeY, 4>(tm_codes, tm_scales, a, grid, smem, st);
-    return head ? tc_launch_t<4, kModeHead, 4>(tm_codes, tm_scales, a, grid, smem, st)
-                : tc_launch_t<4, kModeY, 4>(tm_codes, tm_scales, a, grid, smem, st);
-  }
   if (qbits == 8)
-    return head ? tc_launch_t<8, kModeHead, 2>(tm_codes, tm_scales, a, grid, smem, st)
-                : tc_launch_t<8, kModeY, 2>(tm_codes, tm_scales, a, grid, smem, st);
-  return head ? tc_launch_t<4, kModeHead, 2>(tm_codes, tm_scales, a, grid, smem, st)
-              : tc_launch_t<4, kModeY, 2>(tm_codes, tm_scales, a, grid, smem, st);
+    return head ? tc_launch_nm<8, kModeHead>(tm_codes, tm_scales, a, grid, smem, st)
+                : tc_launch_nm<8, kModeY>(tm_codes, tm_scales, a, grid, smem, st);
+  return head ? tc_launch_nm<4, kModeHead>(tm_codes, tm_scales, a, grid, smem, st)
+              : tc_launch_nm<4, kModeY>(tm_codes, tm_scales, a, grid, smem, st);
 }
 
 }  // namespace sdv

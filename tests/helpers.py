@@ -67,7 +67,7 @@ def check_head_outputs(ref: dict, am: np.ndarray, acc: int, nxt: int):
     return int(elig.sum())
 
 
-PATHS = {"mma": 1, "tc": 2, "tc16": 3}
+PATHS = {"mma": 1, "tc": 2}
 
 
 class gemm_path:

@@ -21,7 +21,7 @@ def sdv():
     return _sdv
 
 
-@pytest.fixture(params=["mma", "tc", "tc16"])
+@pytest.fixture(params=["mma", "tc"])
 def path(request, sdv):
     """Run the test on each GEMM implementation (mma.sync and tcgen05)."""
     with gemm_path(request.param):
