@@ -323,7 +323,7 @@ sdv_status sdv_device_status(void* ws, sdv_stream_t stream) {
   if (word == 0) return SDV_OK;
   const int zero = 0;
   if (cudaMemcpy(ws, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess) return SDV_ERR_CUDA;
-  return SDV_ERR_TIMEOUT;
+  return (word & sdv::kDevErrTimeout) ? SDV_ERR_TIMEOUT : SDV_ERR_CUDA;
 }
 
 sdv_status sdv_quantize_block32(const float* w, int32_t n, int32_t k, int32_t qtype, void* codes,

@@ -9,9 +9,6 @@
 
 namespace sdv {
 
-// Device status word bits (first word of every workspace).
-constexpr int kDevErrTimeout = 1;
-
 // Give up on an asynchronous copy after this long (nanoseconds).
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 

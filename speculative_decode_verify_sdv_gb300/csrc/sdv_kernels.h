@@ -8,6 +8,10 @@
 
 namespace sdv {
 
+// Device status word bits (first word of every workspace).
+constexpr int kDevErrTimeout = 1;
+constexpr int kDevErrTmemBase = 2;  // tensor-memory allocation not at column 0
+
 constexpr int kModeY = 0;     // write fp32 Y [S][N]
 constexpr int kModeHead = 1;  // verify head: argmax partials + last-CTA reduce + accept
 

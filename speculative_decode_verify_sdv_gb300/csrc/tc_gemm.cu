@@ -61,7 +61,7 @@ struct TcRoles {
 };
 
 struct TcPlan {
-  int depth, nmma, xrows, code_stage, sc_stage;
+  int depth, nmma, xrows, kpad, code_stage, sc_stage;
   int x_off, ring_off, sc_off, red_off, bar_off, best_off, misc_off, total;
 };
 
@@ -72,16 +72,19 @@ __host__ __device__ inline TcPlan tc_plan(int qb, int S, int kc, int depth) {
   p.depth = depth;
   p.nmma = S <= 16 ? 16 : 32;
   p.xrows = rup(S, 8);
+  // window rows are staged zero-padded to whole 256-element stages, so every
+  // stage runs all 16 MMAs (missing code blocks get a zero scale)
+  p.kpad = rup(kc, 256);
   p.code_stage = kTileRows * 128 * (qb == 8 ? 2 : 1);
   p.sc_stage = kTileRows * 16;
   // The window rows come first: when N exceeds the staged rows, the MMA's reads
   // of the missing 8-row groups land in the ring and only feed discarded columns.
   p.x_off = 0;
-  p.ring_off = rup(p.xrows * kc * 2, 1024);
+  p.ring_off = rup(p.xrows * p.kpad * 2, 1024);
   p.sc_off = p.ring_off + depth * p.code_stage;
   p.red_off = p.sc_off + depth * p.sc_stage;           // epilogue: [4 warps][S][33] floats
   p.bar_off = rup(p.red_off + 4 * S * 33 * 4, 16);
-  p.best_off = p.bar_off + (2 * depth + 2 * 4 * 2 + 4) * 8;
+  p.best_off = p.bar_off + (2 * depth + 2 * TcRoles::G * kABufs + 4) * 8;
   p.misc_off = p.best_off + 4 * 32 * 8;
   p.total = p.misc_off + 32 * 4 + 16;
   return p;
@@ -114,9 +117,9 @@ __global__ void __launch_bounds__(TcRoles::kThreads, 1)
   const uint32_t sc_ring = base + pl.sc_off;
   const uint32_t bars = base + pl.bar_off;
   const uint32_t bar_full = bars, bar_empty = bars + 8 * depth;
-  const uint32_t bar_afull = bars + 16 * depth;  // [g][buf], g < 2, buf < kABufs (8 slots)
-  const uint32_t bar_afree = bar_afull + 8 * 8;  // [g][buf]
-  const uint32_t bar_tfull = bar_afree + 8 * 8;  // [tile buf]
+  const uint32_t bar_afull = bars + 16 * depth;            // [g][buf]
+  const uint32_t bar_afree = bar_afull + 8 * G * kABufs;  // [g][buf]
+  const uint32_t bar_tfull = bar_afree + 8 * G * kABufs;  // [tile buf]
   const uint32_t bar_tfree = bar_tfull + 2 * 8;  // [tile buf]
   float* const best_v = reinterpret_cast<float*>(sb + pl.best_off);
   int* const best_i = reinterpret_cast<int*>(sb + pl.best_off + 4 * 32 * 4);
@@ -190,7 +193,7 @@ __global__ void __launch_bounds__(TcRoles::kThreads, 1)
       mbar_init(bar_full + 8 * d, 1);
       mbar_init(bar_empty + 8 * d, R::kConvWarps);
     }
-    for (int j = 0; j < 8; ++j) {
+    for (int j = 0; j < G * kABufs; ++j) {
       mbar_init(bar_afull + 8 * j, 4);
       mbar_init(bar_afree + 8 * j, 1);
     }
@@ -218,14 +221,15 @@ __global__ void __launch_bounds__(TcRoles::kThreads, 1)
 
   // ---- stage the window rows: K-major core matrices (8 rows x 8 elements) -------
   {
-    const int g8n = k_len / 8;       // 8-element groups along K
-    const int sbo = p.k_chunk * 16;  // bytes between 8-row groups
+    const int g8n = kst * 32;         // 8-element groups along K, padded to whole stages
+    const int g8v = k_len / 8;        // groups holding window data
+    const int sbo = pl.kpad * 16;     // bytes between 8-row groups
     const int total = pl.xrows * g8n;
 #pragma unroll 4
     for (int v = threadIdx.x; v < total; v += blockDim.x) {
       const int n = v / g8n, g8 = v - n * g8n;
       uint4 in = make_uint4(0u, 0u, 0u, 0u);
-      if (n < p.S) in = *reinterpret_cast<const uint4*>(p.x + (size_t)n * p.K + k_begin + 8 * g8);
+      if (n < p.S && g8 < g8v) in = *reinterpret_cast<const uint4*>(p.x + (size_t)n * p.K + k_begin + 8 * g8);
       uint4 o;
       if (QB == 8) {  // per 4 elements: (k0, k2, k1, k3)
         o.x = __byte_perm(in.x, in.y, 0x5410);
@@ -245,7 +249,12 @@ __global__ void __launch_bounds__(TcRoles::kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem = *s_tmem;
+  // An allocation of all 512 columns always starts at lane 0, column 0.  Every
+  // tensor-memory address below is built on that constant, so the MMA operands
+  // are warp-uniform expressions of the loop counters (a base loaded from shared
+  // memory is not provably uniform and each MMA would pay to make it so).
+  constexpr uint32_t tmem = 0u;
+  if (threadIdx.x == 0 && *s_tmem != tmem) atomicOr(p.status, kDevErrTmemBase);
 
   if (warp == 0) {
     // ---------------- TMA producer -------------------------------------------------
@@ -259,7 +268,7 @@ __global__ void __launch_bounds__(TcRoles::kThreads, 1)
     // ---------------- MMA issuer (warp-uniform loop, one elected lane issues) ------
     // Per stage: uniform bases, then 16 MMAs at compile-time offsets.
     const uint32_t idesc = idesc_f16_f32(kTileRows, NM);
-    const uint64_t bdesc0 = smem_desc_kmajor(x_base, 128u, (uint32_t)p.k_chunk * 16u);
+    const uint64_t bdesc0 = smem_desc_kmajor(x_base, 128u, (uint32_t)pl.kpad * 16u);
     for (Cursor c = cursor_at(0); c.i < nstages; advance(c)) {
       const int t = c.t, ks = c.ks, tb = t & 1;
       const int ab = c.ab;
@@ -277,19 +286,18 @@ __global__ void __launch_bounds__(TcRoles::kThreads, 1)
           break;
         }
         tc_fence_after();
-        const int nb = group_blocks(ks, g);
+        // straight-line issue: a branch around an elected MMA costs a warp
+        // reconvergence per instruction
 #pragma unroll
         for (int blk = 0; blk < BPG; ++blk) {
-          if (blk < nb) {
 #pragma unroll
-            for (int s = 0; s < 2; ++s) {
-              const int sblk = BPG * g + blk;          // compile-time
-              const int mloc = 2 * sblk + s;           // compile-time, 0..15
-              tc_mma_f16_ta_elect(d_tile + (uint32_t)((mloc & (kAcc - 1)) * NM),
-                                  a_stage + (uint32_t)(sblk * 16 + s * 8),
-                                  b_stage + (uint64_t)(sblk * 32 + s * 16), idesc,
-                                  (later || mloc >= kAcc) ? 1u : 0u);
-            }
+          for (int s = 0; s < 2; ++s) {
+            const int sblk = BPG * g + blk;          // compile-time
+            const int mloc = 2 * sblk + s;           // compile-time, 0..15
+            tc_mma_f16_ta_elect(d_tile + (uint32_t)((mloc & (kAcc - 1)) * NM),
+                                a_stage + (uint32_t)(sblk * 16 + s * 8),
+                                b_stage + (uint64_t)(sblk * 32 + s * 16), idesc,
+                                (later || mloc >= kAcc) ? 1u : 0u);
           }
         }
         tc_commit_elect(bar_afree + 8 * (kABufs * g + ab));
@@ -305,7 +313,6 @@ __global__ void __launch_bounds__(TcRoles::kThreads, 1)
     float* const red = reinterpret_cast<float*>(sb + pl.red_off) + q * p.S * 33;  // [S][33]
     float run_v = -FLT_MAX;  // running best of column n = lane
     int run_i = INT_MAX;
-    const int nacc = min(kAcc, 2 * nblk_total);  // accumulators a tile writes
     for (int t = 0; t < ntile; ++t) {
       const int tb = t & 1;
       if (!wait_warp(bar_tfull + 8 * tb, (t >> 1) & 1)) break;
@@ -315,19 +322,17 @@ __global__ void __launch_bounds__(TcRoles::kThreads, 1)
       for (int n = 0; n < 32; ++n) acc[n] = 0.f;
 #pragma unroll
       for (int j = 0; j < kAcc; ++j) {
-        if (j < nacc) {
-          const uint32_t col = (uint32_t)(kACols + (tb * kAcc + j) * NM);
-          uint32_t v[16];
-          tmem_ld16(tmem + lane_base + col, v);
+        const uint32_t col = (uint32_t)(kACols + (tb * kAcc + j) * NM);
+        uint32_t v[16];
+        tmem_ld16(tmem + lane_base + col, v);
+        tmem_wait_ld();
+#pragma unroll
+        for (int n = 0; n < 16; ++n) acc[n] += __uint_as_float(v[n]);
+        if (NM == 32) {
+          tmem_ld16(tmem + lane_base + col + 16, v);
           tmem_wait_ld();
 #pragma unroll
-          for (int n = 0; n < 16; ++n) acc[n] += __uint_as_float(v[n]);
-          if (NM == 32) {
-            tmem_ld16(tmem + lane_base + col + 16, v);
-            tmem_wait_ld();
-#pragma unroll
-            for (int n = 0; n < 16; ++n) acc[16 + n] += __uint_as_float(v[n]);
-          }
+          for (int n = 0; n < 16; ++n) acc[16 + n] += __uint_as_float(v[n]);
         }
       }
       tc_fence_before();
@@ -376,27 +381,37 @@ __global__ void __launch_bounds__(TcRoles::kThreads, 1)
       bool ok = wait_warp(bar_full + 8 * slot, c.phase);
       // codes and scales of this group's blocks (row r) into registers, then the
       // ring slot goes back to the producer before the conversion
-      constexpr int kWords = (QB == 8) ? 8 : 4;  // 16-byte chunks per row per group
+      constexpr int kBlkBytes = (QB == 8) ? 32 : 16;  // code bytes of one 32-block
+      constexpr int kWords = BPG * kBlkBytes / 16;     // 16-byte chunks per row per group
       uint4 wreg[kWords];
-      uint32_t sc_h[4] = {0u, 0u, 0u, 0u};
+      uint32_t sc_h[BPG];
+#pragma unroll
+      for (int blk = 0; blk < BPG; ++blk) sc_h[blk] = 0u;
       if (ok) {
         const uint8_t* const cb = sb + pl.ring_off + slot * pl.code_stage;
         const int sw = r & 7;
 #pragma unroll
-        for (int c = 0; c < kWords; ++c) {
-          // int8: box g holds this group's 128 bytes; int4: chunks 4g..4g+3 of the one box
-          const int chunk = (QB == 8) ? c : 4 * g + c;
-          const uint8_t* const row_p = cb + ((QB == 8) ? g * kTileRows * 128 : 0) + r * 128;
-          wreg[c] = *reinterpret_cast<const uint4*>(row_p + ((chunk ^ sw) << 4));
+        for (int w = 0; w < kWords; ++w) {
+          // byte offset in the stage row -> 128-byte box and swizzled 16-byte chunk
+          const int byte = BPG * g * kBlkBytes + 16 * w;
+          const int box = byte >> 7, chunk = (byte >> 4) & 7;
+          const uint8_t* const row_p = cb + box * kTileRows * 128 + r * 128;
+          wreg[w] = *reinterpret_cast<const uint4*>(row_p + ((chunk ^ sw) << 4));
         }
         if (p.scales_tma) {
-          const uint2 sv = *reinterpret_cast<const uint2*>(sb + pl.sc_off + slot * pl.sc_stage + r * 16 + BPG * g * 2);
-          sc_h[0] = sv.x & 0xFFFFu; sc_h[1] = sv.x >> 16; sc_h[2] = sv.y & 0xFFFFu; sc_h[3] = sv.y >> 16;
+          const uint8_t* const sp = sb + pl.sc_off + slot * pl.sc_stage + r * 16 + BPG * g * 2;
+          if (BPG == 4) {
+            const uint2 sv = *reinterpret_cast<const uint2*>(sp);
+            sc_h[0] = sv.x & 0xFFFFu; sc_h[1] = sv.x >> 16; sc_h[BPG - 2] = sv.y & 0xFFFFu; sc_h[BPG - 1] = sv.y >> 16;
+          } else {
+            const uint32_t sv = *reinterpret_cast<const uint32_t*>(sp);
+            sc_h[0] = sv & 0xFFFFu; sc_h[BPG - 1] = sv >> 16;
+          }
         } else {
           const int row = (tile_lo + c.t) * kTileRows + r;
           const int ks = c.ks;
 #pragma unroll
-          for (int blk = 0; blk < 4; ++blk)
+          for (int blk = 0; blk < BPG; ++blk)
             sc_h[blk] = (blk < nb && row < p.N)
                             ? (uint32_t)__ldg(p.scales + (size_t)row * ks_per_row + k_begin / 32 + ks * 8 + BPG * g + blk)
                             : 0u;
@@ -409,7 +424,8 @@ __global__ void __launch_bounds__(TcRoles::kThreads, 1)
         tc_fence_after();
 #pragma unroll
         for (int blk = 0; blk < BPG; ++blk) {
-          if (blk >= nb) break;
+          // blocks past the reduction length (blk >= nb) have a zero scale: their
+          // A columns are zero, and the padded window rows are zero too
           const __half2 s2 = u32_as_h2(sc_h[blk] | (sc_h[blk] << 16));
           const int sblk = BPG * g + blk;  // block within the stage
           uint32_t cols[16];
