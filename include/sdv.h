@@ -205,6 +205,23 @@ SDV_API sdv_status sdv_moe_gather_qmm(const sdv_qweight* gate, const sdv_qweight
                               sdv_stream_t stream);
 
 /*
+ * The MoE routing and grouping steps alone (the first launch of
+ * sdv_moe_gather_qmm), for inspection and parity tests:
+ *   ids, weights: int32 / fp32 [S][top_k], per row the top_k experts by
+ *     router_logits (larger first, ties to the lower id) and their softmax over
+ *     the selection;
+ *   offsets: int32 [E+1], pair_rows: int32 [S*top_k]: the (row, expert)
+ *     selections counting-sorted by expert, rows ascending within an expert;
+ *     expert e's rows are pair_rows[offsets[e] .. offsets[e+1]-1];
+ *   n_hit: int32 [1], hit: int32 [E]: the distinct selected experts, ascending,
+ *     in hit[0 .. n_hit-1].
+ * 1 <= S <= 32, top_k <= min(E, 32), E <= 1024.  All pointers are device memory.
+ */
+SDV_API sdv_status sdv_moe_route(const float* router_logits, int32_t S, int32_t E, int32_t top_k,
+                         int32_t* ids, float* weights, int32_t* offsets, int32_t* pair_rows,
+                         int32_t* n_hit, int32_t* hit, sdv_stream_t stream);
+
+/*
  * Workspace bytes an operation needs on the current device.
  * `op` is an sdv_op; n, k are the weight's (for SDV_OP_MOE: n = I, k = H);
  * S the window rows; E, top_k for SDV_OP_MOE (ignored otherwise).

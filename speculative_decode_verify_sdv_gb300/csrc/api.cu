@@ -17,6 +17,8 @@ namespace {
 using sdv::GemmArgs;
 
 constexpr size_t kWsHeader = 256;  // status word, ticket counter, reserved
+constexpr int kMaxExperts = 1024;  // MoE routing: one block of 1024 threads
+constexpr int kMaxTopK = 32;
 constexpr int kMaxS = 32;
 constexpr int kMaxDepth = 8;
 
@@ -225,8 +227,11 @@ size_t qlinear_ws_bytes(int qbits, int n, int k, int S) {
 
 // Common part of the weight-streaming GEMM launches.  For kModeY the output
 // `y_final` receives Y (through split-K partials in ws when the plan splits).
+// Split-K partials go to part_area when given (part_bytes long), else behind
+// the workspace header.
 sdv_status run_gemm(const sdv_qweight* w, const uint16_t* x, int S, int mode, GemmArgs& a, void* ws,
-                    size_t ws_bytes, float* y_final, cudaStream_t st) {
+                    size_t ws_bytes, float* y_final, cudaStream_t st, char* part_area = nullptr,
+                    size_t part_bytes = 0) {
   const GemmPlan pl = choose_plan(w->qtype, w->n, w->k, S, mode == sdv::kModeY);
   if (pl.splits == 0) return SDV_ERR_UNSUPPORTED;
   if (mode == sdv::kModeHead) {
@@ -256,19 +261,152 @@ sdv_status run_gemm(const sdv_qweight* w, const uint16_t* x, int S, int mode, Ge
   float* part = nullptr;
   if (mode == sdv::kModeY) {
     if (pl.splits > 1) {
-      const size_t need = kWsHeader + (size_t)pl.splits * S * w->n * sizeof(float);
-      if (ws_bytes < need) return SDV_ERR_WORKSPACE;
-      part = reinterpret_cast<float*>(static_cast<char*>(ws) + kWsHeader);
+      const size_t pbytes = (size_t)pl.splits * S * w->n * sizeof(float);
+      if (part_area != nullptr) {
+        if (part_bytes < pbytes) return SDV_ERR_WORKSPACE;
+        part = reinterpret_cast<float*>(part_area);
+      } else {
+        if (ws_bytes < kWsHeader + pbytes) return SDV_ERR_WORKSPACE;
+        part = reinterpret_cast<float*>(static_cast<char*>(ws) + kWsHeader);
+      }
       a.y = part;
     } else {
       a.y = y_final;
     }
   }
-  cudaError_t e = pl.tc ? sdv::launch_tc_gemm(w->qtype, mode, tc, tsc, a, pl.grid, pl.smem, st)
+  cudaError_t e = pl.tc ? sdv::launch_tc_gemm(w->qtype, mode, tc, tsc, tc, tsc, a, pl.grid, pl.smem, st)
                         : sdv::launch_dq_gemm(w->qtype, mode, tc, tsc, a, pl.grid, pl.smem, st);
   if (e == cudaSuccess && part != nullptr)
     e = sdv::launch_splitk_reduce(part, pl.splits, (long)S * w->n, y_final, st);
   return cuda_status(e);
+}
+
+sdv_status run_gemm_ws(const sdv_qweight* w, const uint16_t* x, int S, GemmArgs& a, void* ws, char* part_area,
+                       size_t part_bytes, float* y, cudaStream_t st) {
+  return run_gemm(w, x, S, sdv::kModeY, a, ws, kWsHeader, y, st, part_area, part_bytes);
+}
+
+// One tcgen05 GEMM in Y mode over w (and w2 when dual): fills the launch fields of
+// `a` from the plan and the weights; the mapping fields are the caller's.
+sdv_status launch_tc_y(const sdv_qweight* w, const sdv_qweight* w2, const GemmPlan& pl, GemmArgs& a,
+                       void* ws, cudaStream_t st) {
+  CUtensorMap tc, tsc, tc2, tsc2;
+  int sc_tma = 0, sc_tma2 = 0;
+  sdv_status s = encode_maps(w, 128, 128, &tc, &tsc, &sc_tma);
+  if (s != SDV_OK) return s;
+  if (w2 != nullptr) {
+    s = encode_maps(w2, 128, 128, &tc2, &tsc2, &sc_tma2);
+    if (s != SDV_OK) return s;
+    if (sc_tma2 != sc_tma) return SDV_ERR_UNSUPPORTED;
+  } else {
+    tc2 = tc;
+    tsc2 = tsc;
+  }
+  a.scales = w->scales;
+  a.scales_tma = sc_tma;
+  a.k_chunk = pl.k_chunk;
+  a.splits = pl.splits;
+  a.m16_tiles = 0;
+  a.depth = pl.depth;
+  a.status = static_cast<int*>(ws);
+  a.ticket = reinterpret_cast<unsigned*>(static_cast<char*>(ws) + 4);
+  return cuda_status(sdv::launch_tc_gemm(w->qtype, sdv::kModeY, tc, tsc, tc2, tsc2, a, pl.grid, pl.smem, st));
+}
+
+size_t align256(size_t b) { return (b + 255) / 256 * 256; }
+
+// Fused SwiGLU gate/up: one tcgen05 launch over both matrices (dual tiles,
+// split-K when the window rows of the full reduction do not fit), fp32 partials
+// [splits][S][2n] in the workspace, then the reduce that applies SwiGLU.
+GemmPlan plan_swiglu(int qbits, int n, int k, int S) {
+  if (k % 256 != 0) return GemmPlan{};
+  return plan_tc(qbits, 2 * n, k, S, true);
+}
+
+size_t swiglu_ws_bytes(int qbits, int n, int k, int S) {
+  const GemmPlan t = plan_swiglu(qbits, n, k, S);
+  size_t b = kWsHeader + (size_t)2 * S * n * sizeof(float);  // the two-GEMM form: g, u
+  if (t.splits > 0) {
+    const size_t bt = kWsHeader + (size_t)t.splits * S * 2 * n * sizeof(float);
+    if (bt > b) b = bt;
+  }
+  // the two-GEMM form also holds each GEMM's split-K partials behind g and u
+  const size_t q = qlinear_ws_bytes(qbits, n, k, S);
+  return b + q;
+}
+
+// Gathered-expert MoE workspace layout (all offsets 256-aligned).
+struct MoeLayout {
+  int n_cap = 0;       // most experts a window can hit: min(E, S * top_k)
+  int gx = 0, ys = 0;  // down projection: CTAs per split, splits (expert-segment slots)
+  GemmPlan gu, dn;     // gate/up and down launch plans
+  size_t ids, w, offsets, pair_rows, n_hit, hit, row_w, gu_part, hbuf, dn_part, total;
+};
+
+MoeLayout plan_moe(int qbits, int E, int I, int H, int top_k, int S) {
+  MoeLayout L;
+  const int sms = device_sms();
+  const int limit = device_smem_optin();
+  if (sms <= 0 || limit <= 0) return L;
+  L.n_cap = E < S * top_k ? E : S * top_k;
+  // gate/up: both matrices of the hit experts, full reduction H, no split
+  L.gu = plan_tc(qbits, 2 * L.n_cap * I, H, S, false);
+  if (L.gu.splits != 1) return MoeLayout{};
+  L.gu.grid = sms;
+  // down: the reduction is the hit experts' I-column segments; gx CTAs share one
+  // split (expert-segment slot) and cover the H rows between them
+  const int tiles = (H + 127) / 128;
+  for (int gx : {4, 2, 1}) {
+    if (gx > tiles) continue;
+    const int ys = sms / gx;
+    if (ys < 1) continue;
+    const int segs = (L.n_cap + ys - 1) / ys;
+    const int k_chunk = segs * I;
+    for (int d = kMaxDepth; d >= 3; --d) {
+      const int b = sdv::tc_smem_bytes(qbits, S, k_chunk, d);
+      if (b <= limit && sdv::tc_plan_valid(qbits, S, k_chunk, d)) {
+        L.dn.splits = ys;
+        L.dn.k_chunk = k_chunk;
+        L.dn.depth = d;
+        L.dn.smem = b > limit / 2 + 1024 ? b : limit / 2 + 1024;
+        L.dn.grid = gx;
+        L.dn.tc = true;
+        L.gx = gx;
+        L.ys = ys;
+        break;
+      }
+    }
+    if (L.ys > 0) break;
+  }
+  if (L.ys == 0) return MoeLayout{};
+  size_t o = kWsHeader;
+  auto take = [&](size_t bytes) {
+    const size_t at = o;
+    o = align256(o + bytes);
+    return at;
+  };
+  L.ids = take((size_t)S * top_k * 4);
+  L.w = take((size_t)S * top_k * 4);
+  L.offsets = take((size_t)(E + 1) * 4);
+  L.pair_rows = take((size_t)S * top_k * 4);
+  L.n_hit = take(4);
+  L.hit = take((size_t)E * 4);
+  L.row_w = take((size_t)S * L.n_cap * 4);
+  L.gu_part = take((size_t)S * 2 * L.n_cap * I * 4);
+  L.hbuf = take((size_t)S * L.n_cap * I * 2);
+  L.dn_part = take((size_t)L.ys * S * H * 4);
+  L.total = o;
+  return L;
+}
+
+bool moe_args_ok(const sdv_qweight* gate, const sdv_qweight* up, const sdv_qweight* down, int E, int I, int H,
+                 int top_k) {
+  if (!valid_weight(gate) || !valid_weight(up) || !valid_weight(down)) return false;
+  if (E < 1 || I < 32 || H < 32 || top_k < 1 || top_k > E) return false;
+  if (gate->qtype != up->qtype || gate->qtype != down->qtype) return false;
+  if (gate->n != E * I || up->n != E * I || gate->k != H || up->k != H) return false;
+  if (down->n != E * H || down->k != I) return false;
+  return true;
 }
 
 }  // namespace
@@ -295,16 +433,22 @@ const char* sdv_status_string(sdv_status s) {
 }
 
 size_t sdv_workspace_bytes(int32_t op, int32_t n, int32_t k, int32_t S, int32_t E, int32_t top_k) {
-  (void)n; (void)k; (void)E; (void)top_k;
   if (S < 1 || S > kMaxS) return 0;
   switch (op) {
     case SDV_OP_QLINEAR: {  // the larger of the two weight types' plans
       const size_t a = qlinear_ws_bytes(8, n, k, S), b = qlinear_ws_bytes(4, n, k, S);
       return a > b ? a : b;
     }
-    case SDV_OP_QLINEAR_SWIGLU: return kWsHeader;
+    case SDV_OP_QLINEAR_SWIGLU: {
+      const size_t a = swiglu_ws_bytes(8, n, k, S), b = swiglu_ws_bytes(4, n, k, S);
+      return a > b ? a : b;
+    }
     case SDV_OP_VERIFY_HEAD: return head_ws_bytes(S);
-    case SDV_OP_MOE: return kWsHeader;
+    case SDV_OP_MOE: {  // n = I, k = H
+      if (E < 1 || top_k < 1 || top_k > E) return 0;
+      const MoeLayout a = plan_moe(8, E, n, k, top_k, S), b = plan_moe(4, E, n, k, top_k, S);
+      return a.total > b.total ? a.total : b.total;
+    }
   }
   return 0;
 }
@@ -379,8 +523,57 @@ sdv_status sdv_greedy_accept(const int32_t* argmax, int32_t S, const int32_t* dr
 
 sdv_status sdv_qlinear_swiglu(const sdv_qweight* gate, const sdv_qweight* up, const uint16_t* x,
                               int32_t S, uint16_t* h, void* ws, size_t ws_bytes, sdv_stream_t stream) {
-  (void)gate; (void)up; (void)x; (void)S; (void)h; (void)ws; (void)ws_bytes; (void)stream;
-  return SDV_ERR_UNSUPPORTED;
+  if (!valid_weight(gate) || !valid_weight(up) || x == nullptr || h == nullptr || !aligned16(x))
+    return SDV_ERR_INVALID_ARG;
+  if (gate->qtype != up->qtype || gate->n != up->n || gate->k != up->k) return SDV_ERR_INVALID_ARG;
+  if (S < 1) return SDV_ERR_INVALID_ARG;
+  if (S > kMaxS) return SDV_ERR_UNSUPPORTED;
+  const int n = gate->n, k = gate->k;
+  const size_t need = swiglu_ws_bytes(gate->qtype, n, k, S);
+  if (ws == nullptr || !aligned16(ws) || ws_bytes < need) return SDV_ERR_WORKSPACE;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  __half* const hh = reinterpret_cast<__half*>(h);
+  float* const part = reinterpret_cast<float*>(static_cast<char*>(ws) + kWsHeader);
+  const GemmPlan pl = g_gemm_path.load() == 1 ? GemmPlan{} : plan_swiglu(gate->qtype, n, k, S);
+  if (pl.splits > 0) {
+    GemmArgs a{};
+    a.x = reinterpret_cast<const __half*>(x);
+    a.S = S;
+    a.N = n;
+    a.K = k;
+    a.ldy = 2 * n;
+    a.dual = 1;
+    a.y = part;
+    sdv_status s = launch_tc_y(gate, up, pl, a, ws, st);
+    if (s != SDV_OK) return s;
+    return cuda_status(sdv::launch_swiglu_reduce(part, pl.splits, (long)S * 2 * n, 2 * n, n, S, n, hh, n,
+                                                 nullptr, 0, 1, nullptr, st));
+  }
+  // two GEMMs (g then u, each [S][n] fp32 behind the header), then the SwiGLU reduce;
+  // each GEMM's split-K partials live behind g and u
+  float* const g = part;
+  float* const u = part + (size_t)S * n;
+  char* const ws2 = reinterpret_cast<char*>(u + (size_t)S * n);
+  const size_t ws2_bytes = ws_bytes - (size_t)(ws2 - static_cast<char*>(ws));
+  for (int m = 0; m < 2; ++m) {
+    GemmArgs a{};
+    sdv_status s = run_gemm_ws(m == 0 ? gate : up, x, S, a, ws, ws2, ws2_bytes, m == 0 ? g : u, st);
+    if (s != SDV_OK) return s;
+  }
+  return cuda_status(sdv::launch_swiglu_reduce(part, 1, 0, n, (long)S * n, S, n, hh, n, nullptr, 0, 1, nullptr, st));
+}
+
+sdv_status sdv_moe_route(const float* router_logits, int32_t S, int32_t E, int32_t top_k, int32_t* ids,
+                         float* weights, int32_t* offsets, int32_t* pair_rows, int32_t* n_hit, int32_t* hit,
+                         sdv_stream_t stream) {
+  if (router_logits == nullptr || ids == nullptr || weights == nullptr || offsets == nullptr ||
+      pair_rows == nullptr || n_hit == nullptr || hit == nullptr)
+    return SDV_ERR_INVALID_ARG;
+  if (S < 1 || E < 1 || top_k < 1 || top_k > E) return SDV_ERR_INVALID_ARG;
+  if (S > kMaxS || E > kMaxExperts || top_k > kMaxTopK) return SDV_ERR_UNSUPPORTED;
+  const int n_cap = E < S * top_k ? E : S * top_k;
+  return cuda_status(sdv::launch_moe_route(router_logits, S, E, top_k, ids, weights, offsets, pair_rows, n_hit,
+                                           hit, nullptr, n_cap, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 sdv_status sdv_moe_gather_qmm(const sdv_qweight* gate, const sdv_qweight* up, const sdv_qweight* down,
@@ -388,10 +581,76 @@ sdv_status sdv_moe_gather_qmm(const sdv_qweight* gate, const sdv_qweight* up, co
                               const float* router_logits, int32_t S, float* out,
                               int32_t* topk_ids_or_null, float* topk_w_or_null, void* ws,
                               size_t ws_bytes, sdv_stream_t stream) {
-  (void)gate; (void)up; (void)down; (void)E; (void)I; (void)H; (void)top_k; (void)x;
-  (void)router_logits; (void)S; (void)out; (void)topk_ids_or_null; (void)topk_w_or_null; (void)ws;
-  (void)ws_bytes; (void)stream;
-  return SDV_ERR_UNSUPPORTED;
+  if (!moe_args_ok(gate, up, down, E, I, H, top_k)) return SDV_ERR_INVALID_ARG;
+  if (x == nullptr || router_logits == nullptr || out == nullptr || !aligned16(x)) return SDV_ERR_INVALID_ARG;
+  if (S < 1) return SDV_ERR_INVALID_ARG;
+  if (S > kMaxS || E > kMaxExperts || top_k > kMaxTopK) return SDV_ERR_UNSUPPORTED;
+  // the tcgen05 path streams whole 128-row tiles of each expert and 256-column
+  // stages of each segment
+  if (I % 256 != 0 || H % 256 != 0 || g_gemm_path.load() == 1) return SDV_ERR_UNSUPPORTED;
+  const MoeLayout L = plan_moe(gate->qtype, E, I, H, top_k, S);
+  if (L.total == 0) return SDV_ERR_UNSUPPORTED;
+  if (ws == nullptr || !aligned16(ws) || ws_bytes < L.total) return SDV_ERR_WORKSPACE;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  char* const w8 = static_cast<char*>(ws);
+  int32_t* const ids = reinterpret_cast<int32_t*>(w8 + L.ids);
+  float* const rw8 = reinterpret_cast<float*>(w8 + L.w);
+  int32_t* const n_hit = reinterpret_cast<int32_t*>(w8 + L.n_hit);
+  int32_t* const hit = reinterpret_cast<int32_t*>(w8 + L.hit);
+  float* const row_w = reinterpret_cast<float*>(w8 + L.row_w);
+  float* const gu = reinterpret_cast<float*>(w8 + L.gu_part);
+  __half* const hb = reinterpret_cast<__half*>(w8 + L.hbuf);
+  float* const dn = reinterpret_cast<float*>(w8 + L.dn_part);
+  const int ncap_i = L.n_cap * I;
+  // a7 + a8: route and group
+  cudaError_t e = sdv::launch_moe_route(router_logits, S, E, top_k, ids, rw8,
+                                        reinterpret_cast<int32_t*>(w8 + L.offsets),
+                                        reinterpret_cast<int32_t*>(w8 + L.pair_rows), n_hit, hit, row_w, L.n_cap, st);
+  if (e != cudaSuccess) return cuda_status(e);
+  // a9, gate and up: every window row through each hit expert's rows (dual tiles
+  // over the hit list), fp32 [S][2 * n_cap * I]
+  {
+    GemmArgs a{};
+    a.x = reinterpret_cast<const __half*>(x);
+    a.S = S;
+    a.N = ncap_i;
+    a.K = H;
+    a.ldy = 2 * ncap_i;
+    a.dual = 1;
+    a.n_hit = n_hit;
+    a.hit = hit;
+    a.rows_per_expert = I;
+    a.y = gu;
+    sdv_status s = launch_tc_y(gate, up, L.gu, a, ws, st);
+    if (s != SDV_OK) return s;
+  }
+  // h'[s][j * I + c] = fp16(w(s, hit j) * SiLU(g) * u), zero where row s did not pick hit j
+  e = sdv::launch_swiglu_reduce(gu, 1, 0, 2 * ncap_i, ncap_i, S, ncap_i, hb, ncap_i, row_w, L.n_cap, I, n_hit, st);
+  if (e != cudaSuccess) return cuda_status(e);
+  // a9, down and combine: out = h' (hit experts' segments along the reduction) x
+  // the hit experts' down rows, split by expert-segment slots, reduced in order
+  {
+    GemmArgs a{};
+    a.x = hb;
+    a.S = S;
+    a.N = H;
+    a.K = ncap_i;
+    a.ldx = ncap_i;
+    a.n_hit = n_hit;
+    a.hit = hit;
+    a.rows_per_expert = H;
+    a.seg_k = I;
+    a.y = dn;
+    sdv_status s = launch_tc_y(down, nullptr, L.dn, a, ws, st);
+    if (s != SDV_OK) return s;
+  }
+  e = sdv::launch_splitk_reduce(dn, L.ys, (long)S * H, out, st);
+  if (e != cudaSuccess) return cuda_status(e);
+  if (topk_ids_or_null != nullptr)
+    e = cudaMemcpyAsync(topk_ids_or_null, ids, (size_t)S * top_k * 4, cudaMemcpyDeviceToDevice, st);
+  if (e == cudaSuccess && topk_w_or_null != nullptr)
+    e = cudaMemcpyAsync(topk_w_or_null, rw8, (size_t)S * top_k * 4, cudaMemcpyDeviceToDevice, st);
+  return cuda_status(e);
 }
 
 }  // extern "C"

@@ -36,6 +36,17 @@ struct GemmArgs {
   int* part_i;              // [grid][S]
   unsigned* ticket;
   int* status;
+  // ---- row / reduction mappings of the tcgen05 path (kModeY; zero = plain) ----
+  int ldx;                  // row stride of x in elements (0: K)
+  int ldy;                  // row stride of y in elements (0: N)
+  int dual;                 // 1: two weight matrices of N rows each (second tensor maps);
+                            //    output column mat * N + row, mat = 0 for the first
+  const int* n_hit;         // device [1]: number of hit experts (MoE), or null
+  const int* hit;           // device [n_hit]: expert ids, ascending
+  int rows_per_expert;      // rows of one expert in a stacked weight
+  int seg_k;                // > 0: the reduction is n_hit segments of seg_k columns, segment j
+                            //    reading expert hit[j]'s rows; split y covers segments
+                            //    [y * n_hit / splits, (y + 1) * n_hit / splits)
 };
 
 int gemm_tile_mt(int qbits);
@@ -48,10 +59,25 @@ cudaError_t launch_dq_gemm(int qbits, int mode, const CUtensorMap& tm_codes,
 int tc_smem_bytes(int qbits, int S, int k_chunk, int depth);
 bool tc_plan_valid(int qbits, int S, int k_chunk, int depth);
 cudaError_t launch_tc_gemm(int qbits, int mode, const CUtensorMap& tm_codes,
-                           const CUtensorMap& tm_scales, const GemmArgs& a, int grid, int smem,
+                           const CUtensorMap& tm_scales, const CUtensorMap& tm_codes2,
+                           const CUtensorMap& tm_scales2, const GemmArgs& a, int grid, int smem,
                            cudaStream_t st);
 
 cudaError_t launch_splitk_reduce(const float* part, int splits, long count, float* y, cudaStream_t st);
+
+// h[s][c] = fp16(SiLU(g) * u [* row_w[s][c / seg]]) for c < n (or c < *n_dev * seg
+// when n_dev is given), with g = sum over splits of part[sp * pstride + s * ldp + c]
+// and u the same at + u_off.
+cudaError_t launch_swiglu_reduce(const float* part, int splits, long pstride, int ldp, long u_off, int S,
+                                 int n, __half* h, int ldh, const float* row_w, int ldw, int seg,
+                                 const int* n_dev, cudaStream_t st);
+
+// MoE routing (top_k of E per row, ties to the lower id, softmax over the
+// selection) and grouping (per-expert row lists by counting sort, the ascending
+// list of hit experts, a dense [S][n_cap] routing-weight table by hit slot).
+cudaError_t launch_moe_route(const float* logits, int S, int E, int top_k, int32_t* ids, float* w,
+                             int32_t* offsets, int32_t* pair_rows, int32_t* n_hit, int32_t* hit,
+                             float* row_w, int n_cap, cudaStream_t st);
 
 cudaError_t launch_quantize(const float* w, int n, int k, int qbits, void* codes, uint16_t* scales,
                             cudaStream_t st);

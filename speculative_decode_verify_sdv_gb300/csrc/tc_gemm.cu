@@ -52,12 +52,11 @@ constexpr int kABufs = 3;        // A operand stage buffers in tensor memory
 constexpr int kACols = kABufs * 128;
 
 struct TcRoles {
-  static constexpr int G = 2;                // converter groups (blocks 0-3 / 4-7 of a stage)
-  static constexpr int kConvWarps = 4 * G;
+  static constexpr int G = 2;                // converter groups: group g takes the stages i with i % 2 == g
+  static constexpr int kConvWarps = 4 * G;   // one warp per tensor-memory lane quarter per group
   static constexpr int kConv0 = 6;           // first converter warp (0 TMA, 1 MMA, 2-5 epilogue)
   static constexpr int kWarps = kConv0 + kConvWarps;
   static constexpr int kThreads = 32 * kWarps;
-  static constexpr int kBlocksPerGroup = 8 / G;
 };
 
 struct TcPlan {
@@ -84,7 +83,7 @@ __host__ __device__ inline TcPlan tc_plan(int qb, int S, int kc, int depth) {
   p.sc_off = p.ring_off + depth * p.code_stage;
   p.red_off = p.sc_off + depth * p.sc_stage;           // epilogue: [4 warps][S][33] floats
   p.bar_off = rup(p.red_off + 4 * S * 33 * 4, 16);
-  p.best_off = p.bar_off + (2 * depth + 2 * TcRoles::G * kABufs + 4) * 8;
+  p.best_off = p.bar_off + (2 * depth + 2 * kABufs + 4) * 8;
   p.misc_off = p.best_off + 4 * 32 * 8;
   p.total = p.misc_off + 32 * 4 + 16;
   return p;
@@ -93,10 +92,10 @@ __host__ __device__ inline TcPlan tc_plan(int qb, int S, int kc, int depth) {
 template <int QB, int MODE, int NM>
 __global__ void __launch_bounds__(TcRoles::kThreads, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_codes,
-                   const __grid_constant__ CUtensorMap tm_scales, const GemmArgs p) {
+                   const __grid_constant__ CUtensorMap tm_scales,
+                   const __grid_constant__ CUtensorMap tm_codes2,
+                   const __grid_constant__ CUtensorMap tm_scales2, const GemmArgs p) {
   using R = TcRoles;
-  constexpr int G = R::G;
-  constexpr int BPG = R::kBlocksPerGroup;
   // independent fp32 accumulators per tile (MMA m of a stage -> m % kAcc), two
   // tile buffers, in the tensor-memory columns behind the A buffers
   constexpr int kAcc = (512 - kACols) / (2 * NM);
@@ -107,8 +106,62 @@ __global__ void __launch_bounds__(TcRoles::kThreads, 1)
   uint8_t* const sb = smem_raw + (base - raw_addr);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int k_begin = blockIdx.y * p.k_chunk;
-  const int k_len = min(p.k_chunk, p.K - k_begin);
+  // Row and reduction mappings (all uniform over the CTA):
+  //  * plain: tile t covers weight rows 128t.., the reduction [k_begin, k_begin + k_len);
+  //  * dual: tiles [0, T) read the first matrix, [T, 2T) the second (T tiles each);
+  //  * hit-list tiles (n_hit, no seg_k): the T tiles of a matrix run over the hit
+  //    experts' row blocks, rows_per_expert rows each;
+  //  * expert segments (n_hit and seg_k): the reduction runs over the hit experts'
+  //    seg_k columns, segment j reading expert hit[j]'s rows.
+  const bool segs = (p.n_hit != nullptr) && p.seg_k > 0;
+  const bool hit_tiles = (p.n_hit != nullptr) && p.seg_k == 0;
+  const int n_hit = (p.n_hit != nullptr) ? *p.n_hit : 0;
+  int k_begin, k_len;
+  if (segs) {
+    const int s_lo = (int)((long)blockIdx.y * n_hit / gridDim.y);
+    const int s_hi = (int)((long)(blockIdx.y + 1) * n_hit / gridDim.y);
+    k_begin = s_lo * p.seg_k;
+    k_len = (s_hi - s_lo) * p.seg_k;
+  } else {
+    k_begin = blockIdx.y * p.k_chunk;
+    k_len = min(p.k_chunk, p.K - k_begin);
+  }
+  const int n_one = hit_tiles ? n_hit * p.rows_per_expert : p.N;  // rows of one matrix
+  const int t_one = (n_one + kTileRows - 1) / kTileRows;          // tiles of one matrix
+  const int ldx = p.ldx > 0 ? p.ldx : p.K;
+  const int ldy = p.ldy > 0 ? p.ldy : p.N;
+  // tile t -> (matrix, tile within the matrix, first weight row)
+  auto tile_split = [&](int t, int& mat, int& lt) {
+    mat = (p.dual && t >= t_one) ? 1 : 0;
+    lt = t - mat * t_one;
+  };
+  auto tile_map = [&](int t, int& mat, int& lt) -> int {
+    tile_split(t, mat, lt);
+    if (hit_tiles) {
+      const int tpe = p.rows_per_expert / kTileRows;
+      const int j = lt / tpe;
+      return __ldg(p.hit + j) * p.rows_per_expert + (lt - j * tpe) * kTileRows;
+    }
+    return lt * kTileRows;
+  };
+
+  // tiles of this CTA
+  const int tiles = p.dual ? 2 * t_one : t_one;
+  const int tile_lo = (int)((long)blockIdx.x * tiles / gridDim.x);
+  const int tile_hi = (int)((long)(blockIdx.x + 1) * tiles / gridDim.x);
+  const int ntile = tile_hi - tile_lo;
+  if (MODE == kModeY && k_len <= 0) {
+    // an empty reduction range still owns its split's partial outputs: zeros
+    float* const yo = p.y + (size_t)blockIdx.y * p.S * ldy;
+    for (int v = threadIdx.x; v < ntile * kTileRows * p.S; v += blockDim.x) {
+      const int n = v / (ntile * kTileRows), tr = v - n * (ntile * kTileRows);
+      int mat, lt;
+      tile_split(tile_lo + tr / kTileRows, mat, lt);
+      const int row = lt * kTileRows + (tr % kTileRows);
+      if (row < n_one) yo[(size_t)n * ldy + mat * p.N + row] = 0.f;
+    }
+    return;
+  }
   const TcPlan pl = tc_plan(QB, p.S, p.k_chunk, p.depth);
   const int depth = pl.depth;
 
@@ -117,9 +170,9 @@ __global__ void __launch_bounds__(TcRoles::kThreads, 1)
   const uint32_t sc_ring = base + pl.sc_off;
   const uint32_t bars = base + pl.bar_off;
   const uint32_t bar_full = bars, bar_empty = bars + 8 * depth;
-  const uint32_t bar_afull = bars + 16 * depth;            // [g][buf]
-  const uint32_t bar_afree = bar_afull + 8 * G * kABufs;  // [g][buf]
-  const uint32_t bar_tfull = bar_afree + 8 * G * kABufs;  // [tile buf]
+  const uint32_t bar_afull = bars + 16 * depth;        // [A buffer]
+  const uint32_t bar_afree = bar_afull + 8 * kABufs;  // [A buffer]
+  const uint32_t bar_tfull = bar_afree + 8 * kABufs;  // [tile buf]
   const uint32_t bar_tfree = bar_tfull + 2 * 8;  // [tile buf]
   float* const best_v = reinterpret_cast<float*>(sb + pl.best_off);
   int* const best_i = reinterpret_cast<int*>(sb + pl.best_off + 4 * 32 * 4);
@@ -128,11 +181,7 @@ __global__ void __launch_bounds__(TcRoles::kThreads, 1)
   int* const s_flag = reinterpret_cast<int*>(sb + pl.misc_off + 8);
   int* const s_am = reinterpret_cast<int*>(sb + pl.misc_off + 16);
 
-  // tiles of this CTA and the stage sequence
-  const int tiles = (p.N + kTileRows - 1) / kTileRows;
-  const int tile_lo = (int)((long)blockIdx.x * tiles / gridDim.x);
-  const int tile_hi = (int)((long)(blockIdx.x + 1) * tiles / gridDim.x);
-  const int ntile = tile_hi - tile_lo;
+  // the stage sequence
   const int kst = (k_len + 255) / 256;
   const int nblk_total = k_len / 32;
   const int nstages = ntile * kst;
@@ -152,9 +201,6 @@ __global__ void __launch_bounds__(TcRoles::kThreads, 1)
     const bool ok = wait(bar, parity);
     return __all_sync(0xffffffffu, ok) != 0;
   };
-  auto group_blocks = [&](int ks, int g) -> int {  // valid 32-blocks of group g at stage column ks
-    return max(0, min(BPG, nblk_total - ks * 8 - BPG * g));
-  };
   // Stage cursor: position i in the stage sequence and its derived indices,
   // advanced incrementally (no per-stage integer division).
   struct Cursor {
@@ -172,28 +218,41 @@ __global__ void __launch_bounds__(TcRoles::kThreads, 1)
   uint64_t policy = 0;
   auto issue = [&](const Cursor& c) {  // TMA of stage c.i into ring slot c.slot
     const int slot = c.slot, ks = c.ks;
-    const int row0 = (tile_lo + c.t) * kTileRows;
+    int mat, lt;
+    int row0 = tile_map(tile_lo + c.t, mat, lt);
     const int boxes = (QB == 8) ? 2 : 1;
-    const int xb = kbyte0 + ks * 128 * boxes;
+    int xb, sc_col;
+    bool all_boxes = false;
+    if (segs) {  // expert segment of this stage (seg_k is a multiple of 256)
+      const int kk = k_begin + ks * 256;
+      const int j = kk / p.seg_k, col = kk - j * p.seg_k;
+      row0 = __ldg(p.hit + j) * p.rows_per_expert + lt * kTileRows;
+      xb = (QB == 8) ? col : col / 2;
+      sc_col = col / 32;
+      all_boxes = true;
+    } else {
+      xb = kbyte0 + ks * 128 * boxes;
+      sc_col = k_begin / 32 + ks * 8;
+    }
+    const CUtensorMap* const mc = mat ? &tm_codes2 : &tm_codes;
+    const CUtensorMap* const ms = mat ? &tm_scales2 : &tm_scales;
     uint32_t bytes = p.scales_tma ? kTileRows * 16 : 0;
     for (int bx = 0; bx < boxes; ++bx)
-      if (xb + 128 * bx < kbyte_end) bytes += kTileRows * 128;
+      if (all_boxes || xb + 128 * bx < kbyte_end) bytes += kTileRows * 128;
     const uint32_t fb = bar_full + 8 * slot;
     mbar_arrive_expect_tx(fb, bytes);
     for (int bx = 0; bx < boxes; ++bx)
-      if (xb + 128 * bx < kbyte_end)
-        tma_load_2d(ring + slot * pl.code_stage + bx * kTileRows * 128, &tm_codes, xb + 128 * bx, row0, fb,
-                    policy);
-    if (p.scales_tma)
-      tma_load_2d(sc_ring + slot * pl.sc_stage, &tm_scales, k_begin / 32 + ks * 8, row0, fb, policy);
+      if (all_boxes || xb + 128 * bx < kbyte_end)
+        tma_load_2d(ring + slot * pl.code_stage + bx * kTileRows * 128, mc, xb + 128 * bx, row0, fb, policy);
+    if (p.scales_tma) tma_load_2d(sc_ring + slot * pl.sc_stage, ms, sc_col, row0, fb, policy);
   };
 
   if (threadIdx.x == 0) {
     for (int d = 0; d < depth; ++d) {
       mbar_init(bar_full + 8 * d, 1);
-      mbar_init(bar_empty + 8 * d, R::kConvWarps);
+      mbar_init(bar_empty + 8 * d, 4);  // the four warps of the stage's group
     }
-    for (int j = 0; j < G * kABufs; ++j) {
+    for (int j = 0; j < kABufs; ++j) {
       mbar_init(bar_afull + 8 * j, 4);
       mbar_init(bar_afree + 8 * j, 1);
     }
@@ -207,6 +266,10 @@ __global__ void __launch_bounds__(TcRoles::kThreads, 1)
     policy = l2_policy_evict_first();
     tma_prefetch_desc(&tm_codes);
     if (p.scales_tma) tma_prefetch_desc(&tm_scales);
+    if (p.dual) {
+      tma_prefetch_desc(&tm_codes2);
+      if (p.scales_tma) tma_prefetch_desc(&tm_scales2);
+    }
     Cursor c = cursor_at(0);
     for (; c.i < depth && c.i < nstages; advance(c)) issue(c);
   }
@@ -229,7 +292,7 @@ __global__ void __launch_bounds__(TcRoles::kThreads, 1)
     for (int v = threadIdx.x; v < total; v += blockDim.x) {
       const int n = v / g8n, g8 = v - n * g8n;
       uint4 in = make_uint4(0u, 0u, 0u, 0u);
-      if (n < p.S && g8 < g8v) in = *reinterpret_cast<const uint4*>(p.x + (size_t)n * p.K + k_begin + 8 * g8);
+      if (n < p.S && g8 < g8v) in = *reinterpret_cast<const uint4*>(p.x + (size_t)n * ldx + k_begin + 8 * g8);
       uint4 o;
       if (QB == 8) {  // per 4 elements: (k0, k2, k1, k3)
         o.x = __byte_perm(in.x, in.y, 0x5410);
@@ -278,31 +341,15 @@ __global__ void __launch_bounds__(TcRoles::kThreads, 1)
       // descriptor start address advances by k (16-byte units) per reduction element k
       const uint64_t b_stage = bdesc0 + (uint64_t)(ks * 256);
       const bool later = ks > 0;
-      bool ok = true;
+      if (!wait_warp(bar_afull + 8 * ab, c.abphase)) break;
+      tc_fence_after();
+      // straight-line issue: a branch around an elected MMA costs a warp
+      // reconvergence per instruction
 #pragma unroll
-      for (int g = 0; g < G; ++g) {
-        if (!wait_warp(bar_afull + 8 * (kABufs * g + ab), c.abphase)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        // straight-line issue: a branch around an elected MMA costs a warp
-        // reconvergence per instruction
-#pragma unroll
-        for (int blk = 0; blk < BPG; ++blk) {
-#pragma unroll
-          for (int s = 0; s < 2; ++s) {
-            const int sblk = BPG * g + blk;          // compile-time
-            const int mloc = 2 * sblk + s;           // compile-time, 0..15
-            tc_mma_f16_ta_elect(d_tile + (uint32_t)((mloc & (kAcc - 1)) * NM),
-                                a_stage + (uint32_t)(sblk * 16 + s * 8),
-                                b_stage + (uint64_t)(sblk * 32 + s * 16), idesc,
-                                (later || mloc >= kAcc) ? 1u : 0u);
-          }
-        }
-        tc_commit_elect(bar_afree + 8 * (kABufs * g + ab));
-      }
-      if (!ok) break;
+      for (int m = 0; m < 16; ++m)  // MMA m: k = 16m .. 16m+15 of the stage
+        tc_mma_f16_ta_elect(d_tile + (uint32_t)((m & (kAcc - 1)) * NM), a_stage + (uint32_t)(m * 8),
+                            b_stage + (uint64_t)(m * 16), idesc, (later || m >= kAcc) ? 1u : 0u);
+      tc_commit_elect(bar_afree + 8 * ab);
       if (ks == kst - 1) tc_commit_elect(bar_tfull + 8 * tb);
     }
   } else if (warp < R::kConv0) {
@@ -338,13 +385,15 @@ __global__ void __launch_bounds__(TcRoles::kThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_tfree + 8 * tb);
-      const int row = (tile_lo + t) * kTileRows + r;
-      const bool valid = row < p.N;
+      int mat, lt;
+      tile_split(tile_lo + t, mat, lt);
+      const int lrow = lt * kTileRows + r;  // row within its matrix
+      const bool valid = lrow < n_one;
       if (p.y != nullptr && valid) {
-        float* const yo = p.y + (size_t)blockIdx.y * p.S * p.N;
+        float* const yo = p.y + (size_t)blockIdx.y * p.S * ldy + mat * p.N + lrow;
 #pragma unroll
         for (int n = 0; n < 32; ++n)
-          if (n < p.S) yo[(size_t)n * p.N + row] = acc[n];
+          if (n < p.S) yo[(size_t)n * ldy] = acc[n];
       }
       if (MODE == kModeHead) {
         // columns through shared memory: lane n then scans the warp's 32 rows
@@ -368,87 +417,97 @@ __global__ void __launch_bounds__(TcRoles::kThreads, 1)
     }
   } else {
     // ---------------- converters ------------------------------------------------------
+    // Group g converts whole stages g, g+2, g+4, ...: while one group waits for
+    // its next stage the other converts, and each stage is one hand-off to the
+    // MMA warp.
     const int cw = warp - R::kConv0;
     const int q = warp & 3;
     const int g = cw >> 2;
     const int r = 32 * q + lane;  // row within the tile (= TMEM lane)
     const uint32_t lane_base = (uint32_t)(32 * q) << 16;
     const int ks_per_row = p.K / 32;
-    for (Cursor c = cursor_at(0); c.i < nstages; advance(c)) {
+    constexpr int kHalves = (QB == 8) ? 2 : 1;   // 128-byte code loads per row and stage
+    constexpr int kHalfBlocks = 8 / kHalves;     // 32-blocks per load
+    const int sw = r & 7;
+    Cursor c = cursor_at(0);
+    if (g == 1) advance(c);
+    for (; c.i < nstages; advance(c), advance(c)) {
       const int slot = c.slot;
       const int ab = c.ab;
-      const int nb = group_blocks(c.ks, g);
+      const int nb = max(0, min(8, nblk_total - c.ks * 8));  // blocks within the reduction length
       bool ok = wait_warp(bar_full + 8 * slot, c.phase);
-      // codes and scales of this group's blocks (row r) into registers, then the
-      // ring slot goes back to the producer before the conversion
-      constexpr int kBlkBytes = (QB == 8) ? 32 : 16;  // code bytes of one 32-block
-      constexpr int kWords = BPG * kBlkBytes / 16;     // 16-byte chunks per row per group
-      uint4 wreg[kWords];
-      uint32_t sc_h[BPG];
+      const uint8_t* const cb = sb + pl.ring_off + slot * pl.code_stage;
+      // the 8 block scales of row r; blocks past the reduction length get zero, so
+      // their A columns are zero (the padded window rows are zero too)
+      uint32_t sc_h[8];
 #pragma unroll
-      for (int blk = 0; blk < BPG; ++blk) sc_h[blk] = 0u;
+      for (int blk = 0; blk < 8; ++blk) sc_h[blk] = 0u;
       if (ok) {
-        const uint8_t* const cb = sb + pl.ring_off + slot * pl.code_stage;
-        const int sw = r & 7;
-#pragma unroll
-        for (int w = 0; w < kWords; ++w) {
-          // byte offset in the stage row -> 128-byte box and swizzled 16-byte chunk
-          const int byte = BPG * g * kBlkBytes + 16 * w;
-          const int box = byte >> 7, chunk = (byte >> 4) & 7;
-          const uint8_t* const row_p = cb + box * kTileRows * 128 + r * 128;
-          wreg[w] = *reinterpret_cast<const uint4*>(row_p + ((chunk ^ sw) << 4));
-        }
         if (p.scales_tma) {
-          const uint8_t* const sp = sb + pl.sc_off + slot * pl.sc_stage + r * 16 + BPG * g * 2;
-          if (BPG == 4) {
-            const uint2 sv = *reinterpret_cast<const uint2*>(sp);
-            sc_h[0] = sv.x & 0xFFFFu; sc_h[1] = sv.x >> 16; sc_h[BPG - 2] = sv.y & 0xFFFFu; sc_h[BPG - 1] = sv.y >> 16;
-          } else {
-            const uint32_t sv = *reinterpret_cast<const uint32_t*>(sp);
-            sc_h[0] = sv & 0xFFFFu; sc_h[BPG - 1] = sv >> 16;
+          const uint4 sv = *reinterpret_cast<const uint4*>(sb + pl.sc_off + slot * pl.sc_stage + r * 16);
+          const uint32_t w4[4] = {sv.x, sv.y, sv.z, sv.w};
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            sc_h[2 * j] = w4[j] & 0xFFFFu;
+            sc_h[2 * j + 1] = w4[j] >> 16;
           }
         } else {
           const int row = (tile_lo + c.t) * kTileRows + r;
           const int ks = c.ks;
 #pragma unroll
-          for (int blk = 0; blk < BPG; ++blk)
+          for (int blk = 0; blk < 8; ++blk)
             sc_h[blk] = (blk < nb && row < p.N)
-                            ? (uint32_t)__ldg(p.scales + (size_t)row * ks_per_row + k_begin / 32 + ks * 8 + BPG * g + blk)
+                            ? (uint32_t)__ldg(p.scales + (size_t)row * ks_per_row + k_begin / 32 + ks * 8 + blk)
                             : 0u;
         }
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar_empty + 8 * slot);
-      if (ok && c.i >= kABufs) ok = wait_warp(bar_afree + 8 * (kABufs * g + ab), c.abphase ^ 1);
-      if (ok) {
-        tc_fence_after();
 #pragma unroll
-        for (int blk = 0; blk < BPG; ++blk) {
-          // blocks past the reduction length (blk >= nb) have a zero scale: their
-          // A columns are zero, and the padded window rows are zero too
-          const __half2 s2 = u32_as_h2(sc_h[blk] | (sc_h[blk] << 16));
-          const int sblk = BPG * g + blk;  // block within the stage
-          uint32_t cols[16];
-          if (QB == 8) {
-            const uint32_t wv[8] = {wreg[2 * blk].x, wreg[2 * blk].y, wreg[2 * blk].z, wreg[2 * blk].w,
-                                    wreg[2 * blk + 1].x, wreg[2 * blk + 1].y, wreg[2 * blk + 1].z, wreg[2 * blk + 1].w};
+      for (int h = 0; h < kHalves; ++h) {
+        // 128 code bytes of row r (int8: half h of the stage; int4: the whole stage)
+        uint4 wreg[8];
+        if (ok) {
+          const uint8_t* const row_p = cb + h * kTileRows * 128 + r * 128;
 #pragma unroll
-            for (int j = 0; j < 8; ++j) i8x4_to_h2x2(wv[j], cols[2 * j], cols[2 * j + 1]);
-          } else {
-            const uint32_t wv[4] = {wreg[blk].x, wreg[blk].y, wreg[blk].z, wreg[blk].w};
-#pragma unroll
-            for (int j = 0; j < 4; ++j)
-              i4x8_to_h2x4(wv[j], cols[4 * j], cols[4 * j + 1], cols[4 * j + 2], cols[4 * j + 3]);
-          }
-#pragma unroll
-          for (int j = 0; j < 16; ++j) cols[j] = h2_as_u32(__hmul2(u32_as_h2(cols[j]), s2));
-          tmem_st16(tmem + lane_base + (uint32_t)(ab * 128 + sblk * 16), cols);
+          for (int w = 0; w < 8; ++w) wreg[w] = *reinterpret_cast<const uint4*>(row_p + ((w ^ sw) << 4));
         }
+        if (h == kHalves - 1) {  // the ring slot goes back to the producer
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar_empty + 8 * slot);
+        }
+        if (h == 0) {
+          if (ok && c.i >= kABufs) ok = wait_warp(bar_afree + 8 * ab, c.abphase ^ 1);
+          if (ok) tc_fence_after();
+        }
+        if (ok) {
+#pragma unroll
+          for (int blk = 0; blk < kHalfBlocks; ++blk) {
+            const int sblk = h * kHalfBlocks + blk;  // block within the stage
+            const __half2 s2 = u32_as_h2(sc_h[sblk] | (sc_h[sblk] << 16));
+            uint32_t cols[16];
+            if (QB == 8) {
+              const uint32_t wv[8] = {wreg[2 * blk].x, wreg[2 * blk].y, wreg[2 * blk].z, wreg[2 * blk].w,
+                                      wreg[2 * blk + 1].x, wreg[2 * blk + 1].y, wreg[2 * blk + 1].z,
+                                      wreg[2 * blk + 1].w};
+#pragma unroll
+              for (int j = 0; j < 8; ++j) i8x4_to_h2x2(wv[j], cols[2 * j], cols[2 * j + 1]);
+            } else {
+              const uint32_t wv[4] = {wreg[blk].x, wreg[blk].y, wreg[blk].z, wreg[blk].w};
+#pragma unroll
+              for (int j = 0; j < 4; ++j)
+                i4x8_to_h2x4(wv[j], cols[4 * j], cols[4 * j + 1], cols[4 * j + 2], cols[4 * j + 3]);
+            }
+#pragma unroll
+            for (int j = 0; j < 16; ++j) cols[j] = h2_as_u32(__hmul2(u32_as_h2(cols[j]), s2));
+            tmem_st16(tmem + lane_base + (uint32_t)(ab * 128 + sblk * 16), cols);
+          }
+        }
+      }
+      if (ok) {
         tmem_wait_st();
         tc_fence_before();
       }
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar_afull + 8 * (kABufs * g + ab));
+      if (lane == 0) mbar_arrive(bar_afull + 8 * ab);
     }
   }
 
@@ -505,21 +564,23 @@ __global__ void __launch_bounds__(TcRoles::kThreads, 1)
   }
 }
 
+struct TcMaps {
+  const CUtensorMap &c, &s, &c2, &s2;
+};
+
 template <int QB, int MODE, int NM>
-cudaError_t tc_launch_t(const CUtensorMap& tc, const CUtensorMap& tsc, const GemmArgs& a, int grid,
-                        int smem, cudaStream_t st) {
+cudaError_t tc_launch_t(const TcMaps& m, const GemmArgs& a, int grid, int smem, cudaStream_t st) {
   auto k = tc_gemm_kernel<QB, MODE, NM>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  k<<<dim3(grid, a.splits), TcRoles::kThreads, smem, st>>>(tc, tsc, a);
+  k<<<dim3(grid, a.splits), TcRoles::kThreads, smem, st>>>(m.c, m.s, m.c2, m.s2, a);
   return cudaGetLastError();
 }
 
 template <int QB, int MODE>
-cudaError_t tc_launch_nm(const CUtensorMap& tc, const CUtensorMap& tsc, const GemmArgs& a, int grid,
-                         int smem, cudaStream_t st) {
-  return a.S <= 16 ? tc_launch_t<QB, MODE, 16>(tc, tsc, a, grid, smem, st)
-                   : tc_launch_t<QB, MODE, 32>(tc, tsc, a, grid, smem, st);
+cudaError_t tc_launch_nm(const TcMaps& m, const GemmArgs& a, int grid, int smem, cudaStream_t st) {
+  return a.S <= 16 ? tc_launch_t<QB, MODE, 16>(m, a, grid, smem, st)
+                   : tc_launch_t<QB, MODE, 32>(m, a, grid, smem, st);
 }
 
 }  // namespace
@@ -538,13 +599,13 @@ bool tc_plan_valid(int qbits, int S, int k_chunk, int depth) {
 }
 
 cudaError_t launch_tc_gemm(int qbits, int mode, const CUtensorMap& tm_codes, const CUtensorMap& tm_scales,
-                           const GemmArgs& a, int grid, int smem, cudaStream_t st) {
+                           const CUtensorMap& tm_codes2, const CUtensorMap& tm_scales2, const GemmArgs& a,
+                           int grid, int smem, cudaStream_t st) {
+  const TcMaps m{tm_codes, tm_scales, tm_codes2, tm_scales2};
   const bool head = mode == kModeHead;
   if (qbits == 8)
-    return head ? tc_launch_nm<8, kModeHead>(tm_codes, tm_scales, a, grid, smem, st)
-                : tc_launch_nm<8, kModeY>(tm_codes, tm_scales, a, grid, smem, st);
-  return head ? tc_launch_nm<4, kModeHead>(tm_codes, tm_scales, a, grid, smem, st)
-              : tc_launch_nm<4, kModeY>(tm_codes, tm_scales, a, grid, smem, st);
+    return head ? tc_launch_nm<8, kModeHead>(m, a, grid, smem, st) : tc_launch_nm<8, kModeY>(m, a, grid, smem, st);
+  return head ? tc_launch_nm<4, kModeHead>(m, a, grid, smem, st) : tc_launch_nm<4, kModeY>(m, a, grid, smem, st);
 }
 
 }  // namespace sdv

@@ -23,6 +23,7 @@ EXPORTED = (
     "sdv_quantize_block32", "sdv_qlinear", "sdv_qlinear_swiglu", "sdv_verify_head",
     "sdv_greedy_accept", "sdv_moe_gather_qmm", "sdv_workspace_bytes", "sdv_workspace_init",
     "sdv_device_status", "sdv_status_string", "sdv_version", "sdv_verify_head_noalloc", "sdv_set_gemm_path",
+    "sdv_moe_route",
 )
 
 
@@ -58,6 +59,7 @@ def load() -> ctypes.CDLL:
         "sdv_verify_head_noalloc": ([qw, vp, i32, vp, i32, vp, vp, vp, vp, vp], i32),
         "sdv_greedy_accept": ([vp, i32, vp, i32, vp, vp, vp], i32),
         "sdv_moe_gather_qmm": ([qw, qw, qw, i32, i32, i32, i32, vp, vp, i32, vp, vp, vp, vp, sz, vp], i32),
+        "sdv_moe_route": ([vp, i32, i32, i32, vp, vp, vp, vp, vp, vp, vp], i32),
         "sdv_workspace_bytes": ([i32, i32, i32, i32, i32, i32], sz),
         "sdv_workspace_init": ([vp, sz, vp], i32),
         "sdv_device_status": ([vp, vp], i32),
@@ -216,6 +218,18 @@ def sdv_moe_gather_qmm(gate: QWeight, up: QWeight, down: QWeight, E: int, I: int
         ctypes.byref(cg), ctypes.byref(cu), ctypes.byref(cd), E, I, H, top_k, _ptr(x),
         _ptr(router_logits), S, _ptr(out), _ptr(topk_ids), _ptr(topk_w), _ptr(ws),
         ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def sdv_moe_route(router_logits: torch.Tensor, S: int, E: int, top_k: int, ids: torch.Tensor,
+                  weights: torch.Tensor, offsets: torch.Tensor, pair_rows: torch.Tensor,
+                  n_hit: torch.Tensor, hit: torch.Tensor, stream=None) -> None:
+    _want(router_logits, torch.float32, "router_logits")
+    _want(weights, torch.float32, "weights")
+    for t, nm in ((ids, "ids"), (offsets, "offsets"), (pair_rows, "pair_rows"), (n_hit, "n_hit"), (hit, "hit")):
+        _want(t, torch.int32, nm)
+    _check("sdv_moe_route", load().sdv_moe_route(
+        _ptr(router_logits), S, E, top_k, _ptr(ids), _ptr(weights), _ptr(offsets), _ptr(pair_rows),
+        _ptr(n_hit), _ptr(hit), _stream(stream)))
 
 
 # ---- small allocation helpers (torch owns the memory) ---------------------------
