@@ -7,7 +7,12 @@ dequant GEMM + argmax + greedy accept; logits never leave the chip), over
 stream (413 MB) is larger than L2, so every window reads it from HBM.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl sdv|reference]
-                    [--config q4b|a3b|tiny] [--S S]
+                    [--config q4b|a3b|tiny|mlp27|moe] [--S S]
+
+Other workloads (--config): the 35B-A3B-shaped int4 head (a3b), the tiny
+L2-resident head (tiny), the 27B-shaped dense SwiGLU MLP (mlp27: gate/up
+17408 x 5120 + down 5120 x 17408, int8) and the 256-expert int4 MoE layer
+(moe).
 
 Prints one JSON line.  ``--impl reference`` times the CPU oracle on a bounded
 sample of the same workload.  With N > 1 (torchrun) every rank runs an
@@ -139,29 +144,102 @@ def max_over_ranks(world, v: float, device=None) -> float:
     return float(t.item())
 
 
+# ---- algorithmic bytes ------------------------------------------------------------
+
+def weight_bytes(n: int, k: int, bits: int) -> int:
+    """Codes + fp16 per-block-32 scales of one [n, k] quantised weight."""
+    return (n * k if bits == 8 else n * k // 2) + n * (k // 32) * 2
+
+
+def mlp_bytes(wl, S: int) -> int:
+    """One dense SwiGLU MLP window: gate, up, down weights + x in + h out and
+    back in (fp16) + y out (fp32)."""
+    return (2 * weight_bytes(wl.inter, wl.h, wl.bits) + weight_bytes(wl.h, wl.inter, wl.bits)
+            + S * wl.h * 2 + 2 * S * wl.inter * 2 + S * wl.h * 4)
+
+
+def moe_expert_bytes(wl) -> int:
+    return 2 * weight_bytes(wl.inter, wl.h, wl.bits) + weight_bytes(wl.h, wl.inter, wl.bits)
+
+
+def moe_bytes(wl, S: int, n_hit: int) -> int:
+    """One MoE window: the distinct hit experts' weights + x in + router
+    logits in + out."""
+    return n_hit * moe_expert_bytes(wl) + S * wl.h * 2 + S * wl.experts * 4 + S * wl.h * 4
+
+
 # ---- CPU oracle (the reference arm and the cpu_baseline leg) ----------------------
 
 def oracle_sample(wl, S: int, budget_s: float):
-    """Time the CPU oracle's verify-head arithmetic on a bounded row sample of
-    one window and scale to windows/s.  Returns (windows/s, description)."""
-    from oracle import quant, verify
-    rows = 4096
-    w = W.head_weights(wl, slice(0, rows))
-    codes, scales = quant.quantize_block32(w, wl.bits)
+    """Time the CPU oracle on a bounded sample of one window and scale to a
+    full window.  Returns (windows/s, description)."""
+    from oracle import mlp, quant, verify
     x = W.activations(wl, 0, S)
-    done, t_used = 0, 0.0
-    t0 = time.perf_counter()
-    while True:
-        y = verify.dequant_gemm64(x, codes, scales)
-        verify.argmax_rows(y.astype(np.float32))
-        done += rows
-        t_used = time.perf_counter() - t0
-        if t_used >= budget_s or done >= wl.n:
-            break
-    per_window = t_used * wl.n / done
-    desc = (f"oracle dequant GEMM + argmax on {done} of {wl.n} vocab rows of window 0 "
-            f"({rows}-row batches, {t_used:.1f} s), scaled to a full window")
-    return 1.0 / per_window, desc
+    done, t_used, total = 0, 0.0, 0
+    if wl.kind == "head":
+        rows = 4096
+        w = W.head_weights(wl, slice(0, rows))
+        codes, scales = quant.quantize_block32(w, wl.bits)
+        total = wl.n
+        t0 = time.perf_counter()
+        while True:
+            y = verify.dequant_gemm64(x, codes, scales)
+            verify.argmax_rows(y.astype(np.float32))
+            done += rows
+            t_used = time.perf_counter() - t0
+            if t_used >= budget_s or done >= total:
+                break
+        what = f"oracle dequant GEMM + argmax on {done} of {total} vocab rows of window 0"
+    elif wl.kind == "mlp":
+        # a row block of gate/up (SwiGLU) and of down per round; rows scale linearly
+        rows = 1024
+        rng = np.random.default_rng(0)
+        wg = rng.normal(0, 0.02, (rows, wl.h)).astype(np.float32)
+        wd = rng.normal(0, 0.02, (rows, wl.inter)).astype(np.float32)
+        cg, sg = quant.quantize_block32(wg, wl.bits)
+        cd, sd = quant.quantize_block32(wd, wl.bits)
+        h = rng.normal(0, 1, (S, wl.inter)).astype(np.float16)
+        total = wl.inter + wl.h  # gate/up row pairs + down rows
+        t0 = time.perf_counter()
+        while True:
+            mlp.qlinear_swiglu(x, cg, sg, cg, sg)
+            verify.dequant_gemm64(h, cd, sd)
+            done += 2 * rows
+            t_used = time.perf_counter() - t0
+            if t_used >= budget_s or done >= total:
+                break
+        what = f"oracle SwiGLU + down on {done} of {total} weight rows (gate/up pairs + down) of window 0"
+    else:
+        # routed (row, expert) pairs of window 0 through the oracle's expert MLP
+        logits = W.router_logits(wl, 0, S)
+        ids, _ = mlp.route_topk(logits, wl.top_k)
+        E, I, H = wl.experts, wl.inter, wl.h
+        rng = np.random.default_rng(0)
+        one = {}
+        for t, shape in (("gate", (I, H)), ("up", (I, H)), ("down", (H, I))):
+            one[t] = quant.quantize_block32(rng.normal(0, 0.02, shape).astype(np.float32), wl.bits)
+        total = S * wl.top_k
+        t0 = time.perf_counter()
+        while True:
+            s = done // wl.top_k
+            mlp.expert_swiglu64(x[s:s + 1], 0, I, H, one["gate"], one["up"], one["down"])
+            done += 1
+            t_used = time.perf_counter() - t0
+            if t_used >= budget_s or done >= total:
+                break
+        what = f"oracle route + expert SwiGLU MLP on {done} of {total} routed pairs of window 0"
+    per_window = t_used * total / done
+    return 1.0 / per_window, f"{what} ({t_used:.1f} s), scaled to a full window"
+
+
+def workload_name(wl, S: int) -> str:
+    if wl.kind == "head":
+        return f"{wl.name}: verify head {wl.n}x{wl.h} int{wl.bits} per-block-32, S={S}"
+    if wl.kind == "mlp":
+        return (f"{wl.name}: SwiGLU MLP gate/up {wl.inter}x{wl.h}, down {wl.h}x{wl.inter} "
+                f"int{wl.bits} per-block-32, S={S}")
+    return (f"{wl.name}: MoE {wl.experts} experts (gate/up {wl.inter}x{wl.h}, down {wl.h}x{wl.inter}) "
+            f"int{wl.bits}, top-{wl.top_k}, S={S}")
 
 
 def run_reference(args, wl, S, world, rank):
@@ -169,17 +247,17 @@ def run_reference(args, wl, S, world, rank):
         return 0
     budget = max(1.0, min(20.0, 60.0 / max(1, args.steps + args.warmup)))
     rates = []
+    desc = ""
     for i in range(args.warmup + args.steps):
         r, desc = oracle_sample(wl, S, budget)
         if i >= args.warmup:
             rates.append(r)
     value = float(np.mean(rates))
-    peak, kind = measured_peak()
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "windows/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000.0 / value, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": f"{wl.name}: head {wl.n}x{wl.h} int{wl.bits}, S={S}", "S": S},
+        "config": {"workload": workload_name(wl, S), "S": S},
         "cpu_baseline": {"value": value, "unit": "windows/s", "cores": os.cpu_count(), "kind": "oracle",
                          "sample": desc},
         "e2e": {"value": value, "unit": "windows/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -188,7 +266,179 @@ def run_reference(args, wl, S, world, rank):
     return 0
 
 
-# ---- GPU path ------------------------------------------------------------------------
+# ---- GPU jobs: resident inputs, one window per step ----------------------------------
+
+class HeadJob:
+    """sdv_verify_head with logits = NULL: one launch per window."""
+
+    def __init__(self, sdv, torch, wl, S, dev, nwin):
+        self.sdv, self.torch, self.wl, self.S, self.dev, self.nwin = sdv, torch, wl, S, dev, nwin
+        w = torch.from_numpy(W.head_weights(wl)).to(dev)
+        self.head = sdv.quantize(w, wl.bits)
+        del w
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+        self.xs = np.stack([W.activations(wl, i, S) for i in range(nwin)])
+        self.x_dev = torch.from_numpy(self.xs.view(np.int16)).to(dev).view(torch.float16)
+        self.ws = sdv.workspace(sdv.SDV_OP_VERIFY_HEAD, wl.n, wl.h, S, device=dev)
+        i32 = torch.int32
+        self.am = torch.empty((nwin, S), dtype=i32, device=dev)
+        self.acc = torch.empty((nwin, 1), dtype=i32, device=dev)
+        self.nxt = torch.empty((nwin, 1), dtype=i32, device=dev)
+        zero_d = torch.zeros((nwin, max(S - 1, 1)), dtype=i32, device=dev)
+        # drafts: the draft rule over this path's own argmax chain (an untimed pre-pass)
+        for i in range(nwin):
+            sdv.sdv_verify_head(self.head, self.x_dev[i], S, zero_d[i], 0, None, self.am[i], self.acc[i],
+                                self.nxt[i], self.ws)
+        chain = self.am.cpu().numpy()
+        dr = np.stack([W.drafts(wl, i, S, chain[i])[0] if S > 1 else np.zeros(1, np.int32) for i in range(nwin)])
+        self.dr = np.ascontiguousarray(dr.reshape(nwin, -1))
+        self.d_dev = torch.from_numpy(self.dr).to(dev)
+        self.n_valid = S - 1
+        self.launches = 1
+        self.kernel = "verify-head GEMM + argmax + accept (one launch)"
+        self.ws_list = [self.ws]
+
+    def bytes(self, i):
+        return head_bytes(self.wl, self.S)
+
+    def step(self, i):
+        j = i % self.nwin
+        self.sdv.sdv_verify_head(self.head, self.x_dev[j], self.S, self.d_dev[j], self.n_valid, None, self.am[j],
+                                 self.acc[j], self.nxt[j], self.ws)
+
+    def e2e_setup(self):
+        t, S, dev = self.torch, self.S, self.dev
+        self.x_host = t.from_numpy(self.xs.view(np.int16)).view(t.float16).pin_memory()
+        self.d_host = t.from_numpy(self.dr).pin_memory()
+        self.x_stage = t.empty_like(self.x_dev[0])
+        self.d_stage = t.empty_like(self.d_dev[0])
+        self.out_host = t.empty((self.nwin, S + 2), dtype=t.int32).pin_memory()
+        self.am1 = t.empty(S, dtype=t.int32, device=dev)
+        self.acc1 = t.empty(1, dtype=t.int32, device=dev)
+        self.nxt1 = t.empty(1, dtype=t.int32, device=dev)
+        self.h2d = S * self.wl.h * 2 + self.dr.shape[1] * 4
+        self.d2h = (S + 2) * 4
+
+    def e2e_step(self, i):
+        j, S = i % self.nwin, self.S
+        self.x_stage.copy_(self.x_host[j], non_blocking=True)
+        self.d_stage.copy_(self.d_host[j], non_blocking=True)
+        self.sdv.sdv_verify_head(self.head, self.x_stage, S, self.d_stage, self.n_valid, None, self.am1,
+                                 self.acc1, self.nxt1, self.ws)
+        self.out_host[j, :S].copy_(self.am1, non_blocking=True)
+        self.out_host[j, S:S + 1].copy_(self.acc1, non_blocking=True)
+        self.out_host[j, S + 1:].copy_(self.nxt1, non_blocking=True)
+
+
+class MlpJob:
+    """Dense SwiGLU MLP: sdv_qlinear_swiglu (gate/up) then sdv_qlinear (down)."""
+
+    def __init__(self, sdv, torch, wl, S, dev, nwin):
+        self.sdv, self.torch, self.wl, self.S, self.dev, self.nwin = sdv, torch, wl, S, dev, nwin
+        self.w = {}
+        for which in ("gate", "up", "down"):
+            w = torch.from_numpy(W.mlp_weights(wl, which)).to(dev)
+            self.w[which] = sdv.quantize(w, wl.bits)
+            del w
+            torch.cuda.synchronize()
+            torch.cuda.empty_cache()
+        self.xs = np.stack([W.activations(wl, i, S) for i in range(nwin)])
+        self.x_dev = torch.from_numpy(self.xs.view(np.int16)).to(dev).view(torch.float16)
+        self.h = torch.empty((S, wl.inter), dtype=torch.float16, device=dev)
+        self.y = torch.empty((nwin, S, wl.h), dtype=torch.float32, device=dev)
+        self.ws_sw = sdv.workspace(sdv.SDV_OP_QLINEAR_SWIGLU, wl.inter, wl.h, S, device=dev)
+        self.ws_dn = sdv.workspace(sdv.SDV_OP_QLINEAR, wl.h, wl.inter, S, device=dev)
+        self.launches = 4  # swiglu: dual GEMM + SwiGLU reduce; down: GEMM + split-K reduce
+        self.kernel = "gate/up + down GEMMs (sdv_qlinear_swiglu + sdv_qlinear)"
+        self.ws_list = [self.ws_sw, self.ws_dn]
+
+    def bytes(self, i):
+        return mlp_bytes(self.wl, self.S)
+
+    def _call(self, x, y):
+        sdv = self.sdv
+        sdv.sdv_qlinear_swiglu(self.w["gate"], self.w["up"], x, self.S, self.h, self.ws_sw)
+        sdv.sdv_qlinear(self.w["down"], self.h, self.S, y, self.ws_dn)
+
+    def step(self, i):
+        j = i % self.nwin
+        self._call(self.x_dev[j], self.y[j])
+
+    def e2e_setup(self):
+        t = self.torch
+        self.x_host = t.from_numpy(self.xs.view(np.int16)).view(t.float16).pin_memory()
+        self.x_stage = t.empty_like(self.x_dev[0])
+        self.y1 = t.empty_like(self.y[0])
+        self.out_host = t.empty((self.nwin,) + tuple(self.y1.shape), dtype=t.float32).pin_memory()
+        self.h2d = self.S * self.wl.h * 2
+        self.d2h = self.S * self.wl.h * 4
+
+    def e2e_step(self, i):
+        j = i % self.nwin
+        self.x_stage.copy_(self.x_host[j], non_blocking=True)
+        self._call(self.x_stage, self.y1)
+        self.out_host[j].copy_(self.y1, non_blocking=True)
+
+
+class MoeJob:
+    """sdv_moe_gather_qmm: route + group, gate/up over the hit experts, down."""
+
+    def __init__(self, sdv, torch, wl, S, dev, nwin):
+        self.sdv, self.torch, self.wl, self.S, self.dev, self.nwin = sdv, torch, wl, S, dev, nwin
+        self.w = {}
+        for which in ("gate", "up", "down"):
+            w = torch.from_numpy(W.moe_weights(wl, which)).to(dev)
+            self.w[which] = sdv.quantize(w, wl.bits)
+            del w
+            torch.cuda.synchronize()
+            torch.cuda.empty_cache()
+        self.xs = np.stack([W.activations(wl, i, S) for i in range(nwin)])
+        self.ls = np.stack([W.router_logits(wl, i, S) for i in range(nwin)])
+        self.x_dev = torch.from_numpy(self.xs.view(np.int16)).to(dev).view(torch.float16)
+        self.l_dev = torch.from_numpy(self.ls).to(dev)
+        self.out = torch.empty((nwin, S, wl.h), dtype=torch.float32, device=dev)
+        self.ws = sdv.workspace(sdv.SDV_OP_MOE, wl.inter, wl.h, S, wl.experts, wl.top_k, device=dev)
+        # distinct experts each window hits (for its algorithmic bytes)
+        from oracle import mlp
+        self.n_hit = [len(np.unique(mlp.route_topk(self.ls[i], wl.top_k)[0])) for i in range(nwin)]
+        self.launches = 5  # route+group, gate/up GEMM, SwiGLU reduce, down GEMM, split reduce
+        self.kernel = "MoE call (route, gate/up GEMM, SwiGLU, down GEMM, reduce)"
+        self.ws_list = [self.ws]
+
+    def bytes(self, i):
+        return moe_bytes(self.wl, self.S, self.n_hit[i % self.nwin])
+
+    def _call(self, x, l, out):
+        wl = self.wl
+        self.sdv.sdv_moe_gather_qmm(self.w["gate"], self.w["up"], self.w["down"], wl.experts, wl.inter, wl.h,
+                                    wl.top_k, x, l, self.S, out, None, None, self.ws)
+
+    def step(self, i):
+        j = i % self.nwin
+        self._call(self.x_dev[j], self.l_dev[j], self.out[j])
+
+    def e2e_setup(self):
+        t = self.torch
+        self.x_host = t.from_numpy(self.xs.view(np.int16)).view(t.float16).pin_memory()
+        self.l_host = t.from_numpy(self.ls).pin_memory()
+        self.x_stage = t.empty_like(self.x_dev[0])
+        self.l_stage = t.empty_like(self.l_dev[0])
+        self.o1 = t.empty_like(self.out[0])
+        self.out_host = t.empty((self.nwin,) + tuple(self.o1.shape), dtype=t.float32).pin_memory()
+        self.h2d = self.S * self.wl.h * 2 + self.S * self.wl.experts * 4
+        self.d2h = self.S * self.wl.h * 4
+
+    def e2e_step(self, i):
+        j = i % self.nwin
+        self.x_stage.copy_(self.x_host[j], non_blocking=True)
+        self.l_stage.copy_(self.l_host[j], non_blocking=True)
+        self._call(self.x_stage, self.l_stage, self.o1)
+        self.out_host[j].copy_(self.o1, non_blocking=True)
+
+
+JOBS = {"head": HeadJob, "mlp": MlpJob, "moe": MoeJob}
+
 
 def run_sdv(args, wl, S, world, rank, local):
     import torch
@@ -199,39 +449,18 @@ def run_sdv(args, wl, S, world, rank, local):
     sdv.sdv_set_gemm_path({"auto": 0, "mma": 1, "tc": 2}[args.path])
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
-
-    # resident inputs: weights (quantised on the GPU), all windows' activations and drafts
-    w = torch.from_numpy(W.head_weights(wl)).to(dev)
-    head = sdv.quantize(w, wl.bits)
-    del w
-    torch.cuda.synchronize()
-    torch.cuda.empty_cache()
     nwin = min(wl.windows, max(1, args.windows))
-    xs = np.stack([W.activations(wl, i, S) for i in range(nwin)])
-    x_dev = torch.from_numpy(xs.view(np.int16)).to(dev).view(torch.float16)
-    ws = sdv.workspace(sdv.SDV_OP_VERIFY_HEAD, wl.n, wl.h, S, device=dev)
-    am = torch.empty((nwin, S), dtype=torch.int32, device=dev)
-    acc = torch.empty((nwin, 1), dtype=torch.int32, device=dev)
-    nxt = torch.empty((nwin, 1), dtype=torch.int32, device=dev)
-    zero_d = torch.zeros((nwin, max(S - 1, 1)), dtype=torch.int32, device=dev)
-    # drafts: the draft rule over this path's own argmax chain (an untimed pre-pass)
-    for i in range(nwin):
-        sdv.sdv_verify_head(head, x_dev[i], S, zero_d[i], 0, None, am[i], acc[i], nxt[i], ws)
-    chain = am.cpu().numpy()
-    dr = np.stack([W.drafts(wl, i, S, chain[i])[0] if S > 1 else np.zeros(1, np.int32) for i in range(nwin)])
-    d_dev = torch.from_numpy(np.ascontiguousarray(dr.reshape(nwin, -1))).to(dev)
-    n_valid = S - 1
+    job = JOBS[wl.kind](sdv, torch, wl, S, dev, nwin)
     stream = torch.cuda.current_stream()
 
-    def step(i):
-        j = i % nwin
-        sdv.sdv_verify_head(head, x_dev[j], S, d_dev[j], n_valid, None, am[j], acc[j], nxt[j], ws)
+    def status_ok():
+        return all(sdv.sdv_device_status(w) == sdv.SDV_OK for w in job.ws_list)
 
     for i in range(args.warmup):
-        step(i)
+        job.step(i)
     torch.cuda.synchronize()
-    if sdv.sdv_device_status(ws) != sdv.SDV_OK:
-        raise RuntimeError("device status reported a timeout during warm-up")
+    if not status_ok():
+        raise RuntimeError("device status reported an error during warm-up")
 
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     t_all0, t_all1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -241,56 +470,38 @@ def run_sdv(args, wl, S, world, rank, local):
         t_all0.record(stream)
         for i in range(args.steps):
             ev[i][0].record(stream)
-            step(i)
+            job.step(i)
             ev[i][1].record(stream)
         t_all1.record(stream)
         torch.cuda.synchronize()
     barrier(world)
     elapsed_ms = t_all0.elapsed_time(t_all1)
-    kernel_ms = float(np.mean([a.elapsed_time(b) for a, b in ev]))
-    if sdv.sdv_device_status(ws) != sdv.SDV_OK:
-        raise RuntimeError("device status reported a timeout during the timed region")
+    per_ms = [a.elapsed_time(b) for a, b in ev]
+    kernel_ms = float(np.mean(per_ms))
+    if not status_ok():
+        raise RuntimeError("device status reported an error during the timed region")
     elapsed_ms = max_over_ranks(world, elapsed_ms, dev)
     kernel_ms = max_over_ranks(world, kernel_ms, dev)
+    nbytes = float(np.mean([job.bytes(i) for i in range(args.steps)]))
 
     # end to end through the C ABI with host buffers: H2D of the window's inputs,
-    # the call, D2H of the ids, every step
-    x_host = torch.from_numpy(xs.view(np.int16)).view(torch.float16).pin_memory()
-    d_host = torch.from_numpy(np.ascontiguousarray(dr.reshape(nwin, -1))).pin_memory()
-    x_stage = torch.empty_like(x_dev[0])
-    d_stage = torch.empty_like(d_dev[0])
-    out_host = torch.empty((nwin, S + 2), dtype=torch.int32).pin_memory()
-    am1 = torch.empty(S, dtype=torch.int32, device=dev)
-    acc1 = torch.empty(1, dtype=torch.int32, device=dev)
-    nxt1 = torch.empty(1, dtype=torch.int32, device=dev)
-
-    def e2e_step(i):
-        j = i % nwin
-        x_stage.copy_(x_host[j], non_blocking=True)
-        d_stage.copy_(d_host[j], non_blocking=True)
-        sdv.sdv_verify_head(head, x_stage, S, d_stage, n_valid, None, am1, acc1, nxt1, ws)
-        out_host[j, :S].copy_(am1, non_blocking=True)
-        out_host[j, S:S + 1].copy_(acc1, non_blocking=True)
-        out_host[j, S + 1:].copy_(nxt1, non_blocking=True)
-
+    # the call, D2H of the result, every step
+    job.e2e_setup()
     for i in range(args.warmup):
-        e2e_step(i)
+        job.e2e_step(i)
     torch.cuda.synchronize()
     barrier(world)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for i in range(args.steps):
-        e2e_step(i)
+        job.e2e_step(i)
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(world, e0.elapsed_time(e1), dev)
-    h2d = S * wl.h * 2 + max(S - 1, 1) * 4
-    d2h = (S + 2) * 4
 
     if rank != 0:
         return 0
     value = world * args.steps / (elapsed_ms / 1000.0)
-    nbytes = head_bytes(wl, S)
     peak, kind = measured_peak()
     achieved = nbytes / (kernel_ms / 1000.0) / 1e9
     cpu_rate, cpu_desc = oracle_sample(wl, S, args.cpu_budget) if args.cpu_budget > 0 else (None, "skipped")
@@ -298,19 +509,18 @@ def run_sdv(args, wl, S, world, rank, local):
         "metric": METRIC, "value": value, "unit": "windows/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": elapsed_ms / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f16 x int%d -> f32" % wl.bits, "data": "synthetic",
-        "config": {"workload": f"{wl.name}: verify head {wl.n}x{wl.h} int{wl.bits} per-block-32, S={S}",
-                   "S": S, "windows": nwin, "bytes_per_window": nbytes,
+        "config": {"workload": workload_name(wl, S), "S": S, "windows": nwin, "bytes_per_window": nbytes,
                    "l2": "inputs larger than L2 (weight stream %.0f MB > 129 MB)" % (nbytes / 1e6),
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "weight_gbs": achieved, "hbm_frac": achieved / peak,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                     "traffic": None, "peak_kind": kind, "kernel": f"verify-head GEMM ({args.path} path)",
-                     "kernel_ms": kernel_ms},
+                     "traffic": None, "peak_kind": kind, "kernel": f"{job.kernel} ({args.path} path)",
+                     "kernel_ms": kernel_ms, "kernel_ms_min": float(np.min(per_ms))},
         "cpu_baseline": {"value": cpu_rate, "unit": "windows/s", "cores": os.cpu_count(), "kind": "oracle",
                          "sample": cpu_desc},
         "e2e": {"value": world * args.steps / (e2e_ms / 1000.0), "unit": "windows/s",
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-        "gpu_launches": args.steps,
+                "h2d_bytes_per_step": job.h2d, "d2h_bytes_per_step": job.d2h},
+        "gpu_launches": args.steps * job.launches,
         "clocks": clk.summary(),
     }
     print(json.dumps(line))
@@ -323,7 +533,7 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["sdv", "reference"], default="sdv")
-    ap.add_argument("--config", default="q4b", choices=["tiny", "q4b", "a3b"])
+    ap.add_argument("--config", default="q4b", choices=["tiny", "q4b", "a3b", "mlp27", "moe"])
     ap.add_argument("--S", type=int, default=0)
     ap.add_argument("--windows", type=int, default=200)
     ap.add_argument("--cpu-budget", type=float, default=10.0)

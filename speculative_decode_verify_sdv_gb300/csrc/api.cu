@@ -124,16 +124,16 @@ GemmPlan plan_gemm(int qbits, int n, int k, int S, bool allow_split) {
   const int tiles = (n + 15) / 16;
   const int warps_total = sms * sdv::gemm_warps_per_cta();
   const int kst = (k + 255) / 256;
-  int splits = 1;
+  int want = 1;  // requested splits; rounding the chunk to 256 may give fewer
   if (allow_split) {
-    splits = (4 * warps_total + tiles - 1) / tiles;
-    if (splits > kst) splits = kst;
-    if (splits < 1) splits = 1;
+    want = (4 * warps_total + tiles - 1) / tiles;
+    if (want > kst) want = kst;
+    if (want < 1) want = 1;
   }
-  for (;;) {
-    int k_chunk = k;
-    if (splits > 1) {
-      k_chunk = ((k + splits - 1) / splits + 255) / 256 * 256;
+  for (;; ++want) {
+    int k_chunk = k, splits = 1;
+    if (want > 1) {
+      k_chunk = ((k + want - 1) / want + 255) / 256 * 256;
       splits = (k + k_chunk - 1) / k_chunk;
     }
     int smem = 0;
@@ -149,8 +149,7 @@ GemmPlan plan_gemm(int qbits, int n, int k, int S, bool allow_split) {
       pl.grid = grid < 1 ? 1 : grid;
       return pl;
     }
-    if (!allow_split || splits >= kst) return GemmPlan{};
-    ++splits;
+    if (!allow_split || want >= kst) return GemmPlan{};
   }
 }
 
@@ -160,7 +159,7 @@ std::atomic<int> g_gemm_path{0};
 
 // tcgen05 path plan: 128-row tiles, one CTA per SM; split-K (Y only) until the
 // tiles cover the SMs and the window rows of one split fit next to a ring of at
-// least three stages.
+// least four stages.
 GemmPlan plan_tc(int qbits, int n, int k, int S, bool allow_split) {
   GemmPlan pl;
   const int sms = device_sms();
@@ -168,18 +167,18 @@ GemmPlan plan_tc(int qbits, int n, int k, int S, bool allow_split) {
   if (sms <= 0 || limit <= 0) return pl;
   const int tiles = (n + 127) / 128;
   const int kst = (k + 255) / 256;
-  int splits = 1;
+  int want = 1;  // requested splits; rounding the chunk to 256 may give fewer
   if (allow_split) {
-    splits = (sms + tiles - 1) / tiles;
-    if (splits > kst) splits = kst;
+    want = (sms + tiles - 1) / tiles;
+    if (want > kst) want = kst;
   }
-  for (;;) {
-    int k_chunk = k;
-    if (splits > 1) {
-      k_chunk = ((k + splits - 1) / splits + 255) / 256 * 256;
+  for (;; ++want) {
+    int k_chunk = k, splits = 1;
+    if (want > 1) {
+      k_chunk = ((k + want - 1) / want + 255) / 256 * 256;
       splits = (k + k_chunk - 1) / k_chunk;
     }
-    for (int d = kMaxDepth; d >= 3; --d) {
+    for (int d = kMaxDepth; d >= 4; --d) {  // tc_plan_valid rejects shallower rings
       const int b = sdv::tc_smem_bytes(qbits, S, k_chunk, d);
       if (b <= limit && sdv::tc_plan_valid(qbits, S, k_chunk, d)) {
         pl.splits = splits;
@@ -188,15 +187,15 @@ GemmPlan plan_tc(int qbits, int n, int k, int S, bool allow_split) {
         // at least half the SM's shared memory: one CTA (one 512-column tensor
         // memory allocation) per SM
         pl.smem = b > limit / 2 + 1024 ? b : limit / 2 + 1024;
-        int grid = (sms + splits - 1) / splits;
+        // one wave: at most one CTA per SM over all splits
+        int grid = sms / splits;
         if (grid > tiles) grid = tiles;
         pl.grid = grid < 1 ? 1 : grid;
         pl.tc = true;
         return pl;
       }
     }
-    if (!allow_split || splits >= kst) return GemmPlan{};
-    ++splits;
+    if (!allow_split || want >= kst) return GemmPlan{};
   }
 }
 
@@ -340,7 +339,7 @@ struct MoeLayout {
   int n_cap = 0;       // most experts a window can hit: min(E, S * top_k)
   int gx = 0, ys = 0;  // down projection: CTAs per split, splits (expert-segment slots)
   GemmPlan gu, dn;     // gate/up and down launch plans
-  size_t ids, w, offsets, pair_rows, n_hit, hit, row_w, gu_part, hbuf, dn_part, total;
+  size_t ids, w, offsets, pair_rows, n_hit, hit, row_w, hbuf, dn_part, total;
 };
 
 MoeLayout plan_moe(int qbits, int E, int I, int H, int top_k, int S) {
@@ -362,7 +361,7 @@ MoeLayout plan_moe(int qbits, int E, int I, int H, int top_k, int S) {
     if (ys < 1) continue;
     const int segs = (L.n_cap + ys - 1) / ys;
     const int k_chunk = segs * I;
-    for (int d = kMaxDepth; d >= 3; --d) {
+    for (int d = kMaxDepth; d >= 4; --d) {  // tc_plan_valid rejects shallower rings
       const int b = sdv::tc_smem_bytes(qbits, S, k_chunk, d);
       if (b <= limit && sdv::tc_plan_valid(qbits, S, k_chunk, d)) {
         L.dn.splits = ys;
@@ -392,7 +391,6 @@ MoeLayout plan_moe(int qbits, int E, int I, int H, int top_k, int S) {
   L.n_hit = take(4);
   L.hit = take((size_t)E * 4);
   L.row_w = take((size_t)S * L.n_cap * 4);
-  L.gu_part = take((size_t)S * 2 * L.n_cap * I * 4);
   L.hbuf = take((size_t)S * L.n_cap * I * 2);
   L.dn_part = take((size_t)L.ys * S * H * 4);
   L.total = o;
@@ -541,6 +539,12 @@ sdv_status sdv_qlinear_swiglu(const sdv_qweight* gate, const sdv_qweight* up, co
     a.S = S;
     a.N = n;
     a.K = k;
+    if (pl.splits == 1) {  // SwiGLU in the GEMM epilogue
+      a.dual = 2;
+      a.h = hh;
+      a.ldh = n;
+      return launch_tc_y(gate, up, pl, a, ws, st);
+    }
     a.ldy = 2 * n;
     a.dual = 1;
     a.y = part;
@@ -598,7 +602,6 @@ sdv_status sdv_moe_gather_qmm(const sdv_qweight* gate, const sdv_qweight* up, co
   int32_t* const n_hit = reinterpret_cast<int32_t*>(w8 + L.n_hit);
   int32_t* const hit = reinterpret_cast<int32_t*>(w8 + L.hit);
   float* const row_w = reinterpret_cast<float*>(w8 + L.row_w);
-  float* const gu = reinterpret_cast<float*>(w8 + L.gu_part);
   __half* const hb = reinterpret_cast<__half*>(w8 + L.hbuf);
   float* const dn = reinterpret_cast<float*>(w8 + L.dn_part);
   const int ncap_i = L.n_cap * I;
@@ -607,26 +610,26 @@ sdv_status sdv_moe_gather_qmm(const sdv_qweight* gate, const sdv_qweight* up, co
                                         reinterpret_cast<int32_t*>(w8 + L.offsets),
                                         reinterpret_cast<int32_t*>(w8 + L.pair_rows), n_hit, hit, row_w, L.n_cap, st);
   if (e != cudaSuccess) return cuda_status(e);
-  // a9, gate and up: every window row through each hit expert's rows (dual tiles
-  // over the hit list), fp32 [S][2 * n_cap * I]
+  // a9, gate and up: every window row through each hit expert's rows (gate/up
+  // tile pairs over the hit list) with the SwiGLU epilogue writing
+  // h'[s][j * I + c] = fp16(w(s, hit j) * SiLU(g) * u), zero where row s did not pick hit j
   {
     GemmArgs a{};
     a.x = reinterpret_cast<const __half*>(x);
     a.S = S;
     a.N = ncap_i;
     a.K = H;
-    a.ldy = 2 * ncap_i;
-    a.dual = 1;
+    a.dual = 2;
     a.n_hit = n_hit;
     a.hit = hit;
     a.rows_per_expert = I;
-    a.y = gu;
+    a.h = hb;
+    a.ldh = ncap_i;
+    a.row_w = row_w;
+    a.ldw = L.n_cap;
     sdv_status s = launch_tc_y(gate, up, L.gu, a, ws, st);
     if (s != SDV_OK) return s;
   }
-  // h'[s][j * I + c] = fp16(w(s, hit j) * SiLU(g) * u), zero where row s did not pick hit j
-  e = sdv::launch_swiglu_reduce(gu, 1, 0, 2 * ncap_i, ncap_i, S, ncap_i, hb, ncap_i, row_w, L.n_cap, I, n_hit, st);
-  if (e != cudaSuccess) return cuda_status(e);
   // a9, down and combine: out = h' (hit experts' segments along the reduction) x
   // the hit experts' down rows, split by expert-segment slots, reduced in order
   {

@@ -453,8 +453,17 @@ cudaError_t launch_nt(int nt, const CUtensorMap& tc, const CUtensorMap& tsc, con
 __global__ void splitk_reduce_kernel(const float* __restrict__ part, int splits, long count,
                                      float* __restrict__ y) {
   for (long i = (long)blockIdx.x * blockDim.x + threadIdx.x; i < count; i += (long)gridDim.x * blockDim.x) {
+    // loads in batches of 8 (independent), sums in split order
     float v = part[i];
-    for (int sp = 1; sp < splits; ++sp) v += part[(long)sp * count + i];
+    int sp = 1;
+    for (; sp + 8 <= splits; sp += 8) {
+      float b[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) b[j] = __ldcg(part + (long)(sp + j) * count + i);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) v += b[j];
+    }
+    for (; sp < splits; ++sp) v += __ldcg(part + (long)sp * count + i);
     y[i] = v;
   }
 }

@@ -81,29 +81,36 @@ __global__ void __launch_bounds__(kRouteThreads) moe_route_kernel(
     const float* __restrict__ logits, int S, int E, int top_k, int32_t* __restrict__ ids,
     float* __restrict__ w, int32_t* __restrict__ offsets, int32_t* __restrict__ pair_rows,
     int32_t* __restrict__ n_hit, int32_t* __restrict__ hit, float* __restrict__ row_w, int n_cap) {
-  __shared__ uint32_t sel[kMaxRows][kMaxExperts / 32];
   __shared__ int s_ids[kMaxRows][kMaxTopK];
   __shared__ int cnt[kMaxExperts];
   __shared__ int slot[kMaxExperts];
   __shared__ int wsum[32];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  for (int v = tid; v < kMaxRows * (kMaxExperts / 32); v += blockDim.x) (&sel[0][0])[v] = 0u;
   for (int e = tid; e < kMaxExperts; e += blockDim.x) cnt[e] = 0;
   __syncthreads();
 
   // ---- route: top_k by repeated warp argmax over the unselected experts ----
+  // lane holds experts lane + 32 m in registers; bit m of `taken` marks a selection
   if (warp < S) {
     const float* const row = logits + (long)warp * E;
+    constexpr int kSlots = kMaxExperts / 32;
+    float lv[kSlots];
+#pragma unroll
+    for (int m = 0; m < kSlots; ++m) {
+      const int e = lane + 32 * m;
+      lv[m] = (e < E) ? row[e] : 0.f;
+    }
+    uint32_t taken = 0u;
     float first = 0.f, sum = 0.f;
     float chosen_l[kMaxTopK];
     for (int i = 0; i < top_k; ++i) {
       float bv = -__int_as_float(0x7f800000);  // -inf
       int be = INT32_MAX;
-      for (int e = lane; e < E; e += 32) {
-        if (sel[warp][e >> 5] & (1u << (e & 31))) continue;
-        const float v = row[e];
-        if (route_better(v, e, bv, be)) {
-          bv = v;
+#pragma unroll
+      for (int m = 0; m < kSlots; ++m) {
+        const int e = lane + 32 * m;
+        if (e < E && !((taken >> m) & 1u) && route_better(lv[m], e, bv, be)) {
+          bv = lv[m];
           be = e;
         }
       }
@@ -116,19 +123,20 @@ __global__ void __launch_bounds__(kRouteThreads) moe_route_kernel(
           be = oe;
         }
       }
-      if (lane == 0) sel[warp][be >> 5] |= 1u << (be & 31);
-      __syncwarp();
+      if ((be & 31) == lane) taken |= 1u << (be >> 5);
       if (lane == 0) s_ids[warp][i] = be;
       if (i == 0) first = bv;
-      chosen_l[i < kMaxTopK ? i : 0] = bv;
+      chosen_l[i] = bv;
     }
     // softmax over the selection (the first selected logit is the largest)
     for (int i = 0; i < top_k; ++i) sum += expf(chosen_l[i] - first);
-    if (lane == 0) {
-      for (int i = 0; i < top_k; ++i) {
-        ids[warp * top_k + i] = s_ids[warp][i];
-        w[warp * top_k + i] = expf(chosen_l[i] - first) / sum;
-      }
+    __syncwarp();  // lane 0's s_ids writes, visible to the lanes below
+    if (lane < top_k) {
+      float li = 0.f;
+      for (int i = 0; i < top_k; ++i)
+        if (i == lane) li = chosen_l[i];
+      ids[warp * top_k + lane] = s_ids[warp][lane];
+      w[warp * top_k + lane] = expf(li - first) / sum;
     }
   }
   __syncthreads();

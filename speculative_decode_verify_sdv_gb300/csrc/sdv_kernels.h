@@ -40,13 +40,21 @@ struct GemmArgs {
   int ldx;                  // row stride of x in elements (0: K)
   int ldy;                  // row stride of y in elements (0: N)
   int dual;                 // 1: two weight matrices of N rows each (second tensor maps);
-                            //    output column mat * N + row, mat = 0 for the first
+                            //    output column mat * N + row, mat = 0 for the first;
+                            // 2: the same two matrices as interleaved (first, second) tile
+                            //    pairs with the SwiGLU epilogue: h = SiLU(first) * second
   const int* n_hit;         // device [1]: number of hit experts (MoE), or null
   const int* hit;           // device [n_hit]: expert ids, ascending
   int rows_per_expert;      // rows of one expert in a stacked weight
   int seg_k;                // > 0: the reduction is n_hit segments of seg_k columns, segment j
                             //    reading expert hit[j]'s rows; split y covers segments
                             //    [y * n_hit / splits, (y + 1) * n_hit / splits)
+  // SwiGLU epilogue (dual == 2, one split): h[s * ldh + row] = fp16(SiLU(g) * u
+  // [* row_w[s * ldw + row / rows_per_expert]])
+  __half* h;
+  int ldh;
+  const float* row_w;
+  int ldw;
 };
 
 int gemm_tile_mt(int qbits);

@@ -49,6 +49,7 @@ namespace {
 constexpr int kTileRows = 128;
 constexpr uint32_t kTmemCols = 512;
 constexpr int kABufs = 3;        // A operand stage buffers in tensor memory
+constexpr int kMinDepth = 4;     // ring stages (see tc_plan_valid)
 constexpr int kACols = kABufs * 128;
 
 struct TcRoles {
@@ -132,8 +133,13 @@ __global__ void __launch_bounds__(TcRoles::kThreads, 1)
   const int ldy = p.ldy > 0 ? p.ldy : p.N;
   // tile t -> (matrix, tile within the matrix, first weight row)
   auto tile_split = [&](int t, int& mat, int& lt) {
-    mat = (p.dual && t >= t_one) ? 1 : 0;
-    lt = t - mat * t_one;
+    if (p.dual == 2) {  // interleaved (first, second) pairs
+      mat = t & 1;
+      lt = t >> 1;
+    } else {
+      mat = (p.dual && t >= t_one) ? 1 : 0;
+      lt = t - mat * t_one;
+    }
   };
   auto tile_map = [&](int t, int& mat, int& lt) -> int {
     tile_split(t, mat, lt);
@@ -145,10 +151,11 @@ __global__ void __launch_bounds__(TcRoles::kThreads, 1)
     return lt * kTileRows;
   };
 
-  // tiles of this CTA
+  // tiles of this CTA (whole pairs for the SwiGLU epilogue)
   const int tiles = p.dual ? 2 * t_one : t_one;
-  const int tile_lo = (int)((long)blockIdx.x * tiles / gridDim.x);
-  const int tile_hi = (int)((long)(blockIdx.x + 1) * tiles / gridDim.x);
+  const int unit = (p.dual == 2) ? 2 : 1;
+  const int tile_lo = unit * (int)((long)blockIdx.x * (tiles / unit) / gridDim.x);
+  const int tile_hi = unit * (int)((long)(blockIdx.x + 1) * (tiles / unit) / gridDim.x);
   const int ntile = tile_hi - tile_lo;
   if (MODE == kModeY && k_len <= 0) {
     // an empty reduction range still owns its split's partial outputs: zeros
@@ -352,6 +359,14 @@ __global__ void __launch_bounds__(TcRoles::kThreads, 1)
       tc_commit_elect(bar_afree + 8 * ab);
       if (ks == kst - 1) tc_commit_elect(bar_tfull + 8 * tb);
     }
+    // No asynchronous arrive may outlive the CTA (a late one would land in the
+    // shared memory of the next CTA on this SM): wait for the A-buffer releases of
+    // the last stages, which no converter waits for.  The epilogue waits for every
+    // tile's commit.
+    for (int d = max(0, nstages - kABufs); d < nstages; ++d) {
+      const Cursor cd = cursor_at(d);
+      if (!wait_warp(bar_afree + 8 * cd.ab, cd.abphase)) break;
+    }
   } else if (warp < R::kConv0) {
     // ---------------- tile epilogue (one warp per tensor-memory lane quarter) --------
     const int q = warp & 3;
@@ -360,6 +375,7 @@ __global__ void __launch_bounds__(TcRoles::kThreads, 1)
     float* const red = reinterpret_cast<float*>(sb + pl.red_off) + q * p.S * 33;  // [S][33]
     float run_v = -FLT_MAX;  // running best of column n = lane
     int run_i = INT_MAX;
+    const int tpe = p.rows_per_expert > 0 ? p.rows_per_expert / kTileRows : 1;
     for (int t = 0; t < ntile; ++t) {
       const int tb = t & 1;
       if (!wait_warp(bar_tfull + 8 * tb, (t >> 1) & 1)) break;
@@ -389,7 +405,25 @@ __global__ void __launch_bounds__(TcRoles::kThreads, 1)
       tile_split(tile_lo + t, mat, lt);
       const int lrow = lt * kTileRows + r;  // row within its matrix
       const bool valid = lrow < n_one;
-      if (p.y != nullptr && valid) {
+      if (MODE == kModeY && p.dual == 2) {
+        // the pair's first tile waits in this warp's shared-memory rows (lane = row)
+        if (mat == 0) {
+#pragma unroll
+          for (int n = 0; n < 32; ++n)
+            if (n < p.S) red[n * 33 + lane] = acc[n];
+        } else if (valid) {
+          const float* const rw = (p.row_w != nullptr) ? p.row_w + lt / tpe : nullptr;
+#pragma unroll
+          for (int n = 0; n < 32; ++n) {
+            if (n < p.S) {
+              const float g = red[n * 33 + lane];
+              float v = g / (1.f + expf(-g)) * acc[n];
+              if (rw != nullptr) v *= rw[(size_t)n * p.ldw];
+              p.h[(size_t)n * p.ldh + lrow] = __float2half_rn(v);
+            }
+          }
+        }
+      } else if (p.y != nullptr && valid) {
         float* const yo = p.y + (size_t)blockIdx.y * p.S * ldy + mat * p.N + lrow;
 #pragma unroll
         for (int n = 0; n < 32; ++n)
@@ -591,10 +625,20 @@ int tc_smem_bytes(int qbits, int S, int k_chunk, int depth) {
 
 // The aliased 8-row groups of N read up to one group stride past the staged
 // rows; the ring behind them must be at least that long.
+//
+// The ring needs at least kMinDepth stages.  Converter group g takes stages g,
+// g+2, ...; before it waits on slot (i % depth) for stage i, the slot's previous
+// phase (stage i - depth) must be complete, else the parity wait would match the
+// phase before that and return early.  With an even depth the previous user is
+// the same group (already past it); with an odd depth >= 5 the group's own
+// wait at stage i - 2 for the A-buffer release of stage i - 5 implies, by the
+// in-order MMAs, that stage i - depth was converted.  Depth 3 has no such
+// guarantee: the other group's stage i - 3 may not even have landed.
 bool tc_plan_valid(int qbits, int S, int k_chunk, int depth) {
+  if (depth < kMinDepth) return false;
   const TcPlan p = tc_plan(qbits, S, k_chunk, depth);
   const int ring_bytes = depth * p.code_stage;
-  const int over = (p.nmma - p.xrows) * k_chunk * 2;  // bytes of missing groups
+  const int over = (p.nmma - p.xrows) * p.kpad * 2;  // bytes of missing groups
   return over <= ring_bytes;
 }
 
