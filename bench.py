@@ -58,6 +58,45 @@ def measured_peak():
         return 6800.0, "fallback"
 
 
+KERNEL_SOURCES = ("tc_gemm.cu", "sdv_device.cuh", "sdv_kernels.h")
+
+
+def kernel_source_hash() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "speculative_decode_verify_sdv_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload: str):
+    """DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) from
+    the committed ncu summary of this workload, or None when there is none or the
+    kernel sources changed since it was taken."""
+    pdir = os.path.join(ROOT, "profiles")
+    try:
+        names = sorted(os.listdir(pdir))
+    except OSError:
+        return None, None
+    cur = kernel_source_hash()
+    for name in names:
+        if not name.endswith(".md"):
+            continue
+        fields = {}
+        with open(os.path.join(pdir, name)) as fh:
+            for line in fh:
+                if ":" in line and line.split(":", 1)[0] in ("kernel_source_sha256", "workload",
+                                                             "traffic_bytes_per_launch"):
+                    k, v = line.split(":", 1)
+                    fields[k] = v.strip()
+        if fields.get("workload") == workload and "traffic_bytes_per_launch" in fields:
+            if fields.get("kernel_source_sha256") != cur:
+                return None, f"profiles/{name} (stale: kernel changed since the capture)"
+            return float(fields["traffic_bytes_per_launch"]), f"profiles/{name}"
+    return None, None
+
+
 class ClockSampler:
     """nvidia-smi clocks and throttle reasons, sampled during the timed region."""
 
@@ -504,6 +543,7 @@ def run_sdv(args, wl, S, world, rank, local):
     value = world * args.steps / (elapsed_ms / 1000.0)
     peak, kind = measured_peak()
     achieved = nbytes / (kernel_ms / 1000.0) / 1e9
+    traffic, traffic_src = (profiled_traffic(f"{wl.name} S={S}") if wl.kind == "head" else (None, None))
     cpu_rate, cpu_desc = oracle_sample(wl, S, args.cpu_budget) if args.cpu_budget > 0 else (None, "skipped")
     line = {
         "metric": METRIC, "value": value, "unit": "windows/s", "n_gpus": world, "steps": args.steps,
@@ -514,7 +554,7 @@ def run_sdv(args, wl, S, world, rank, local):
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "weight_gbs": achieved, "hbm_frac": achieved / peak,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                     "traffic": None, "peak_kind": kind, "kernel": f"{job.kernel} ({args.path} path)",
+                     "traffic": traffic, "traffic_source": traffic_src, "peak_kind": kind, "kernel": f"{job.kernel} ({args.path} path)",
                      "kernel_ms": kernel_ms, "kernel_ms_min": float(np.min(per_ms))},
         "cpu_baseline": {"value": cpu_rate, "unit": "windows/s", "cores": os.cpu_count(), "kind": "oracle",
                          "sample": cpu_desc},
