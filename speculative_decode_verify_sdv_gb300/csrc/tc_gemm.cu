@@ -84,9 +84,10 @@ __host__ __device__ inline TcPlan tc_plan(int qb, int S, int kc, int depth) {
   p.sc_off = p.ring_off + depth * p.code_stage;
   p.red_off = p.sc_off + depth * p.sc_stage;           // epilogue: [4 warps][S][33] floats
   p.bar_off = rup(p.red_off + 4 * S * 33 * 4, 16);
-  p.best_off = p.bar_off + (2 * depth + 2 * kABufs + 4) * 8;
+  // ring full/empty, A buffers afull/afree, tiles tfull/tfree, row slices xready
+  p.best_off = p.bar_off + (2 * depth + 2 * kABufs + 4 + p.kpad / 256) * 8;
   p.misc_off = p.best_off + 4 * 32 * 8;
-  p.total = p.misc_off + 32 * 4 + 16;
+  p.total = p.misc_off + 16 + 32 * 4 + 32 * 4;  // flags, argmax [32], drafts [32]
   return p;
 }
 
@@ -128,8 +129,8 @@ __global__ void __launch_bounds__(TcRoles::kThreads, 1)
     k_len = min(p.k_chunk, p.K - k_begin);
   }
   const int n_one = hit_tiles ? n_hit * p.rows_per_expert : p.N;  // rows of one matrix
-  const int t_one = (n_one + kTileRows - 1) / kTileRows;          // tiles of one matrix
   const int ldx = p.ldx > 0 ? p.ldx : p.K;
+  const int t_one = (n_one + kTileRows - 1) / kTileRows;          // tiles of one matrix
   const int ldy = p.ldy > 0 ? p.ldy : p.N;
   // tile t -> (matrix, tile within the matrix, first weight row)
   auto tile_split = [&](int t, int& mat, int& lt) {
@@ -181,12 +182,14 @@ __global__ void __launch_bounds__(TcRoles::kThreads, 1)
   const uint32_t bar_afree = bar_afull + 8 * kABufs;  // [A buffer]
   const uint32_t bar_tfull = bar_afree + 8 * kABufs;  // [tile buf]
   const uint32_t bar_tfree = bar_tfull + 2 * 8;  // [tile buf]
+  const uint32_t bar_xready = bar_tfree + 2 * 8;  // [row slice]: staged (epilogue warps)
   float* const best_v = reinterpret_cast<float*>(sb + pl.best_off);
   int* const best_i = reinterpret_cast<int*>(sb + pl.best_off + 4 * 32 * 4);
   uint32_t* const s_tmem = reinterpret_cast<uint32_t*>(sb + pl.misc_off);
   volatile int* const s_dead = reinterpret_cast<volatile int*>(sb + pl.misc_off + 4);
   int* const s_flag = reinterpret_cast<int*>(sb + pl.misc_off + 8);
   int* const s_am = reinterpret_cast<int*>(sb + pl.misc_off + 16);
+  int* const s_drafts = reinterpret_cast<int*>(sb + pl.misc_off + 16 + 32 * 4);
 
   // the stage sequence
   const int kst = (k_len + 255) / 256;
@@ -210,21 +213,32 @@ __global__ void __launch_bounds__(TcRoles::kThreads, 1)
   };
   // Stage cursor: position i in the stage sequence and its derived indices,
   // advanced incrementally (no per-stage integer division).
+  // ks is the stage's position within its tile, kx the 256-column slice of the
+  // reduction it covers: each CTA walks a tile's slices starting at its own
+  // rotation, so the CTAs do not all fetch the same window-row slice at once.
   struct Cursor {
-    int i, slot, phase, ks, t, ab, abphase;
+    int i, slot, phase, ks, kx, t, ab, abphase;
   };
+  const int rot = (kst > 0) ? (int)(blockIdx.x % (unsigned)kst) : 0;
   auto cursor_at = [&](int i) -> Cursor {
-    return Cursor{i, i % depth, (i / depth) & 1, i % kst, i / kst, i % kABufs, (i / kABufs) & 1};
+    const int ks = i % kst;
+    return Cursor{i, i % depth, (i / depth) & 1, ks, (ks + rot) % kst, i / kst, i % kABufs, (i / kABufs) & 1};
   };
   auto advance = [&](Cursor& c) {
     ++c.i;
     if (++c.slot == depth) { c.slot = 0; c.phase ^= 1; }
-    if (++c.ks == kst) { c.ks = 0; ++c.t; }
+    if (++c.ks == kst) {
+      c.ks = 0;
+      c.kx = rot;
+      ++c.t;
+    } else if (++c.kx == kst) {
+      c.kx = 0;
+    }
     if (++c.ab == kABufs) { c.ab = 0; c.abphase ^= 1; }
   };
   uint64_t policy = 0;
   auto issue = [&](const Cursor& c) {  // TMA of stage c.i into ring slot c.slot
-    const int slot = c.slot, ks = c.ks;
+    const int slot = c.slot, ks = c.kx;
     int mat, lt;
     int row0 = tile_map(tile_lo + c.t, mat, lt);
     const int boxes = (QB == 8) ? 2 : 1;
@@ -267,9 +281,34 @@ __global__ void __launch_bounds__(TcRoles::kThreads, 1)
       mbar_init(bar_tfull + 8 * b, 1);
       mbar_init(bar_tfree + 8 * b, 4);
     }
+    for (int j = 0; j < pl.kpad / 256; ++j) mbar_init(bar_xready + 8 * j, 4 * 32);
     *s_dead = 0;
     fence_barrier_init();
-    // start streaming weights before the window rows are staged
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_addr(s_tmem), kTmemCols);
+    tmem_relinquish();
+  }
+  if (threadIdx.x < 4 * 32) {
+    best_v[threadIdx.x] = -FLT_MAX;
+    best_i[threadIdx.x] = INT_MAX;
+  }
+  // the drafts, for the accept at the end (whichever CTA runs it)
+  if (MODE == kModeHead && warp == 2 && lane < p.n_valid) s_drafts[lane] = p.drafts[lane];
+
+  tc_fence_before();
+  __syncthreads();  // barriers initialised, tensor memory allocated
+  tc_fence_after();
+  // An allocation of all 512 columns always starts at lane 0, column 0.  Every
+  // tensor-memory address below is built on that constant, so the MMA operands
+  // are warp-uniform expressions of the loop counters (a base loaded from shared
+  // memory is not provably uniform and each MMA would pay to make it so).
+  constexpr uint32_t tmem = 0u;
+  if (threadIdx.x == 0 && *s_tmem != tmem) atomicOr(p.status, kDevErrTmemBase);
+
+  // ---- start the weight stream (the TMA unit carries only weights: each TMA
+  // issue costs ~0.15 us at start-up) ----
+  if (threadIdx.x == 0) {
     policy = l2_policy_evict_first();
     tma_prefetch_desc(&tm_codes);
     if (p.scales_tma) tma_prefetch_desc(&tm_scales);
@@ -280,51 +319,54 @@ __global__ void __launch_bounds__(TcRoles::kThreads, 1)
     Cursor c = cursor_at(0);
     for (; c.i < depth && c.i < nstages; advance(c)) issue(c);
   }
-  if (warp == 1) {
-    tmem_alloc(smem_addr(s_tmem), kTmemCols);
-    tmem_relinquish();
-  }
-  if (threadIdx.x < 4 * 32) {
-    best_v[threadIdx.x] = -FLT_MAX;
-    best_i[threadIdx.x] = INT_MAX;
-  }
-
-  // ---- stage the window rows: K-major core matrices (8 rows x 8 elements) -------
-  {
-    const int g8n = kst * 32;         // 8-element groups along K, padded to whole stages
-    const int g8v = k_len / 8;        // groups holding window data
+  // ---- window rows, slice by slice in this CTA's rotated order: the epilogue
+  // warps (idle until the first tile) load each 16-byte chunk, permute it like
+  // the converted codes and store it as K-major core matrices (zeros past S and
+  // past the reduction length); the MMA warp waits for the slice it multiplies ----
+  if (warp >= 2 && warp < R::kConv0) {
+    const int st = threadIdx.x - 64;
+    constexpr int kStagers = 4 * 32;
+    constexpr int kBatch = 4;
     const int sbo = pl.kpad * 16;     // bytes between 8-row groups
-    const int total = pl.xrows * g8n;
-#pragma unroll 4
-    for (int v = threadIdx.x; v < total; v += blockDim.x) {
-      const int n = v / g8n, g8 = v - n * g8n;
-      uint4 in = make_uint4(0u, 0u, 0u, 0u);
-      if (n < p.S && g8 < g8v) in = *reinterpret_cast<const uint4*>(p.x + (size_t)n * ldx + k_begin + 8 * g8);
-      uint4 o;
-      if (QB == 8) {  // per 4 elements: (k0, k2, k1, k3)
-        o.x = __byte_perm(in.x, in.y, 0x5410);
-        o.y = __byte_perm(in.x, in.y, 0x7632);
-        o.z = __byte_perm(in.z, in.w, 0x5410);
-        o.w = __byte_perm(in.z, in.w, 0x7632);
-      } else {  // per 8 elements: (k0, k4, k1, k5, k2, k6, k3, k7)
-        o.x = __byte_perm(in.x, in.z, 0x5410);
-        o.y = __byte_perm(in.x, in.z, 0x7632);
-        o.z = __byte_perm(in.y, in.w, 0x5410);
-        o.w = __byte_perm(in.y, in.w, 0x7632);
+    const int chunks = pl.xrows * 32;  // 16-byte chunks of one slice
+    for (int j = 0; j < kst; ++j) {
+      const int ks = (rot + j) % kst;
+      const int gv = min(32, max(0, k_len / 8 - 32 * ks));  // groups holding window data
+      for (int base = st; base < chunks; base += kBatch * kStagers) {
+        uint4 in[kBatch];
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+          const int v = base + u * kStagers;
+          const int n = v >> 5, g = v & 31;
+          in[u] = make_uint4(0u, 0u, 0u, 0u);
+          if (v < chunks && n < p.S && g < gv)
+            in[u] = *reinterpret_cast<const uint4*>(p.x + (size_t)n * ldx + k_begin + 8 * (32 * ks + g));
+        }
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+          const int v = base + u * kStagers;
+          if (v >= chunks) break;
+          const int n = v >> 5, g8 = 32 * ks + (v & 31);
+          const uint4 x4 = in[u];
+          uint4 o;
+          if (QB == 8) {  // per 4 elements: (k0, k2, k1, k3)
+            o.x = __byte_perm(x4.x, x4.y, 0x5410);
+            o.y = __byte_perm(x4.x, x4.y, 0x7632);
+            o.z = __byte_perm(x4.z, x4.w, 0x5410);
+            o.w = __byte_perm(x4.z, x4.w, 0x7632);
+          } else {  // per 8 elements: (k0, k4, k1, k5, k2, k6, k3, k7)
+            o.x = __byte_perm(x4.x, x4.z, 0x5410);
+            o.y = __byte_perm(x4.x, x4.z, 0x7632);
+            o.z = __byte_perm(x4.y, x4.w, 0x5410);
+            o.w = __byte_perm(x4.y, x4.w, 0x7632);
+          }
+          *reinterpret_cast<uint4*>(sb + pl.x_off + (n >> 3) * sbo + g8 * 128 + (n & 7) * 16) = o;
+        }
       }
-      *reinterpret_cast<uint4*>(sb + pl.x_off + (n >> 3) * sbo + g8 * 128 + (n & 7) * 16) = o;
+      fence_proxy_async_smem();  // generic-proxy writes, read by the tensor cores
+      mbar_arrive(bar_xready + 8 * ks);
     }
   }
-  fence_proxy_async_smem();
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  // An allocation of all 512 columns always starts at lane 0, column 0.  Every
-  // tensor-memory address below is built on that constant, so the MMA operands
-  // are warp-uniform expressions of the loop counters (a base loaded from shared
-  // memory is not provably uniform and each MMA would pay to make it so).
-  constexpr uint32_t tmem = 0u;
-  if (threadIdx.x == 0 && *s_tmem != tmem) atomicOr(p.status, kDevErrTmemBase);
 
   if (warp == 0) {
     // ---------------- TMA producer -------------------------------------------------
@@ -343,10 +385,12 @@ __global__ void __launch_bounds__(TcRoles::kThreads, 1)
       const int t = c.t, ks = c.ks, tb = t & 1;
       const int ab = c.ab;
       if (ks == 0 && t >= 2 && !wait_warp(bar_tfree + 8 * tb, ((t >> 1) - 1) & 1)) break;
+      // first tile: the slice of window rows this stage multiplies must be in place
+      if (t == 0 && !wait_warp(bar_xready + 8 * c.kx, 0)) break;
       const uint32_t a_stage = tmem + (uint32_t)(ab * 128);
       const uint32_t d_tile = tmem + (uint32_t)(kACols + tb * kAcc * NM);
       // descriptor start address advances by k (16-byte units) per reduction element k
-      const uint64_t b_stage = bdesc0 + (uint64_t)(ks * 256);
+      const uint64_t b_stage = bdesc0 + (uint64_t)(c.kx * 256);
       const bool later = ks > 0;
       if (!wait_warp(bar_afull + 8 * ab, c.abphase)) break;
       tc_fence_after();
@@ -468,7 +512,7 @@ __global__ void __launch_bounds__(TcRoles::kThreads, 1)
     for (; c.i < nstages; advance(c), advance(c)) {
       const int slot = c.slot;
       const int ab = c.ab;
-      const int nb = max(0, min(8, nblk_total - c.ks * 8));  // blocks within the reduction length
+      const int nb = max(0, min(8, nblk_total - c.kx * 8));  // blocks within the reduction length
       bool ok = wait_warp(bar_full + 8 * slot, c.phase);
       const uint8_t* const cb = sb + pl.ring_off + slot * pl.code_stage;
       // the 8 block scales of row r; blocks past the reduction length get zero, so
@@ -487,7 +531,7 @@ __global__ void __launch_bounds__(TcRoles::kThreads, 1)
           }
         } else {
           const int row = (tile_lo + c.t) * kTileRows + r;
-          const int ks = c.ks;
+          const int ks = c.kx;
 #pragma unroll
           for (int blk = 0; blk < 8; ++blk)
             sc_h[blk] = (blk < nb && row < p.N)
@@ -575,7 +619,23 @@ __global__ void __launch_bounds__(TcRoles::kThreads, 1)
   for (int col = warp; col < p.S; col += R::kWarps) {
     float bv = -FLT_MAX;
     int bi = INT_MAX;
-    for (int j = lane; j < (int)gridDim.x; j += 32)
+    // all of a lane's partials are loaded before they are merged (one round of latency)
+    constexpr int kPf = 8;
+    float pv[kPf];
+    int pi[kPf];
+#pragma unroll
+    for (int u = 0; u < kPf; ++u) {
+      const int j = lane + 32 * u;
+      pv[u] = -FLT_MAX;
+      pi[u] = INT_MAX;
+      if (j < (int)gridDim.x) {
+        pv[u] = __ldcg(p.part_v + (size_t)j * p.S + col);
+        pi[u] = __ldcg(p.part_i + (size_t)j * p.S + col);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kPf; ++u) argmax_merge(bv, bi, pv[u], pi[u]);
+    for (int j = lane + 32 * kPf; j < (int)gridDim.x; j += 32)
       argmax_merge(bv, bi, __ldcg(p.part_v + (size_t)j * p.S + col), __ldcg(p.part_i + (size_t)j * p.S + col));
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) {
@@ -589,12 +649,15 @@ __global__ void __launch_bounds__(TcRoles::kThreads, 1)
     }
   }
   __syncthreads();
-  if (threadIdx.x == 0) {
-    int j = 0;
-    while (j < p.n_valid && p.drafts[j] == s_am[j]) ++j;
-    *p.accepted = j;
-    *p.next_a0 = s_am[j];
-    *p.ticket = 0u;
+  if (warp == 0) {  // accepted = the first window position whose draft misses (n_valid <= 31)
+    const bool hit = lane < p.n_valid && s_drafts[lane] == s_am[lane];
+    const unsigned miss = ~__ballot_sync(0xffffffffu, hit);
+    const int j = __ffs(miss) - 1;
+    if (lane == 0) {
+      *p.accepted = j;
+      *p.next_a0 = s_am[j];
+      *p.ticket = 0u;
+    }
   }
 }
 
