@@ -272,6 +272,14 @@ __host__ __device__ constexpr uint32_t idesc_f16_f32(int m, int n) {
   return (1u << 4) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
 }
 
+// Programmatic dependent launch: wait until the previous grid in the stream has
+// completed and its memory is visible (a no-op without the launch attribute), and
+// let the next grid's CTAs be scheduled as this grid's CTAs finish.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }

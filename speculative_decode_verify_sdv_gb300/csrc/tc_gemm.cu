@@ -108,6 +108,9 @@ __global__ void __launch_bounds__(TcRoles::kThreads, 1)
   uint8_t* const sb = smem_raw + (base - raw_addr);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // launched as a programmatic dependent of the previous kernel in the stream:
+  // nothing in global memory is touched before that grid has completed
+  griddep_wait();
   // Row and reduction mappings (all uniform over the CTA):
   //  * plain: tile t covers weight rows 128t.., the reduction [k_begin, k_begin + k_len);
   //  * dual: tiles [0, T) read the first matrix, [T, 2T) the second (T tiles each);
@@ -593,6 +596,7 @@ __global__ void __launch_bounds__(TcRoles::kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  griddep_launch_dependents();  // the next grid may take this SM once the CTA exits
   if (warp == 1) {
     __syncwarp();
     tmem_dealloc(tmem, kTmemCols);
@@ -609,13 +613,15 @@ __global__ void __launch_bounds__(TcRoles::kThreads, 1)
   }
   __syncthreads();
   if (threadIdx.x == 0) {
-    __threadfence();
-    const unsigned tk = atomicAdd(p.ticket, 1u);
+    // one acquire-release ticket: publishes this CTA's partials (the release is
+    // cumulative over the block's stores before the barrier) and, for the last
+    // CTA, acquires every other CTA's; the barrier below passes that on
+    unsigned tk;
+    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(tk) : "l"(p.ticket) : "memory");
     *s_flag = (tk == gridDim.x - 1) ? 1 : 0;
   }
   __syncthreads();
   if (*s_flag == 0) return;
-  __threadfence();
   for (int col = warp; col < p.S; col += R::kWarps) {
     float bv = -FLT_MAX;
     int bi = INT_MAX;
@@ -670,8 +676,19 @@ cudaError_t tc_launch_t(const TcMaps& m, const GemmArgs& a, int grid, int smem, 
   auto k = tc_gemm_kernel<QB, MODE, NM>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  k<<<dim3(grid, a.splits), TcRoles::kThreads, smem, st>>>(m.c, m.s, m.c2, m.s2, a);
-  return cudaGetLastError();
+  // programmatic stream serialisation: the kernel's CTAs may be scheduled while
+  // the previous kernel drains; they wait for it in griddep_wait()
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid, a.splits);
+  cfg.blockDim = dim3(TcRoles::kThreads);
+  cfg.dynamicSmemBytes = (size_t)smem;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, k, m.c, m.s, m.c2, m.s2, a);
 }
 
 template <int QB, int MODE>
