@@ -452,6 +452,8 @@ cudaError_t launch_nt(int nt, const CUtensorMap& tc, const CUtensorMap& tsc, con
 // y[s][n] = sum over splits of part[split][s][n], in split order (deterministic).
 __global__ void splitk_reduce_kernel(const float* __restrict__ part, int splits, long count,
                                      float* __restrict__ y) {
+  griddep_wait();
+  griddep_launch_dependents();
   for (long i = (long)blockIdx.x * blockDim.x + threadIdx.x; i < count; i += (long)gridDim.x * blockDim.x) {
     // loads in batches of 8 (independent), sums in split order
     float v = part[i];
@@ -473,8 +475,7 @@ __global__ void splitk_reduce_kernel(const float* __restrict__ part, int splits,
 cudaError_t launch_splitk_reduce(const float* part, int splits, long count, float* y, cudaStream_t st) {
   long grid = (count + 255) / 256;
   if (grid > 4096) grid = 4096;
-  splitk_reduce_kernel<<<(unsigned)grid, 256, 0, st>>>(part, splits, count, y);
-  return cudaGetLastError();
+  return launch_pdl(splitk_reduce_kernel, dim3((unsigned)grid), dim3(256), 0, st, part, splits, count, y);
 }
 
 int gemm_tile_mt(int qbits) { return qbits == 8 ? 2 : 4; }

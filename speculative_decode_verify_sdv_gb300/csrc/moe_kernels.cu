@@ -10,6 +10,7 @@
 
 #include <cstdint>
 
+#include "sdv_device.cuh"
 #include "sdv_kernels.h"
 
 namespace sdv {
@@ -22,6 +23,8 @@ __global__ void swiglu_reduce_kernel(const float* __restrict__ part, int splits,
                                      int S, int n, __half* __restrict__ h, int ldh,
                                      const float* __restrict__ row_w, int ldw, int seg,
                                      const int* __restrict__ n_dev) {
+  griddep_wait();
+  griddep_launch_dependents();
   const int ncols = (n_dev != nullptr) ? min(n, *n_dev * seg) : n;
   const long count = (long)S * ncols;
   for (long i = (long)blockIdx.x * blockDim.x + threadIdx.x; i < count; i += (long)gridDim.x * blockDim.x) {
@@ -77,15 +80,20 @@ constexpr int kMaxRows = 32;
 constexpr int kMaxTopK = 32;
 
 // One block: warp s routes row s; then the block groups the selections.
+// SLOTS = logits per lane (E <= 32 * SLOTS), kept in registers.
+template <int SLOTS>
 __global__ void __launch_bounds__(kRouteThreads) moe_route_kernel(
     const float* __restrict__ logits, int S, int E, int top_k, int32_t* __restrict__ ids,
     float* __restrict__ w, int32_t* __restrict__ offsets, int32_t* __restrict__ pair_rows,
     int32_t* __restrict__ n_hit, int32_t* __restrict__ hit, float* __restrict__ row_w, int n_cap) {
   __shared__ int s_ids[kMaxRows][kMaxTopK];
+  __shared__ float s_val[kMaxRows][kMaxTopK];
   __shared__ int cnt[kMaxExperts];
   __shared__ int slot[kMaxExperts];
   __shared__ int wsum[32];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  griddep_wait();
+  griddep_launch_dependents();  // the GEMM that follows may take the other SMs now
   for (int e = tid; e < kMaxExperts; e += blockDim.x) cnt[e] = 0;
   __syncthreads();
 
@@ -93,7 +101,7 @@ __global__ void __launch_bounds__(kRouteThreads) moe_route_kernel(
   // lane holds experts lane + 32 m in registers; bit m of `taken` marks a selection
   if (warp < S) {
     const float* const row = logits + (long)warp * E;
-    constexpr int kSlots = kMaxExperts / 32;
+    constexpr int kSlots = SLOTS;
     float lv[kSlots];
 #pragma unroll
     for (int m = 0; m < kSlots; ++m) {
@@ -102,7 +110,6 @@ __global__ void __launch_bounds__(kRouteThreads) moe_route_kernel(
     }
     uint32_t taken = 0u;
     float first = 0.f, sum = 0.f;
-    float chosen_l[kMaxTopK];
     for (int i = 0; i < top_k; ++i) {
       float bv = -__int_as_float(0x7f800000);  // -inf
       int be = INT32_MAX;
@@ -124,19 +131,18 @@ __global__ void __launch_bounds__(kRouteThreads) moe_route_kernel(
         }
       }
       if ((be & 31) == lane) taken |= 1u << (be >> 5);
-      if (lane == 0) s_ids[warp][i] = be;
+      if (lane == 0) {
+        s_ids[warp][i] = be;
+        s_val[warp][i] = bv;
+      }
       if (i == 0) first = bv;
-      chosen_l[i] = bv;
     }
+    __syncwarp();  // lane 0's writes, visible to the whole warp
     // softmax over the selection (the first selected logit is the largest)
-    for (int i = 0; i < top_k; ++i) sum += expf(chosen_l[i] - first);
-    __syncwarp();  // lane 0's s_ids writes, visible to the lanes below
+    for (int i = 0; i < top_k; ++i) sum += expf(s_val[warp][i] - first);
     if (lane < top_k) {
-      float li = 0.f;
-      for (int i = 0; i < top_k; ++i)
-        if (i == lane) li = chosen_l[i];
       ids[warp * top_k + lane] = s_ids[warp][lane];
-      w[warp * top_k + lane] = expf(li - first) / sum;
+      w[warp * top_k + lane] = expf(s_val[warp][lane] - first) / sum;
     }
   }
   __syncthreads();
@@ -183,9 +189,8 @@ cudaError_t launch_swiglu_reduce(const float* part, int splits, long pstride, in
   long grid = ((long)S * n + 255) / 256;
   if (grid > 4096) grid = 4096;
   if (grid < 1) grid = 1;
-  swiglu_reduce_kernel<<<(unsigned)grid, 256, 0, st>>>(part, splits, pstride, ldp, u_off, S, n, h, ldh, row_w, ldw,
-                                                       seg > 0 ? seg : 1, n_dev);
-  return cudaGetLastError();
+  return launch_pdl(swiglu_reduce_kernel, dim3((unsigned)grid), dim3(256), 0, st, part, splits, pstride, ldp, u_off,
+                    S, n, h, ldh, row_w, ldw, seg > 0 ? seg : 1, n_dev);
 }
 
 cudaError_t launch_moe_route(const float* logits, int S, int E, int top_k, int32_t* ids, float* w,
@@ -193,9 +198,11 @@ cudaError_t launch_moe_route(const float* logits, int S, int E, int top_k, int32
                              int n_cap, cudaStream_t st) {
   if (S < 1 || S > kMaxRows || E < 1 || E > kMaxExperts || top_k < 1 || top_k > kMaxTopK || top_k > E)
     return cudaErrorInvalidValue;
-  moe_route_kernel<<<1, kRouteThreads, 0, st>>>(logits, S, E, top_k, ids, w, offsets, pair_rows, n_hit, hit,
-                                                row_w, n_cap);
-  return cudaGetLastError();
+  if (E <= 256)
+    return launch_pdl(moe_route_kernel<8>, dim3(1), dim3(kRouteThreads), 0, st, logits, S, E, top_k, ids, w,
+                      offsets, pair_rows, n_hit, hit, row_w, n_cap);
+  return launch_pdl(moe_route_kernel<kMaxExperts / 32>, dim3(1), dim3(kRouteThreads), 0, st, logits, S, E, top_k,
+                    ids, w, offsets, pair_rows, n_hit, hit, row_w, n_cap);
 }
 
 }  // namespace sdv

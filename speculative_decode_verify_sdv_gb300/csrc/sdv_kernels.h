@@ -8,6 +8,25 @@
 
 namespace sdv {
 
+// Launch with programmatic stream serialisation: the kernel may be scheduled
+// while the previous kernel in the stream drains, and must call
+// griddepcontrol.wait before reading anything that kernel wrote.
+template <typename... Params, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(Params...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                       Args&&... args) {
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
+}
+
 // Device status word bits (first word of every workspace).
 constexpr int kDevErrTimeout = 1;
 constexpr int kDevErrTmemBase = 2;  // tensor-memory allocation not at column 0

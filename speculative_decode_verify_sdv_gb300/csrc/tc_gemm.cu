@@ -676,19 +676,9 @@ cudaError_t tc_launch_t(const TcMaps& m, const GemmArgs& a, int grid, int smem, 
   auto k = tc_gemm_kernel<QB, MODE, NM>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  // programmatic stream serialisation: the kernel's CTAs may be scheduled while
-  // the previous kernel drains; they wait for it in griddep_wait()
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(grid, a.splits);
-  cfg.blockDim = dim3(TcRoles::kThreads);
-  cfg.dynamicSmemBytes = (size_t)smem;
-  cfg.stream = st;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, k, m.c, m.s, m.c2, m.s2, a);
+  // the CTAs may be scheduled while the previous kernel drains; they wait for it
+  // in griddep_wait()
+  return launch_pdl(k, dim3(grid, a.splits), dim3(TcRoles::kThreads), (size_t)smem, st, m.c, m.s, m.c2, m.s2, a);
 }
 
 template <int QB, int MODE>
