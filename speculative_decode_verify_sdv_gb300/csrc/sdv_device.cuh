@@ -185,30 +185,45 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
-// D[tmem] (+)= A[tmem] * B[smem desc], kind::f16, issued by one thread.
-__device__ __forceinline__ void tc_mma_f16_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
-                                              uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
+// The 16 MMAs of one 256-column stage under a single elect.sync (one lane
+// issues, the warp stays converged): MMA m multiplies A columns a + 8m by the
+// B descriptor b + 16m (16-byte units) into accumulator m % NACC at d + N (m % NACC);
+// the first NACC MMAs overwrite their accumulator unless `accumulate`.
+#define SDV_MMA1(D, P) "@e tcgen05.mma.cta_group::1.kind::f16 [" D "], [ta], tb, %3, " P ";\n\t" \
+                        "add.u32 ta, ta, 8;\n\tadd.u64 tb, tb, 16;\n\t"
+template <int NACC>
+__device__ __forceinline__ void tc_mma_stage16(uint32_t d, uint32_t a, uint64_t b, uint32_t idesc, uint32_t n,
+                                               uint32_t accumulate) {
+  static_assert(NACC == 2 || NACC == 4, "accumulators per tile");
+  if (NACC == 2) {
+    asm volatile(
+        "{\n\t.reg .pred e, p, t;\n\t.reg .b32 ta, d0, d1;\n\t.reg .b64 tb;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\tsetp.eq.b32 t, 0, 0;\n\t"
+        "mov.b32 ta, %1;\n\tmov.b64 tb, %2;\n\tmov.b32 d0, %0;\n\tadd.u32 d1, %0, %5;\n\t"
+        SDV_MMA1("d0", "p") SDV_MMA1("d1", "p")
+        SDV_MMA1("d0", "t") SDV_MMA1("d1", "t") SDV_MMA1("d0", "t") SDV_MMA1("d1", "t")
+        SDV_MMA1("d0", "t") SDV_MMA1("d1", "t") SDV_MMA1("d0", "t") SDV_MMA1("d1", "t")
+        SDV_MMA1("d0", "t") SDV_MMA1("d1", "t") SDV_MMA1("d0", "t") SDV_MMA1("d1", "t")
+        SDV_MMA1("d0", "t") SDV_MMA1("d1", "t")
+        "}" ::"r"(d), "r"(a), "l"(b), "r"(idesc), "r"(accumulate), "r"(n)
+        : "memory");
+  } else {
+    asm volatile(
+        "{\n\t.reg .pred e, p, t;\n\t.reg .b32 ta, d0, d1, d2, d3;\n\t.reg .b64 tb;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\tsetp.eq.b32 t, 0, 0;\n\t"
+        "mov.b32 ta, %1;\n\tmov.b64 tb, %2;\n\tmov.b32 d0, %0;\n\tadd.u32 d1, %0, %5;\n\t"
+        "add.u32 d2, d1, %5;\n\tadd.u32 d3, d2, %5;\n\t"
+        SDV_MMA1("d0", "p") SDV_MMA1("d1", "p") SDV_MMA1("d2", "p") SDV_MMA1("d3", "p")
+        SDV_MMA1("d0", "t") SDV_MMA1("d1", "t") SDV_MMA1("d2", "t") SDV_MMA1("d3", "t")
+        SDV_MMA1("d0", "t") SDV_MMA1("d1", "t") SDV_MMA1("d2", "t") SDV_MMA1("d3", "t")
+        SDV_MMA1("d0", "t") SDV_MMA1("d1", "t") SDV_MMA1("d2", "t") SDV_MMA1("d3", "t")
+        "}" ::"r"(d), "r"(a), "l"(b), "r"(idesc), "r"(accumulate), "r"(n)
+        : "memory");
+  }
 }
-
-// Same MMA issued from a warp-uniform loop: every lane executes the call with
-// identical operands and one elected lane issues the instruction (keeps the
-// operands in the warp-uniform datapath, so back-to-back MMAs issue cheaply).
-__device__ __forceinline__ void tc_mma_f16_ta_elect(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
-                                                    uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p, e;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "elect.sync _|e, 0xffffffff;\n\t"
-      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
+#undef SDV_MMA1
 
 // tcgen05.commit from a warp-uniform context (one elected lane).
 __device__ __forceinline__ void tc_commit_elect(uint32_t bar) {

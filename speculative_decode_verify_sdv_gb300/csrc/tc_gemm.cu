@@ -397,12 +397,10 @@ __global__ void __launch_bounds__(TcRoles::kThreads, 1)
       const bool later = ks > 0;
       if (!wait_warp(bar_afull + 8 * ab, c.abphase)) break;
       tc_fence_after();
-      // straight-line issue: a branch around an elected MMA costs a warp
-      // reconvergence per instruction
-#pragma unroll
-      for (int m = 0; m < 16; ++m)  // MMA m: k = 16m .. 16m+15 of the stage
-        tc_mma_f16_ta_elect(d_tile + (uint32_t)((m & (kAcc - 1)) * NM), a_stage + (uint32_t)(m * 8),
-                            b_stage + (uint64_t)(m * 16), idesc, (later || m >= kAcc) ? 1u : 0u);
+      // the stage's 16 MMAs (k = 16m .. 16m+15) in one straight-line block under a
+      // single elect: a branch or a fresh elect per MMA costs issue slots that
+      // the converters on this scheduler need
+      tc_mma_stage16<kAcc>(d_tile, a_stage, b_stage, idesc, (uint32_t)NM, later ? 1u : 0u);
       tc_commit_elect(bar_afree + 8 * ab);
       if (ks == kst - 1) tc_commit_elect(bar_tfull + 8 * tb);
     }
