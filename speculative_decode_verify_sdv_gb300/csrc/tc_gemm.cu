@@ -108,9 +108,12 @@ __global__ void __launch_bounds__(TcRoles::kThreads, 1)
   uint8_t* const sb = smem_raw + (base - raw_addr);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // launched as a programmatic dependent of the previous kernel in the stream:
-  // nothing in global memory is touched before that grid has completed
-  griddep_wait();
+  // Launched as a programmatic dependent of the previous kernel in the stream:
+  // nothing in global memory is read or written before that grid has completed.
+  // Only the MoE mappings need global data (the hit count) up front; other
+  // launches set up barriers and tensor memory first, overlapping its tail.
+  const bool dep_early = (p.n_hit != nullptr);
+  if (dep_early) griddep_wait();
   // Row and reduction mappings (all uniform over the CTA):
   //  * plain: tile t covers weight rows 128t.., the reduction [k_begin, k_begin + k_len);
   //  * dual: tiles [0, T) read the first matrix, [T, 2T) the second (T tiles each);
@@ -296,6 +299,7 @@ __global__ void __launch_bounds__(TcRoles::kThreads, 1)
     best_v[threadIdx.x] = -FLT_MAX;
     best_i[threadIdx.x] = INT_MAX;
   }
+  if (!dep_early) griddep_wait();
   // the drafts, for the accept at the end (whichever CTA runs it)
   if (MODE == kModeHead && warp == 2 && lane < p.n_valid) s_drafts[lane] = p.drafts[lane];
 
