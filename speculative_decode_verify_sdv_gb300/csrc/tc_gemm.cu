@@ -52,8 +52,11 @@ constexpr int kABufs = 3;        // A operand stage buffers in tensor memory
 constexpr int kMinDepth = 4;     // ring stages (see tc_plan_valid)
 constexpr int kACols = kABufs * 128;
 
+// Converter groups: group g takes the stages i with i % G == g.  An int4 stage
+// carries twice the weights per byte of an int8 stage, so it gets a third group.
+template <int QB>
 struct TcRoles {
-  static constexpr int G = 2;                // converter groups: group g takes the stages i with i % 2 == g
+  static constexpr int G = (QB == 4) ? 3 : 2;
   static constexpr int kConvWarps = 4 * G;   // one warp per tensor-memory lane quarter per group
   static constexpr int kConv0 = 6;           // first converter warp (0 TMA, 1 MMA, 2-5 epilogue)
   static constexpr int kWarps = kConv0 + kConvWarps;
@@ -92,12 +95,12 @@ __host__ __device__ inline TcPlan tc_plan(int qb, int S, int kc, int depth) {
 }
 
 template <int QB, int MODE, int NM>
-__global__ void __launch_bounds__(TcRoles::kThreads, 1)
+__global__ void __launch_bounds__(TcRoles<QB>::kThreads, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_codes,
                    const __grid_constant__ CUtensorMap tm_scales,
                    const __grid_constant__ CUtensorMap tm_codes2,
                    const __grid_constant__ CUtensorMap tm_scales2, const GemmArgs p) {
-  using R = TcRoles;
+  using R = TcRoles<QB>;
   // independent fp32 accumulators per tile (MMA m of a stage -> m % kAcc), two
   // tile buffers, in the tensor-memory columns behind the A buffers
   constexpr int kAcc = (512 - kACols) / (2 * NM);
@@ -500,8 +503,8 @@ __global__ void __launch_bounds__(TcRoles::kThreads, 1)
     }
   } else {
     // ---------------- converters ------------------------------------------------------
-    // Group g converts whole stages g, g+2, g+4, ...: while one group waits for
-    // its next stage the other converts, and each stage is one hand-off to the
+    // Group g converts whole stages g, g+G, g+2G, ...: while one group waits for
+    // its next stage the others convert, and each stage is one hand-off to the
     // MMA warp.
     const int cw = warp - R::kConv0;
     const int q = warp & 3;
@@ -513,12 +516,15 @@ __global__ void __launch_bounds__(TcRoles::kThreads, 1)
     constexpr int kHalfBlocks = 8 / kHalves;     // 32-blocks per load
     const int sw = r & 7;
     Cursor c = cursor_at(0);
-    if (g == 1) advance(c);
-    for (; c.i < nstages; advance(c), advance(c)) {
+    for (int j = 0; j < g; ++j) advance(c);
+    for (; c.i < nstages;) {
       const int slot = c.slot;
       const int ab = c.ab;
       const int nb = max(0, min(8, nblk_total - c.kx * 8));  // blocks within the reduction length
-      bool ok = wait_warp(bar_full + 8 * slot, c.phase);
+      // the A buffer first, then the ring slot (the order tc_plan_valid relies on)
+      bool ok = true;
+      if (c.i >= kABufs) ok = wait_warp(bar_afree + 8 * ab, c.abphase ^ 1);
+      if (ok) ok = wait_warp(bar_full + 8 * slot, c.phase);
       const uint8_t* const cb = sb + pl.ring_off + slot * pl.code_stage;
       // the 8 block scales of row r; blocks past the reduction length get zero, so
       // their A columns are zero (the padded window rows are zero too)
@@ -557,10 +563,7 @@ __global__ void __launch_bounds__(TcRoles::kThreads, 1)
           __syncwarp();
           if (lane == 0) mbar_arrive(bar_empty + 8 * slot);
         }
-        if (h == 0) {
-          if (ok && c.i >= kABufs) ok = wait_warp(bar_afree + 8 * ab, c.abphase ^ 1);
-          if (ok) tc_fence_after();
-        }
+        if (h == 0 && ok) tc_fence_after();
         if (ok) {
 #pragma unroll
           for (int blk = 0; blk < kHalfBlocks; ++blk) {
@@ -591,6 +594,7 @@ __global__ void __launch_bounds__(TcRoles::kThreads, 1)
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_afull + 8 * ab);
+      for (int j = 0; j < R::G; ++j) advance(c);
     }
   }
 
@@ -680,7 +684,8 @@ cudaError_t tc_launch_t(const TcMaps& m, const GemmArgs& a, int grid, int smem, 
   if (e != cudaSuccess) return e;
   // the CTAs may be scheduled while the previous kernel drains; they wait for it
   // in griddep_wait()
-  return launch_pdl(k, dim3(grid, a.splits), dim3(TcRoles::kThreads), (size_t)smem, st, m.c, m.s, m.c2, m.s2, a);
+  return launch_pdl(k, dim3(grid, a.splits), dim3(TcRoles<QB>::kThreads), (size_t)smem, st, m.c, m.s, m.c2, m.s2,
+                    a);
 }
 
 template <int QB, int MODE>
@@ -698,14 +703,13 @@ int tc_smem_bytes(int qbits, int S, int k_chunk, int depth) {
 // The aliased 8-row groups of N read up to one group stride past the staged
 // rows; the ring behind them must be at least that long.
 //
-// The ring needs at least kMinDepth stages.  Converter group g takes stages g,
-// g+2, ...; before it waits on slot (i % depth) for stage i, the slot's previous
-// phase (stage i - depth) must be complete, else the parity wait would match the
-// phase before that and return early.  With an even depth the previous user is
-// the same group (already past it); with an odd depth >= 5 the group's own
-// wait at stage i - 2 for the A-buffer release of stage i - 5 implies, by the
-// in-order MMAs, that stage i - depth was converted.  Depth 3 has no such
-// guarantee: the other group's stage i - 3 may not even have landed.
+// Before a converter group waits on slot (i % depth) for stage i, the slot's
+// previous phase (stage i - depth) must be complete, else the parity wait would
+// match the phase before that and return early.  The group first waits for the
+// release of its A buffer by the MMAs of stage i - kABufs; the MMAs run in stage
+// order, so every stage up to i - kABufs has been converted, hence has landed,
+// and any depth >= kABufs is safe.  The ring takes at least kMinDepth stages so
+// that the weight stream has some stages in flight.
 bool tc_plan_valid(int qbits, int S, int k_chunk, int depth) {
   if (depth < kMinDepth) return false;
   const TcPlan p = tc_plan(qbits, S, k_chunk, depth);

@@ -110,6 +110,37 @@ def test_ragged_shapes(sdv, path, bits, n, k):
         _window(sdv, head, codes, scales, _x(S, k, n + S), n + S, k)
 
 
+@pytest.mark.parametrize("S", [17, 25, 32])
+def test_int4_long_reduction_wide_windows(sdv, path, S):
+    """int4 at K = 2048 with window sizes whose staged rows fill most of the
+    tensor-core path's shared memory (S = 32: ring depth 4)."""
+    n, k = 3000, 2048
+    codes, scales, stored = _synthetic_head(n, k, 4, 7)
+    head = device_weight(stored, scales, 4, n, k)
+    _window(sdv, head, codes, scales, _x(S, k, 70 + S), 70 + S, k)
+
+
+@pytest.mark.parametrize("bits", [8, 4])
+def test_large_block_scales(sdv, path, bits):
+    """Some 32-blocks carry weights ~1e4 times larger (int4 block scales of about
+    50 to 160), scattered so that some warps hold none, some a few; rows without
+    them are checked against their own magnitude too."""
+    n, k, S = 1500, 512, 9
+    w = G.normal(G.stream_seed(902, n, k, bits), (n, k), 0.02)
+    rng = np.random.default_rng(5)
+    big = rng.random((n, k // 32)) < 0.02
+    big[:400] = False                      # the first 400 rows: no large block at all
+    w = w.reshape(n, k // 32, 32)
+    w[big] *= np.float32(1.5e4)
+    w = w.reshape(n, k)
+    codes, scales, stored = oracle_weight(w, bits)
+    head = device_weight(stored, scales, bits, n, k)
+    ref, _, _, _ = _window(sdv, head, codes, scales, _x(S, k, 3), 3, k)
+    logits, _, _, _ = run_head(head, _x(S, k, 3), np.zeros(S - 1, np.int32), 0)
+    plain = ~big.any(axis=1)
+    assert_gemm_close(logits[:, plain], ref["logits"][:, plain], k, "logits of rows without large blocks")
+
+
 def test_planted_ties_and_tail_maximum(sdv, path):
     # rows with identical codes and scales give identical logits: lowest index wins;
     # a dominant row in the last (ragged) tile must be found
