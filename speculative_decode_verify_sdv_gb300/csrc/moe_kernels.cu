@@ -41,11 +41,6 @@ __global__ void swiglu_reduce_kernel(const float* __restrict__ part, int splits,
   }
 }
 
-// (value, id) order of the routing: larger logit first, ties to the lower id.
-__device__ __forceinline__ bool route_better(float v, int e, float bv, int be) {
-  return v > bv || (v == bv && e < be);
-}
-
 // Exclusive prefix sum over the block (blockDim.x == 1024); returns the
 // exclusive sum of thread tid's value and writes the total to *total.
 __device__ int block_excl_scan(int v, int* wsum, int* total) {
@@ -70,8 +65,19 @@ __device__ int block_excl_scan(int v, int* wsum, int* total) {
   __syncthreads();
   const int excl = incl - v + (warp > 0 ? wsum[warp - 1] : 0);
   *total = wsum[31];
-  __syncthreads();
   return excl;
+}
+
+// Order-preserving 32-bit key of a routing logit: a larger logit has a larger
+// key, -0 and +0 share one key (they compare equal), and NaN sorts below -inf.
+__device__ __forceinline__ uint32_t route_key(float v) {
+  if (v != v) return 0u;
+  const uint32_t u = __float_as_uint(v + 0.f);  // -0 -> +0
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+__device__ __forceinline__ float route_key_value(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
 }
 
 constexpr int kRouteThreads = 1024;
@@ -79,105 +85,159 @@ constexpr int kMaxExperts = 1024;
 constexpr int kMaxRows = 32;
 constexpr int kMaxTopK = 32;
 
-// One block: warp s routes row s; then the block groups the selections.
-// SLOTS = logits per lane (E <= 32 * SLOTS), kept in registers.
+// One block.  Warp s routes row s: its lanes hold the experts lane + 32 m
+// (m < SLOTS, E <= 32 SLOTS) in registers, each lane keeps its best untaken
+// expert, and every selection round is one warp max over the keys plus one warp
+// min over the ids of the lanes holding that key (larger logit first, ties to
+// the lower id).  Each selection then counts its expert and marks its row in the
+// expert's row mask.  The block scans the packed (count, hit) pairs of all
+// experts at once; a selection's place among its expert's rows is the number of
+// lower rows in the mask.
 template <int SLOTS>
 __global__ void __launch_bounds__(kRouteThreads) moe_route_kernel(
     const float* __restrict__ logits, int S, int E, int top_k, int32_t* __restrict__ ids,
     float* __restrict__ w, int32_t* __restrict__ offsets, int32_t* __restrict__ pair_rows,
     int32_t* __restrict__ n_hit, int32_t* __restrict__ hit, float* __restrict__ row_w, int n_cap) {
   __shared__ int s_ids[kMaxRows][kMaxTopK];
-  __shared__ float s_val[kMaxRows][kMaxTopK];
+  __shared__ float s_w[kMaxRows][kMaxTopK];
   __shared__ int cnt[kMaxExperts];
-  __shared__ int slot[kMaxExperts];
+  __shared__ uint32_t rowmask[kMaxExperts];
+  __shared__ int s_off[kMaxExperts];
+  __shared__ int s_slot[kMaxExperts];
   __shared__ int wsum[32];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   griddep_wait();
   griddep_launch_dependents();  // the GEMM that follows may take the other SMs now
-  for (int e = tid; e < kMaxExperts; e += blockDim.x) cnt[e] = 0;
+  for (int e = tid; e < kMaxExperts; e += blockDim.x) {
+    cnt[e] = 0;
+    rowmask[e] = 0u;
+  }
   __syncthreads();
 
-  // ---- route: top_k by repeated warp argmax over the unselected experts ----
-  // lane holds experts lane + 32 m in registers; bit m of `taken` marks a selection
+  // ---- route ----
   if (warp < S) {
     const float* const row = logits + (long)warp * E;
-    constexpr int kSlots = SLOTS;
-    float lv[kSlots];
+    uint32_t key[SLOTS];
+    int idx[SLOTS];  // slot m of key[] holds expert lane + 32 idx[m]
 #pragma unroll
-    for (int m = 0; m < kSlots; ++m) {
+    for (int m = 0; m < SLOTS; ++m) {
       const int e = lane + 32 * m;
-      lv[m] = (e < E) ? row[e] : 0.f;
+      key[m] = (e < E) ? route_key(__ldg(row + e)) : 0u;
+      idx[m] = m;
+    }
+    // With up to 8 experts a lane sorts its list once (key descending, then id
+    // ascending; a bitonic network on registers) and each pick pops the head;
+    // with more, the lane recomputes its best untaken expert after each pick.
+    constexpr bool kSorted = SLOTS <= 8;
+    if (kSorted) {
+#pragma unroll
+      for (int k = 2; k <= SLOTS; k <<= 1)
+#pragma unroll
+        for (int j = k >> 1; j > 0; j >>= 1)
+#pragma unroll
+          for (int i = 0; i < SLOTS; ++i) {
+            const int l = i ^ j;
+            if (l <= i) continue;
+            // in the block (i & k) == 0 the better entry goes first, else last
+            const bool l_better = key[l] > key[i] || (key[l] == key[i] && idx[l] < idx[i]);
+            const bool swap = ((i & k) == 0) ? l_better : !l_better;
+            const uint32_t ki = key[i], kl = key[l];
+            const int ii = idx[i], il = idx[l];
+            key[i] = swap ? kl : ki;
+            key[l] = swap ? ki : kl;
+            idx[i] = swap ? il : ii;
+            idx[l] = swap ? ii : il;
+          }
     }
     uint32_t taken = 0u;
-    float first = 0.f, sum = 0.f;
+    // the lane's best untaken expert: highest key, then lowest m (= lowest id)
+    auto local_best = [&](uint32_t& bk, int& bm) {
+      if (kSorted) {
+        bk = key[0];
+        bm = (lane + 32 * idx[0] < E) ? idx[0] : -1;
+        return;
+      }
+      bk = 0u;
+      bm = -1;
+#pragma unroll
+      for (int m = 0; m < SLOTS; ++m) {
+        const bool live = (lane + 32 * m < E) && !((taken >> m) & 1u);
+        if (live && (bm < 0 || key[m] > bk)) {
+          bk = key[m];
+          bm = m;
+        }
+      }
+    };
+    uint32_t bk;
+    int bm;
+    local_best(bk, bm);
+    float first = 0.f;
     for (int i = 0; i < top_k; ++i) {
-      float bv = -__int_as_float(0x7f800000);  // -inf
-      int be = INT32_MAX;
-#pragma unroll
-      for (int m = 0; m < kSlots; ++m) {
-        const int e = lane + 32 * m;
-        if (e < E && !((taken >> m) & 1u) && route_better(lv[m], e, bv, be)) {
-          bv = lv[m];
-          be = e;
-        }
-      }
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) {
-        const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
-        const int oe = __shfl_xor_sync(0xffffffffu, be, off);
-        if (route_better(ov, oe, bv, be)) {
-          bv = ov;
-          be = oe;
-        }
-      }
-      if ((be & 31) == lane) taken |= 1u << (be >> 5);
+      const uint32_t kmax = __reduce_max_sync(0xffffffffu, bm >= 0 ? bk : 0u);
+      const unsigned cand = (bm >= 0 && bk == kmax) ? (unsigned)(lane + 32 * bm) : 0xFFFFFFFFu;
+      const int win = (int)__reduce_min_sync(0xffffffffu, cand);
+      const float v = route_key_value(kmax);
+      if (i == 0) first = v;
       if (lane == 0) {
-        s_ids[warp][i] = be;
-        s_val[warp][i] = bv;
+        s_ids[warp][i] = win;
+        s_w[warp][i] = v;
       }
-      if (i == 0) first = bv;
+      if ((win & 31) == lane) {
+        if (kSorted) {  // pop the head
+#pragma unroll
+          for (int m = 0; m + 1 < SLOTS; ++m) {
+            key[m] = key[m + 1];
+            idx[m] = idx[m + 1];
+          }
+          key[SLOTS - 1] = 0u;
+          idx[SLOTS - 1] = SLOTS;  // expert lane + 32 SLOTS >= E: never live
+        } else {
+          taken |= 1u << (win >> 5);
+        }
+        local_best(bk, bm);
+      }
     }
-    __syncwarp();  // lane 0's writes, visible to the whole warp
+    __syncwarp();
     // softmax over the selection (the first selected logit is the largest)
-    for (int i = 0; i < top_k; ++i) sum += expf(s_val[warp][i] - first);
+    float sum = 0.f;
+    for (int i = 0; i < top_k; ++i) sum += expf(s_w[warp][i] - first);
+    __syncwarp();
     if (lane < top_k) {
-      ids[warp * top_k + lane] = s_ids[warp][lane];
-      w[warp * top_k + lane] = expf(s_val[warp][lane] - first) / sum;
+      const int e = s_ids[warp][lane];
+      const float wt = expf(s_w[warp][lane] - first) / sum;
+      s_w[warp][lane] = wt;
+      ids[warp * top_k + lane] = e;
+      w[warp * top_k + lane] = wt;
+      atomicAdd(&cnt[e], 1);
+      atomicOr(&rowmask[e], 1u << warp);
     }
   }
   __syncthreads();
 
-  // ---- group: per-expert counts, offsets, hit slots ----
-  const int pairs = S * top_k;
-  for (int pidx = tid; pidx < pairs; pidx += blockDim.x) atomicAdd(&cnt[s_ids[pidx / top_k][pidx % top_k]], 1);
-  __syncthreads();
-  int total = 0;
+  // ---- group: one scan of (count << 16 | hit) over the experts ----
   const int c = (tid < E) ? cnt[tid] : 0;
-  const int off = block_excl_scan(c, wsum, &total);
-  if (tid < E) offsets[tid] = off;
-  if (tid == 0) offsets[E] = total;
-  int nh = 0;
-  const int f = (c > 0) ? 1 : 0;
-  const int sl = block_excl_scan(f, wsum, &nh);
+  int total = 0;
+  const int packed = block_excl_scan((c << 16) | (c > 0 ? 1 : 0), wsum, &total);
   if (tid < E) {
-    slot[tid] = sl;
-    if (f) hit[sl] = tid;
+    const int off = packed >> 16, sl = packed & 0xFFFF;
+    s_off[tid] = off;
+    s_slot[tid] = sl;
+    offsets[tid] = off;
+    if (c > 0) hit[sl] = tid;
   }
-  if (tid == 0) *n_hit = nh;
-  // zero the routing-weight table, then fill it and the per-expert row lists
+  if (tid == 0) {
+    offsets[E] = total >> 16;
+    *n_hit = total & 0xFFFF;
+  }
   if (row_w != nullptr)
     for (int v = tid; v < S * n_cap; v += blockDim.x) row_w[v] = 0.f;
-  for (int e = tid; e < kMaxExperts; e += blockDim.x) cnt[e] = (e < E) ? offsets[e] : 0;
   __syncthreads();
+  const int pairs = S * top_k;
   for (int pidx = tid; pidx < pairs; pidx += blockDim.x) {
     const int s = pidx / top_k, i = pidx - s * top_k;
     const int e = s_ids[s][i];
-    // rows before s that also selected e (each row selects an expert at most once)
-    int before = 0;
-    for (int s2 = 0; s2 < s; ++s2)
-      for (int i2 = 0; i2 < top_k; ++i2) before += (s_ids[s2][i2] == e) ? 1 : 0;
-    pair_rows[cnt[e] + before] = s;
-    if (row_w != nullptr) row_w[s * n_cap + slot[e]] = w[pidx];
+    pair_rows[s_off[e] + __popc(rowmask[e] & ((1u << s) - 1u))] = s;
+    if (row_w != nullptr) row_w[s * n_cap + s_slot[e]] = s_w[s][i];
   }
 }
 
