@@ -157,46 +157,54 @@ GemmPlan plan_gemm(int qbits, int n, int k, int S, bool allow_split) {
 // mma.sync path, 2 = the tcgen05 path only.
 std::atomic<int> g_gemm_path{0};
 
-// tcgen05 path plan: 128-row tiles, one CTA per SM; split-K (Y only) until the
-// tiles cover the SMs and the window rows of one split fit next to a ring of at
-// least four stages.
-GemmPlan plan_tc(int qbits, int n, int k, int S, bool allow_split) {
-  GemmPlan pl;
+// tcgen05 path plan: 128-row tiles, at most one CTA per SM.  Without split-K
+// (the verify head, the MoE gate/up) one split covers the full reduction.
+// With split-K every split count whose window rows fit next to a ring of at
+// least four stages is costed in bytes at the HBM rate: the busiest CTA's weight
+// stages (a stage is one 128 x 256 code tile; every SM streams at the same rate)
+// plus the split partials' write and read-back; the cheapest wins, ties to fewer
+// splits.  `unit` tiles move together (2: the gate/up pairs of the fused SwiGLU).
+GemmPlan plan_tc(int qbits, int n, int k, int S, bool allow_split, int unit = 1) {
+  GemmPlan best;
   const int sms = device_sms();
   const int limit = device_smem_optin();
-  if (sms <= 0 || limit <= 0) return pl;
+  if (sms <= 0 || limit <= 0) return best;
   const int tiles = (n + 127) / 128;
+  const int units = tiles / unit > 0 ? tiles / unit : 1;
   const int kst = (k + 255) / 256;
-  int want = 1;  // requested splits; rounding the chunk to 256 may give fewer
-  if (allow_split) {
-    want = (sms + tiles - 1) / tiles;
-    if (want > kst) want = kst;
-  }
-  for (;; ++want) {
-    int k_chunk = k, splits = 1;
-    if (want > 1) {
-      k_chunk = ((k + want - 1) / want + 255) / 256 * 256;
-      splits = (k + k_chunk - 1) / k_chunk;
-    }
-    for (int d = kMaxDepth; d >= 4; --d) {  // tc_plan_valid rejects shallower rings
+  const long long stage_bytes = 128LL * 128 * (qbits == 8 ? 2 : 1);
+  long long best_cost = 0;
+  for (int want = 1; want <= (allow_split ? kst : 1); ++want) {
+    const int stages = (kst + want - 1) / want;  // per split
+    const int k_chunk = want > 1 ? stages * 256 : k;
+    const int splits = (k + k_chunk - 1) / k_chunk;
+    if (splits != want) continue;  // the same chunk as a smaller split count
+    int depth = 0, bytes = 0;
+    for (int d = kMaxDepth; d >= 4 && depth == 0; --d) {  // tc_plan_valid rejects shallower rings
       const int b = sdv::tc_smem_bytes(qbits, S, k_chunk, d);
       if (b <= limit && sdv::tc_plan_valid(qbits, S, k_chunk, d)) {
-        pl.splits = splits;
-        pl.k_chunk = k_chunk;
-        pl.depth = d;
-        // at least half the SM's shared memory: one CTA (one 512-column tensor
-        // memory allocation) per SM
-        pl.smem = b > limit / 2 + 1024 ? b : limit / 2 + 1024;
-        // one wave: at most one CTA per SM over all splits
-        int grid = sms / splits;
-        if (grid > tiles) grid = tiles;
-        pl.grid = grid < 1 ? 1 : grid;
-        pl.tc = true;
-        return pl;
+        depth = d;
+        bytes = b;
       }
     }
-    if (!allow_split || want >= kst) return GemmPlan{};
+    if (depth == 0) continue;
+    int grid = sms / splits;  // one wave: at most one CTA per SM over all splits
+    if (grid > units) grid = units;
+    if (grid < 1) continue;
+    const long long busiest = (long long)((units + grid - 1) / grid) * unit * stages;
+    const long long cost = busiest * stage_bytes * sms + (splits > 1 ? 2LL * splits * S * n * 4 : 0);
+    if (best.splits != 0 && cost >= best_cost) continue;
+    best_cost = cost;
+    best.splits = splits;
+    best.k_chunk = k_chunk;
+    best.depth = depth;
+    // at least half the SM's shared memory: one CTA (one 512-column tensor
+    // memory allocation) per SM
+    best.smem = bytes > limit / 2 + 1024 ? bytes : limit / 2 + 1024;
+    best.grid = grid;
+    best.tc = true;
   }
+  return best;
 }
 
 GemmPlan choose_plan(int qbits, int n, int k, int S, bool allow_split) {
@@ -319,7 +327,7 @@ size_t align256(size_t b) { return (b + 255) / 256 * 256; }
 // [splits][S][2n] in the workspace, then the reduce that applies SwiGLU.
 GemmPlan plan_swiglu(int qbits, int n, int k, int S) {
   if (k % 256 != 0) return GemmPlan{};
-  return plan_tc(qbits, 2 * n, k, S, true);
+  return plan_tc(qbits, 2 * n, k, S, true, 2);
 }
 
 size_t swiglu_ws_bytes(int qbits, int n, int k, int S) {
