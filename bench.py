@@ -222,9 +222,10 @@ def oracle_sample(wl, S: int, budget_s: float):
         total = wl.n
         t0 = time.perf_counter()
         while True:
-            y = verify.dequant_gemm64(x, codes, scales)
+            take = min(rows, total - done)  # the last block stops at the vocabulary's end
+            y = verify.dequant_gemm64(x, codes[:take], scales[:take])
             verify.argmax_rows(y.astype(np.float32))
-            done += rows
+            done += take
             t_used = time.perf_counter() - t0
             if t_used >= budget_s or done >= total:
                 break
