@@ -579,6 +579,56 @@ def run_sdv(args, wl, S, world, rank, local):
     return 0
 
 
+def run_spec_loop(args, wl, S):
+    """End-to-end greedy n-gram speculative decoding through the verify head:
+    the toy model body of ``synth.toy_model`` feeds hidden rows, the host loop
+    drafts and commits, every round is one ``sdv_verify_head`` call.  Prints one
+    JSON line: spec tokens/s against plain greedy (S = 1 per token), both wall
+    clock on the host (the loop is synchronous), losslessness, tokens per
+    round against E(alpha, K)."""
+    import torch
+    from speculative_decode_verify_sdv_gb300 import build, sdv, specdec
+    from synth.toy_model import ToyHidden
+    if wl.kind != "head":
+        raise SystemExit("--spec-loop needs a head workload (tiny, q4b, a3b)")
+    build.build()
+    sdv.load()
+    dev = "cuda:0"
+    torch.cuda.set_device(0)
+    w = torch.from_numpy(W.head_weights(wl)).to(dev)
+    head = sdv.quantize(w, wl.bits)
+    del w
+    torch.cuda.synchronize()
+    K = S - 1
+    hidden = ToyHidden(wl.h, W.stream_seed(wl.key, 90), lambda t: W.head_weights(wl, slice(t, t + 1))[0],
+                       W.W_SIGMA, p_echo=args.p_echo, period=5)
+    prompt = [int(t) for t in W.randint(W.stream_seed(wl.key, 91), 32, wl.n)]
+    ver1, verS = specdec.HeadVerifier(head, 1, device=dev), specdec.HeadVerifier(head, S, device=dev)
+    specdec.spec_decode(verS, hidden, prompt, 16, K, args.ngram)   # warm-up (shapes, caches)
+    specdec.greedy_decode(ver1, hidden, prompt, 16)
+    t0 = time.perf_counter()
+    greedy = specdec.greedy_decode(ver1, hidden, prompt, args.gen)
+    t1 = time.perf_counter()
+    stats = {}
+    spec = specdec.spec_decode(verS, hidden, prompt, args.gen, K, args.ngram, stats)
+    t2 = time.perf_counter()
+    alpha = specdec.alpha_estimate(stats)
+    per_round = (stats["accepted"] + stats["rounds"]) / max(1, stats["rounds"])
+    line = {
+        "metric": "greedy n-gram spec-decode tokens/s through the verify head (toy model body)",
+        "value": args.gen / (t2 - t1), "unit": "tokens/s", "higher_is_better": True,
+        "greedy_tokens_per_s": args.gen / (t1 - t0), "speedup": (t1 - t0) / (t2 - t1),
+        "lossless": spec == greedy, "rounds": stats["rounds"], "accepted": stats["accepted"],
+        "tokens_per_round": per_round, "alpha": alpha,
+        "E_alpha_K": specdec.expected_tokens_per_round(alpha, K), "K": K, "ngram": args.ngram,
+        "gen": args.gen, "p_echo": args.p_echo,
+        "config": {"workload": workload_name(wl, S), "S": S, "model_body": "synth.toy_model.ToyHidden (period 5)"},
+        "timing": "host wall clock around each whole decode (H2D of the window, the call, D2H, sync per round)",
+    }
+    print(json.dumps(line), flush=True)
+    return 0 if line["lossless"] else 1
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -591,11 +641,18 @@ def main(argv=None):
     ap.add_argument("--cpu-budget", type=float, default=10.0)
     ap.add_argument("--path", choices=["auto", "mma", "tc"], default="auto",
                     help="GEMM implementation (auto: tcgen05 where its plan fits)")
+    ap.add_argument("--spec-loop", action="store_true",
+                    help="end-to-end n-gram speculative decoding on the head workload instead of the kernel bench")
+    ap.add_argument("--gen", type=int, default=512, help="--spec-loop: tokens to generate")
+    ap.add_argument("--ngram", type=int, default=3, help="--spec-loop: n-gram order of the drafter")
+    ap.add_argument("--p-echo", type=float, default=0.7, help="--spec-loop: share of echo contexts in the toy model")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3
     wl = W.BY_NAME[args.config]
     S = args.S or wl.s_default
+    if args.spec_loop:
+        return run_spec_loop(args, wl, S)
     world, rank, local = dist_setup()
     if args.impl == "reference":
         return run_reference(args, wl, S, world, rank)
