@@ -1,0 +1,137 @@
+"""Sampling (temperature > 0) verify of speculative decoding -- TEST
+INFRASTRUCTURE ONLY (imported by tests/, __graft_entry__.smoke() and the CPU
+baseline of bench.py; never by the product path).
+
+The pages defer it: "Stream C -- Speculative decoding: feasibility verdict +
+implementation plan", section "Deferred / harder": a lossless sampling verify
+needs the probabilities and a resample from the residual distribution, not the
+argmax.  The method is speculative sampling (Leviathan, Kalman & Matias, "Fast
+Inference from Transformers via Speculative Decoding", ICML 2023; Chen et al.,
+"Accelerating Large Language Model Decoding with Speculative Sampling", 2023):
+draft token d drawn from q is kept with probability min(1, p(d) / q(d)); at the
+first rejection the token is drawn from norm(max(0, p - q)); when every draft
+is kept the bonus token is drawn from the last row's p.  The n-gram drafter of
+the pages proposes one token deterministically, q = the point mass on d, so:
+
+* keep d_i iff u_i < p_i(d_i)            (u_i uniform on (0, 1));
+* at the first rejection, row j: draw from p_j restricted to v != d_j,
+  renormalised (norm(max(0, p - q)) for a point-mass q);
+* all kept: draw from p_{n_valid};
+
+with p_i = softmax(L_i / T) over the vocabulary, L_i the logits of window row i.
+Draws use the Gumbel-max trick (Gumbel 1954; Maddison, Tarlow & Minka 2014):
+argmax_v (L_i(v) / T + g_i(v)) with g i.i.d. standard Gumbel is a draw from
+p_i, and the same argmax over v != d is a draw from the residual.
+
+Random numbers come from a counter-based generator implemented here from its
+published definition (the kernel implements its own copy; the two share no
+code): SplitMix64 (Steele, Lea & Flood, OOPSLA 2014; finaliser constants as
+published by Vigna) keyed by (seed, counter):
+
+    key    = mix(seed + (counter + 1) * G)          (mod 2**64, G = 0x9E3779B97F4A7C15)
+    raw(e) = mix(key + (e + 1) * G)
+    u(e)   = (2 * (raw(e) >> 41) + 1) * 2**-24      in (0, 1), exact in fp32
+    Gumbel for row i, entry v:   e = i * V + v,  g = -log(-log(u))
+    acceptance uniform, row i:   e = 32 * V + i
+
+-log(u) is taken as -log1p(-(1 - u)) (1 - u is exact), which keeps the large-g
+tail (u near 1) accurate.  Everything here is fp64.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+G = np.uint64(0x9E3779B97F4A7C15)
+_M1 = np.uint64(0xBF58476D1CE4E5B9)
+_M2 = np.uint64(0x94D049BB133111EB)
+MAX_ROWS = 32
+
+
+def mix(z):
+    """SplitMix64 finaliser on uint64 (array or scalar), mod 2**64."""
+    z = np.asarray(z, dtype=np.uint64).copy()
+    with np.errstate(over="ignore"):
+        z ^= z >> np.uint64(30)
+        z *= _M1
+        z ^= z >> np.uint64(27)
+        z *= _M2
+        z ^= z >> np.uint64(31)
+    return z
+
+
+def rng_key(seed: int, counter: int) -> np.uint64:
+    with np.errstate(over="ignore"):
+        return mix(np.uint64(seed % 2**64) + (np.uint64(counter % 2**64) + np.uint64(1)) * G)[()]
+
+
+def uniforms(key, idx) -> np.ndarray:
+    """u(e) for the element indices ``idx`` (float64 values exact in fp32)."""
+    idx = np.asarray(idx, dtype=np.uint64)
+    with np.errstate(over="ignore"):
+        raw = mix(np.uint64(key) + (idx + np.uint64(1)) * G)
+    k = (raw >> np.uint64(41)).astype(np.float64)
+    return (2.0 * k + 1.0) * 2.0 ** -24
+
+
+def gumbel(key, S: int, V: int) -> np.ndarray:
+    """Standard Gumbel noise ``[S, V]``: row i, entry v uses element i * V + v."""
+    e = np.arange(S, dtype=np.uint64)[:, None] * np.uint64(V) + np.arange(V, dtype=np.uint64)[None, :]
+    u = uniforms(key, e)
+    w = -np.log1p(-(1.0 - u))     # -log(u)
+    return -np.log(w)
+
+
+def accept_uniforms(key, S: int, V: int) -> np.ndarray:
+    return uniforms(key, np.uint64(MAX_ROWS) * np.uint64(V) + np.arange(S, dtype=np.uint64))
+
+
+def _first_argmax(z: np.ndarray) -> int:
+    """Largest value, ties to the lowest index."""
+    return int(np.argmax(z))  # numpy returns the first occurrence
+
+
+def verify_sample(logits: np.ndarray, drafts, n_valid: int, temperature: float, seed: int, counter: int):
+    """Speculative-sampling verify of one window.
+
+    ``logits`` [S, V] (fp64 from ``verify.dequant_gemm64``), drafts [S-1].
+    Returns a dict: ``accepted`` (kept drafts), ``token`` (the draw at the first
+    rejection or the bonus draw), ``samples`` [S] (each row's full-distribution
+    draw), ``p_draft`` [n_valid] (p_i(d_i)), ``u`` [S] and, for tolerance
+    decisions, ``z_gap`` [S] (top-2 gap of L/T + g per row), ``z_gap_res``
+    [S] (the same gap with the row's draft excluded) and ``u_margin`` (the
+    smallest |u_i - p_i(d_i)| over the rows the accept scan read).
+    """
+    if not temperature > 0.0:
+        raise ValueError("temperature must be > 0")
+    L = np.asarray(logits, dtype=np.float64)
+    S, V = L.shape
+    if not 1 <= S <= MAX_ROWS or not 0 <= n_valid <= S - 1:
+        raise ValueError("bad window")
+    key = rng_key(seed, counter)
+    l = L / temperature
+    z = l + gumbel(key, S, V)
+    u = accept_uniforms(key, S, V)
+    samples = np.array([_first_argmax(z[i]) for i in range(S)], dtype=np.int32)
+    m = l.max(axis=1, keepdims=True)
+    p = np.exp(l - m)
+    p /= p.sum(axis=1, keepdims=True)
+    d = np.asarray(drafts, dtype=np.int64)[:n_valid]
+    p_draft = np.array([p[i, d[i]] for i in range(n_valid)])
+
+    def top2_gap(row):
+        s = np.sort(row)
+        return float(s[-1] - s[-2]) if row.size > 1 else np.inf
+
+    z_gap = np.array([top2_gap(z[i]) for i in range(S)])
+    z_gap_res = np.full(S, np.inf)
+    j, token, margin = n_valid, int(samples[n_valid]), np.inf
+    for i in range(n_valid):
+        margin = min(margin, abs(u[i] - p_draft[i]))
+        zr = z[i].copy()
+        zr[d[i]] = -np.inf
+        z_gap_res[i] = top2_gap(zr)
+        if not u[i] < p_draft[i]:
+            j, token = i, _first_argmax(zr)
+            break
+    return {"accepted": j, "token": token, "samples": samples, "p_draft": p_draft, "u": u,
+            "z_gap": z_gap, "z_gap_res": z_gap_res, "u_margin": margin, "probs": p}
