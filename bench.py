@@ -371,6 +371,32 @@ class HeadJob:
         self.out_host[j, S + 1:].copy_(self.nxt1, non_blocking=True)
 
 
+class SampleJob(HeadJob):
+    """sdv_verify_sample (temperature 1, a fresh counter per window) on the head
+    workload: the same weight stream with the sampling epilogue."""
+
+    def __init__(self, sdv, torch, wl, S, dev, nwin):
+        super().__init__(sdv, torch, wl, S, dev, nwin)
+        self.ws = sdv.workspace(sdv.SDV_OP_VERIFY_SAMPLE, wl.n, wl.h, S, device=dev)
+        self.ws_list = [self.ws]
+        self.kernel = "sampling verify: GEMM + Gumbel-max draws + softmax + accept (one launch)"
+
+    def step(self, i):
+        j = i % self.nwin
+        self.sdv.sdv_verify_sample(self.head, self.x_dev[j], self.S, self.d_dev[j], self.n_valid, 1.0, 1, i, None,
+                                   self.am[j], self.acc[j], self.nxt[j], self.ws)
+
+    def e2e_step(self, i):
+        j, S = i % self.nwin, self.S
+        self.x_stage.copy_(self.x_host[j], non_blocking=True)
+        self.d_stage.copy_(self.d_host[j], non_blocking=True)
+        self.sdv.sdv_verify_sample(self.head, self.x_stage, S, self.d_stage, self.n_valid, 1.0, 1, i, None,
+                                   self.am1, self.acc1, self.nxt1, self.ws)
+        self.out_host[j, :S].copy_(self.am1, non_blocking=True)
+        self.out_host[j, S:S + 1].copy_(self.acc1, non_blocking=True)
+        self.out_host[j, S + 1:].copy_(self.nxt1, non_blocking=True)
+
+
 class MlpJob:
     """Dense SwiGLU MLP: sdv_qlinear_swiglu (gate/up) then sdv_qlinear (down)."""
 
@@ -490,7 +516,8 @@ def run_sdv(args, wl, S, world, rank, local):
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     nwin = min(wl.windows, max(1, args.windows))
-    job = JOBS[wl.kind](sdv, torch, wl, S, dev, nwin)
+    sampling = args.verify == "sample" and wl.kind == "head"
+    job = (SampleJob if sampling else JOBS[wl.kind])(sdv, torch, wl, S, dev, nwin)
     stream = torch.cuda.current_stream()
 
     def status_ok():
@@ -554,13 +581,15 @@ def run_sdv(args, wl, S, world, rank, local):
     value = world * args.steps / (elapsed_ms / 1000.0)
     peak, kind = measured_peak()
     achieved = nbytes / (kernel_ms / 1000.0) / 1e9
-    traffic, traffic_src = (profiled_traffic(f"{wl.name} S={S}") if wl.kind == "head" else (None, None))
+    prof_key = f"{wl.name} S={S}" + (" sample" if sampling else "")
+    traffic, traffic_src = (profiled_traffic(prof_key) if wl.kind == "head" else (None, None))
     cpu_rate, cpu_desc = oracle_sample(wl, S, args.cpu_budget) if args.cpu_budget > 0 else (None, "skipped")
     line = {
         "metric": METRIC, "value": value, "unit": "windows/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": elapsed_ms / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f16 x int%d -> f32" % wl.bits, "data": "synthetic",
-        "config": {"workload": workload_name(wl, S), "S": S, "windows": nwin, "bytes_per_window": nbytes,
+        "config": {"workload": workload_name(wl, S) + (", sampling verify T=1" if sampling else ""), "S": S,
+                   "windows": nwin, "bytes_per_window": nbytes,
                    "l2": "inputs larger than L2 (weight stream %.0f MB > 129 MB)" % (nbytes / 1e6),
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "weight_gbs": achieved, "hbm_frac": achieved / peak,
@@ -641,6 +670,8 @@ def main(argv=None):
     ap.add_argument("--cpu-budget", type=float, default=10.0)
     ap.add_argument("--path", choices=["auto", "mma", "tc"], default="auto",
                     help="GEMM implementation (auto: tcgen05 where its plan fits)")
+    ap.add_argument("--verify", choices=["greedy", "sample"], default="greedy",
+                    help="head workloads: greedy verify (sdv_verify_head) or sampling verify at T = 1")
     ap.add_argument("--spec-loop", action="store_true",
                     help="end-to-end n-gram speculative decoding on the head workload instead of the kernel bench")
     ap.add_argument("--gen", type=int, default=512, help="--spec-loop: tokens to generate")

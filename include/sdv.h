@@ -80,7 +80,8 @@ typedef enum {
   SDV_OP_QLINEAR = 1,
   SDV_OP_QLINEAR_SWIGLU = 2,
   SDV_OP_VERIFY_HEAD = 3,
-  SDV_OP_MOE = 4
+  SDV_OP_MOE = 4,
+  SDV_OP_VERIFY_SAMPLE = 5
 } sdv_op;
 
 /*
@@ -151,6 +152,40 @@ SDV_API sdv_status sdv_verify_head(const sdv_qweight* head, const uint16_t* x, i
                            const int32_t* drafts, int32_t n_valid, float* logits_or_null,
                            int32_t* argmax, int32_t* accepted, int32_t* next_a0,
                            void* ws, size_t ws_bytes, sdv_stream_t stream);
+
+/*
+ * The sampling (temperature > 0) verify of one window: speculative sampling
+ * (Leviathan, Kalman & Matias, ICML 2023) with a drafter that proposes each
+ * token deterministically, the lossless temperature > 0 variant that "Stream C --
+ * Speculative decoding: feasibility verdict + implementation plan" defers
+ * (section "Deferred / harder": probabilities and a residual resample).
+ *   p_i(v)   = softmax over v of logits[i][v] / temperature   (logits as in
+ *              sdv_verify_head)
+ *   samples[i] = argmax_v ( logits[i][v] / temperature + g_i(v) )   (Gumbel-max
+ *              draw from p_i; ties to the lower v)
+ *   accepted = the first i < n_valid with NOT (u_i < p_i(drafts[i])), else n_valid
+ *   next_token = at a rejection in row i: argmax over v != drafts[i] of
+ *              logits[i][v] / temperature + g_i(v) (a draw from the residual
+ *              distribution); when every draft is kept: samples[n_valid]
+ * Random numbers: SplitMix64 (Steele, Lea & Flood 2014) keyed by
+ *   key = mix(seed + (counter + 1) * 0x9E3779B97F4A7C15); output
+ *   w(c) = mix(key + (c + 1) * 0x9E3779B97F4A7C15) carries element 2c in its low
+ *   and 2c + 1 in its high 32 bits h, u = (2 * (h >> 9) + 1) * 2^-24;
+ *   g_i(v) = -log(-log(u)) with e = 32 * v + i; u_i with e = 32 * n + i.
+ *   A caller advances `counter` once per call.
+ * Arguments as for sdv_verify_head; temperature: finite and > 0 (else
+ * SDV_ERR_INVALID_ARG); samples: int32 [S]; next_token: int32 [1]; the workspace
+ * is sdv_workspace_bytes(SDV_OP_VERIFY_SAMPLE, n, k, S, 0, 0) bytes.  Runs on the
+ * tcgen05 path only: SDV_ERR_UNSUPPORTED where its plan does not fit (window rows
+ * x reduction length beyond shared memory, e.g. an int8 head with k = 2560 at S >= 17).
+ * One kernel launch; fp32 logits, so a draw or an accept whose margin is below
+ * the logits' rounding may differ from an fp64 evaluation.
+ */
+SDV_API sdv_status sdv_verify_sample(const sdv_qweight* head, const uint16_t* x, int32_t S,
+                             const int32_t* drafts, int32_t n_valid, float temperature,
+                             uint64_t seed, uint64_t counter, float* logits_or_null,
+                             int32_t* samples, int32_t* accepted, int32_t* next_token,
+                             void* ws, size_t ws_bytes, sdv_stream_t stream);
 
 /*
  * sdv_verify_head without a workspace, for callers that cannot allocate device

@@ -29,9 +29,10 @@ code): SplitMix64 (Steele, Lea & Flood, OOPSLA 2014; finaliser constants as
 published by Vigna) keyed by (seed, counter):
 
     key    = mix(seed + (counter + 1) * G)          (mod 2**64, G = 0x9E3779B97F4A7C15)
-    raw(e) = mix(key + (e + 1) * G)
-    u(e)   = (2 * (raw(e) >> 41) + 1) * 2**-24      in (0, 1), exact in fp32
-    Gumbel for row i, entry v:   e = i * V + v,  g = -log(-log(u))
+    w(c)   = mix(key + (c + 1) * G)                  one output per pair of elements
+    h(e)   = the low 32 bits of w(e >> 1) for even e, the high 32 bits for odd e
+    u(e)   = (2 * (h(e) >> 9) + 1) * 2**-24         in (0, 1), exact in fp32
+    Gumbel for row i, entry v:   e = 32 * v + i,  g = -log(-log(u))
     acceptance uniform, row i:   e = 32 * V + i
 
 -log(u) is taken as -log1p(-(1 - u)) (1 - u is exact), which keeps the large-g
@@ -68,14 +69,15 @@ def uniforms(key, idx) -> np.ndarray:
     """u(e) for the element indices ``idx`` (float64 values exact in fp32)."""
     idx = np.asarray(idx, dtype=np.uint64)
     with np.errstate(over="ignore"):
-        raw = mix(np.uint64(key) + (idx + np.uint64(1)) * G)
-    k = (raw >> np.uint64(41)).astype(np.float64)
+        w = mix(np.uint64(key) + ((idx >> np.uint64(1)) + np.uint64(1)) * G)
+    half = np.where((idx & np.uint64(1)) == 1, w >> np.uint64(32), w & np.uint64(0xFFFFFFFF))
+    k = (half >> np.uint64(9)).astype(np.float64)
     return (2.0 * k + 1.0) * 2.0 ** -24
 
 
 def gumbel(key, S: int, V: int) -> np.ndarray:
-    """Standard Gumbel noise ``[S, V]``: row i, entry v uses element i * V + v."""
-    e = np.arange(S, dtype=np.uint64)[:, None] * np.uint64(V) + np.arange(V, dtype=np.uint64)[None, :]
+    """Standard Gumbel noise ``[S, V]``: row i, entry v uses element 32 * v + i."""
+    e = np.arange(V, dtype=np.uint64)[None, :] * np.uint64(MAX_ROWS) + np.arange(S, dtype=np.uint64)[:, None]
     u = uniforms(key, e)
     w = -np.log1p(-(1.0 - u))     # -log(u)
     return -np.log(w)

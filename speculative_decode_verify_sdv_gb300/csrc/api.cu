@@ -4,12 +4,14 @@
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
+#include <cmath>
 #include <cstdint>
 #include <cstring>
 #include <atomic>
 #include <mutex>
 
 #include "sdv.h"
+#include "sdv_device.cuh"
 #include "sdv_kernels.h"
 
 namespace {
@@ -221,6 +223,12 @@ size_t head_ws_bytes(int S) {
   return kWsHeader + (size_t)(sms > 0 ? sms : 1024) * (size_t)S * 8;
 }
 
+// [grid][S][8] floats of per-CTA sampling partials behind the header
+size_t sample_ws_bytes(int S) {
+  const int sms = device_sms();
+  return kWsHeader + (size_t)(sms > 0 ? sms : 1024) * (size_t)S * 32;
+}
+
 size_t qlinear_ws_bytes(int qbits, int n, int k, int S) {
   size_t need = kWsHeader;
   for (const GemmPlan& pl : {plan_gemm(qbits, n, k, S, true), plan_tc(qbits, n, k, S, true)}) {
@@ -244,6 +252,10 @@ sdv_status run_gemm(const sdv_qweight* w, const uint16_t* x, int S, int mode, Ge
   if (mode == sdv::kModeHead) {
     a.part_v = reinterpret_cast<float*>(static_cast<char*>(ws) + kWsHeader);
     a.part_i = reinterpret_cast<int*>(static_cast<char*>(ws) + kWsHeader + (size_t)pl.grid * S * 4);
+  }
+  if (mode == sdv::kModeSample) {
+    if (!pl.tc) return SDV_ERR_UNSUPPORTED;  // the sampling epilogue exists on the tcgen05 path only
+    a.part_s = reinterpret_cast<float*>(static_cast<char*>(ws) + kWsHeader);
   }
   CUtensorMap tc, tsc;
   int scales_tma = 0;
@@ -450,6 +462,7 @@ size_t sdv_workspace_bytes(int32_t op, int32_t n, int32_t k, int32_t S, int32_t 
       return a > b ? a : b;
     }
     case SDV_OP_VERIFY_HEAD: return head_ws_bytes(S);
+    case SDV_OP_VERIFY_SAMPLE: return sample_ws_bytes(S);
     case SDV_OP_MOE: {  // n = I, k = H
       if (E < 1 || top_k < 1 || top_k > E) return 0;
       const MoeLayout a = plan_moe(8, E, n, k, top_k, S), b = plan_moe(4, E, n, k, top_k, S);
@@ -495,6 +508,33 @@ sdv_status sdv_qlinear(const sdv_qweight* w, const uint16_t* x, int32_t S, float
   if (ws == nullptr || !aligned16(ws) || ws_bytes < kWsHeader) return SDV_ERR_WORKSPACE;
   GemmArgs a{};
   return run_gemm(w, x, S, sdv::kModeY, a, ws, ws_bytes, y, reinterpret_cast<cudaStream_t>(stream));
+}
+
+sdv_status sdv_verify_sample(const sdv_qweight* head, const uint16_t* x, int32_t S, const int32_t* drafts,
+                             int32_t n_valid, float temperature, uint64_t seed, uint64_t counter,
+                             float* logits_or_null, int32_t* samples, int32_t* accepted, int32_t* next_token,
+                             void* ws, size_t ws_bytes, sdv_stream_t stream) {
+  if (!valid_weight(head) || x == nullptr || !aligned16(x)) return SDV_ERR_INVALID_ARG;
+  if (samples == nullptr || accepted == nullptr || next_token == nullptr) return SDV_ERR_INVALID_ARG;
+  if (!(temperature > 0.f) || !(temperature < INFINITY)) return SDV_ERR_INVALID_ARG;
+  if (S < 1) return SDV_ERR_INVALID_ARG;
+  if (S > kMaxS) return SDV_ERR_UNSUPPORTED;
+  if (n_valid < 0 || n_valid > S - 1) return SDV_ERR_INVALID_ARG;
+  if (n_valid > 0 && drafts == nullptr) return SDV_ERR_INVALID_ARG;
+  const size_t need = sdv_workspace_bytes(SDV_OP_VERIFY_SAMPLE, head->n, head->k, S, 0, 0);
+  if (ws == nullptr || !aligned16(ws) || ws_bytes < need) return SDV_ERR_WORKSPACE;
+  const int path = g_gemm_path.load();
+  if (path == 1) return SDV_ERR_UNSUPPORTED;
+  GemmArgs a{};
+  a.y = logits_or_null;
+  a.drafts = drafts;
+  a.n_valid = n_valid;
+  a.argmax = samples;
+  a.accepted = accepted;
+  a.next_a0 = next_token;
+  a.inv_temp = 1.f / temperature;
+  a.rng_key = sdv::splitmix_mix(seed + (counter + 1ull) * sdv::kSplitMixG);
+  return run_gemm(head, x, S, sdv::kModeSample, a, ws, ws_bytes, nullptr, reinterpret_cast<cudaStream_t>(stream));
 }
 
 sdv_status sdv_verify_head(const sdv_qweight* head, const uint16_t* x, int32_t S, const int32_t* drafts,

@@ -134,6 +134,65 @@ __device__ __forceinline__ void i4x8_to_h2x4(uint32_t w, uint32_t& p0, uint32_t&
   p3 = h2_as_u32(__hfma2(u32_as_h2(t3), sixteenth, b_hi));
 }
 
+// Counter stream of the sampling verify: SplitMix64 (Steele, Lea & Flood,
+// OOPSLA 2014; finaliser constants as published by Vigna) keyed by
+// key = mix(seed + (counter + 1) * G); output c = mix(key + (c + 1) * G) carries
+// elements 2c (low 32 bits) and 2c + 1 (high 32 bits).
+constexpr unsigned long long kSplitMixG = 0x9E3779B97F4A7C15ull;
+
+__host__ __device__ __forceinline__ unsigned long long splitmix_mix(unsigned long long z) {
+  z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+  z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+  return z ^ (z >> 31);
+}
+
+// u = (2 * (h >> 9) + 1) * 2^-24 for a 32-bit half h: in (0, 1), exact in fp32.
+__device__ __forceinline__ float half_uniform(unsigned h) {
+  return (float)(2u * (h >> 9) + 1u) * 5.9604644775390625e-8f;
+}
+
+__device__ __forceinline__ unsigned long long counter_pair(unsigned long long key, unsigned long long c) {
+  return splitmix_mix(key + (c + 1ull) * kSplitMixG);
+}
+
+// u(e) of element e.
+__device__ __forceinline__ float counter_uniform(unsigned long long key, unsigned long long e) {
+  const unsigned long long w = counter_pair(key, e >> 1);
+  return half_uniform((e & 1ull) ? (unsigned)(w >> 32) : (unsigned)w);
+}
+
+// Standard Gumbel from u: -log(-log(u)), with -log(u) = -log1p(-(1 - u)) (1 - u
+// is exact) so that the upper tail (u near 1) keeps its accuracy; the outer log
+// is the fast hardware one (absolute error ~1e-6, below what the draws compare).
+__device__ __forceinline__ float gumbel_of(float u) { return -__logf(-log1pf(-(1.f - u))); }
+
+// Top-2 under the argmax order (value desc, index asc).
+__device__ __forceinline__ void top2_add(float& z1, int& v1, float& z2, int& v2, float z, int v) {
+  if (z > z1 || (z == z1 && v < v1)) {
+    z2 = z1;
+    v2 = v1;
+    z1 = z;
+    v1 = v;
+  } else if (z > z2 || (z == z2 && v < v2)) {
+    z2 = z;
+    v2 = v;
+  }
+}
+
+// Online softmax statistics: m = max, s = sum exp(x - m); -inf entries are absent.
+__device__ __forceinline__ void softmax_merge(float& m, float& s, float m2, float s2) {
+  if (m2 == -INFINITY) return;
+  if (m == -INFINITY) {
+    m = m2;
+    s = s2;
+  } else if (m2 > m) {
+    s = s * expf(m - m2) + s2;
+    m = m2;
+  } else {
+    s += s2 * expf(m2 - m);
+  }
+}
+
 // D = A * B + C, m16n8k16, fp16 inputs, fp32 accumulate.
 __device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
                                           uint32_t a3, uint32_t b0, uint32_t b1, const float (&c)[4]) {

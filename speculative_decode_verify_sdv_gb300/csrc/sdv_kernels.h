@@ -33,6 +33,7 @@ constexpr int kDevErrTmemBase = 2;  // tensor-memory allocation not at column 0
 
 constexpr int kModeY = 0;     // write fp32 Y [S][N]
 constexpr int kModeHead = 1;  // verify head: argmax partials + last-CTA reduce + accept
+constexpr int kModeSample = 2;  // sampling verify: Gumbel-max draws + softmax partials + last-CTA accept
 
 struct GemmArgs {
   const __half* x;          // fp16 [S][K]
@@ -55,6 +56,12 @@ struct GemmArgs {
   int* part_i;              // [grid][S]
   unsigned* ticket;
   int* status;
+  // sampling verify (kModeSample): p_i = softmax(L_i * inv_temp); draws from the
+  // counter stream rng_key; per-CTA partials [grid][S][8] (top-2 of L/T + g with
+  // their entries, softmax max and sum of L/T, the draft's L/T)
+  float inv_temp;
+  unsigned long long rng_key;
+  float* part_s;
   // ---- row / reduction mappings of the tcgen05 path (kModeY; zero = plain) ----
   int ldx;                  // row stride of x in elements (0: K)
   int ldy;                  // row stride of y in elements (0: N)

@@ -94,6 +94,102 @@ __host__ __device__ inline TcPlan tc_plan(int qb, int S, int kc, int depth) {
   return p;
 }
 
+// Tail of the sampling verify, run by every thread of the CTA after the
+// teardown barrier.  `stb` holds the four epilogue warps' column states
+// ([field][quarter][S] floats).  Each CTA publishes its merged partial per
+// window row; the last CTA (acquire-release ticket, as for the verify head)
+// merges all of them in CTA order and runs the accept: draft d_i is kept iff
+// u_i < p_i(d_i) = exp(L_i(d_i)/T - M_i) / sum_v exp(L_i(v)/T - M_i); at the first
+// rejection the token is the largest L/T + g of row i other than d_i (the
+// residual draw), and if every draft is kept it is row n_valid's draw.
+__device__ __noinline__ void sample_tail(const GemmArgs& p, uint8_t* stb, const int* s_drafts, int* s_flag,
+                                         int warp, int lane, int nwarps) {
+  float* const st = reinterpret_cast<float*>(stb);
+  const int S = p.S, f = 4 * S;
+  if ((int)threadIdx.x < S) {
+    const int c = threadIdx.x;
+    float z1 = st[c], z2 = st[2 * f + c], m = st[4 * f + c], s = st[5 * f + c], ld = st[6 * f + c];
+    int v1 = __float_as_int(st[f + c]), v2 = __float_as_int(st[3 * f + c]);
+    for (int q = 1; q < 4; ++q) {
+      const int o = q * S + c;
+      top2_add(z1, v1, z2, v2, st[o], __float_as_int(st[f + o]));
+      top2_add(z1, v1, z2, v2, st[2 * f + o], __float_as_int(st[3 * f + o]));
+      softmax_merge(m, s, st[4 * f + o], st[5 * f + o]);
+      const float lq = st[6 * f + o];
+      if (lq == lq) ld = lq;
+    }
+    float* const out = p.part_s + ((size_t)blockIdx.x * S + c) * 8;
+    __stcg(out + 0, z1);
+    __stcg(out + 1, __int_as_float(v1));
+    __stcg(out + 2, z2);
+    __stcg(out + 3, __int_as_float(v2));
+    __stcg(out + 4, m);
+    __stcg(out + 5, s);
+    __stcg(out + 6, ld);
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    unsigned tk;
+    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(tk) : "l"(p.ticket) : "memory");
+    *s_flag = (tk == gridDim.x - 1) ? 1 : 0;
+  }
+  __syncthreads();
+  if (*s_flag == 0) return;
+  // merged rows: [S][8] = v1, v2, m, s, ld
+  for (int col = warp; col < S; col += nwarps) {
+    float z1 = -INFINITY, z2 = -INFINITY, m = -INFINITY, s = 0.f, ld = __int_as_float(0x7fc00000);
+    int v1 = INT_MAX, v2 = INT_MAX;
+    for (int j = lane; j < (int)gridDim.x; j += 32) {
+      const float* const in = p.part_s + ((size_t)j * S + col) * 8;
+      top2_add(z1, v1, z2, v2, __ldcg(in + 0), __float_as_int(__ldcg(in + 1)));
+      top2_add(z1, v1, z2, v2, __ldcg(in + 2), __float_as_int(__ldcg(in + 3)));
+      softmax_merge(m, s, __ldcg(in + 4), __ldcg(in + 5));
+      const float lq = __ldcg(in + 6);
+      if (lq == lq) ld = lq;
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      const float oz1 = __shfl_xor_sync(0xffffffffu, z1, off), oz2 = __shfl_xor_sync(0xffffffffu, z2, off);
+      const int ov1 = __shfl_xor_sync(0xffffffffu, v1, off), ov2 = __shfl_xor_sync(0xffffffffu, v2, off);
+      const float om = __shfl_xor_sync(0xffffffffu, m, off), os = __shfl_xor_sync(0xffffffffu, s, off);
+      const float old = __shfl_xor_sync(0xffffffffu, ld, off);
+      top2_add(z1, v1, z2, v2, oz1, ov1);
+      top2_add(z1, v1, z2, v2, oz2, ov2);
+      softmax_merge(m, s, om, os);
+      if (old == old) ld = old;
+    }
+    if (lane == 0) {
+      float* const r = st + col * 8;
+      r[0] = __int_as_float(v1);
+      r[1] = __int_as_float(v2);
+      r[2] = m;
+      r[3] = s;
+      r[4] = ld;
+      p.argmax[col] = v1;  // the row's draw from its full distribution
+    }
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int j = p.n_valid;
+    int token = __float_as_int(st[p.n_valid * 8]);
+    for (int i = 0; i < p.n_valid; ++i) {
+      const float* const r = st + i * 8;
+      const int d = s_drafts[i];
+      const float pr = expf(r[4] - r[2]) / r[3];
+      const float u = counter_uniform(p.rng_key, 32ull * (unsigned)p.N + (unsigned)i);
+      if (!(u < pr)) {
+        j = i;
+        const int a1 = __float_as_int(r[0]);
+        token = (a1 != d) ? a1 : __float_as_int(r[1]);
+        break;
+      }
+    }
+    *p.accepted = j;
+    *p.next_a0 = token;
+    *p.ticket = 0u;
+  }
+}
+
 template <int QB, int MODE, int NM>
 __global__ void __launch_bounds__(TcRoles<QB>::kThreads, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_codes,
@@ -304,7 +400,7 @@ __global__ void __launch_bounds__(TcRoles<QB>::kThreads, 1)
   }
   if (!dep_early) griddep_wait();
   // the drafts, for the accept at the end (whichever CTA runs it)
-  if (MODE == kModeHead && warp == 2 && lane < p.n_valid) s_drafts[lane] = p.drafts[lane];
+  if (MODE != kModeY && warp == 2 && lane < p.n_valid) s_drafts[lane] = p.drafts[lane];
 
   tc_fence_before();
   __syncthreads();  // barriers initialised, tensor memory allocated
@@ -427,6 +523,10 @@ __global__ void __launch_bounds__(TcRoles<QB>::kThreads, 1)
     float* const red = reinterpret_cast<float*>(sb + pl.red_off) + q * p.S * 33;  // [S][33]
     float run_v = -FLT_MAX;  // running best of column n = lane
     int run_i = INT_MAX;
+    // sampling verify, column n = lane: top-2 of L/T + g with their entries,
+    // softmax max and sum of L/T, the logit L/T of the row's draft (NaN: not here)
+    float z1 = -INFINITY, z2 = -INFINITY, sm_m = -INFINITY, sm_s = 0.f, l_d = __int_as_float(0x7fc00000);
+    int v1 = INT_MAX, v2 = INT_MAX;
     const int tpe = p.rows_per_expert > 0 ? p.rows_per_expert / kTileRows : 1;
     for (int t = 0; t < ntile; ++t) {
       const int tb = t & 1;
@@ -496,10 +596,101 @@ __global__ void __launch_bounds__(TcRoles<QB>::kThreads, 1)
         }
         __syncwarp();
       }
+      if (MODE == kModeSample) {
+        // Rolled loops over small bodies throughout (the fully unrolled form of
+        // this code measured 25-35 % slower); the epilogue warps share their
+        // schedulers with busy converters, so every instruction here counts.
+        // (1) l = L/T of this thread's row, column n at red[n][lane]
+#pragma unroll
+        for (int n = 0; n < 32; ++n)
+          if (n < p.S) red[n * 33 + lane] = acc[n] * p.inv_temp;
+        __syncwarp();
+        const int row0 = (tile_lo + t) * kTileRows + 32 * q;
+        const int nrow = max(0, min(32, p.N - row0));  // rows of this warp's slab inside the vocabulary
+        // (2) lane n: the slab's max of column n, its sum of exp(l - max) and
+        // the draft's l, in four independent chains
+        if (lane < p.S) {
+          const float* const col = red + lane * 33;
+          float m0 = -INFINITY, m1 = -INFINITY, m2 = -INFINITY, m3 = -INFINITY;
+#pragma unroll 1
+          for (int j = 0; j < nrow - 3; j += 4) {
+            m0 = fmaxf(m0, col[j]);
+            m1 = fmaxf(m1, col[j + 1]);
+            m2 = fmaxf(m2, col[j + 2]);
+            m3 = fmaxf(m3, col[j + 3]);
+          }
+          for (int j = nrow & ~3; j < nrow; ++j) m0 = fmaxf(m0, col[j]);
+          const float M = fmaxf(fmaxf(m0, m1), fmaxf(m2, m3));
+          float e0 = 0.f, e1 = 0.f, e2 = 0.f, e3 = 0.f;
+#pragma unroll 1
+          for (int j = 0; j < nrow - 3; j += 4) {
+            e0 += expf(col[j] - M);
+            e1 += expf(col[j + 1] - M);
+            e2 += expf(col[j + 2] - M);
+            e3 += expf(col[j + 3] - M);
+          }
+          for (int j = nrow & ~3; j < nrow; ++j) e0 += expf(col[j] - M);
+          softmax_merge(sm_m, sm_s, M, (e0 + e1) + (e2 + e3));
+          const int dv = (lane < p.n_valid) ? s_drafts[lane] : -1;
+          if (dv >= row0 && dv < row0 + nrow) l_d = col[dv - row0];
+        }
+        __syncwarp();
+        // (3) z = l + g for this thread's row: entry lrow, column n is element
+        // 32 lrow + n, so one counter output serves columns 2c and 2c + 1
+        if (valid) {
+          const unsigned long long c0 = (unsigned long long)(unsigned)lrow * 16ull;
+#pragma unroll 2
+          for (int c = 0; c < (p.S + 1) / 2; ++c) {
+            const unsigned long long w = counter_pair(p.rng_key, c0 + (unsigned)c);
+            red[(2 * c) * 33 + lane] += gumbel_of(half_uniform((unsigned)w));
+            if (2 * c + 1 < p.S) red[(2 * c + 1) * 33 + lane] += gumbel_of(half_uniform((unsigned)(w >> 32)));
+          }
+        }
+        __syncwarp();
+        // (4) lane n: top 2 of column n's z over the slab, four chains, merged
+        if (lane < p.S) {
+          const float* const col = red + lane * 33;
+          float a1[4], a2[4];
+          int b1[4], b2[4];
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            a1[c] = a2[c] = -INFINITY;
+            b1[c] = b2[c] = INT_MAX;
+          }
+#pragma unroll 1
+          for (int j = 0; j < nrow - 3; j += 4) {
+#pragma unroll
+            for (int c = 0; c < 4; ++c) top2_add(a1[c], b1[c], a2[c], b2[c], col[j + c], row0 + j + c);
+          }
+          for (int j = nrow & ~3; j < nrow; ++j) top2_add(a1[0], b1[0], a2[0], b2[0], col[j], row0 + j);
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            top2_add(z1, v1, z2, v2, a1[c], b1[c]);
+            top2_add(z1, v1, z2, v2, a2[c], b2[c]);
+          }
+        }
+        __syncwarp();
+      }
     }
     if (MODE == kModeHead && lane < p.S) {
       best_v[q * 32 + lane] = run_v;
       best_i[q * 32 + lane] = run_i;
+    }
+    if (MODE == kModeSample) {
+      // the four warps' column states into shared memory, [field][quarter][S],
+      // once every epilogue warp is done with its rows of the reduction buffer
+      named_bar_sync(1, 4 * 32);
+      float* const st = reinterpret_cast<float*>(sb + pl.red_off);
+      if (lane < p.S) {
+        const int o = q * p.S + lane, f = 4 * p.S;
+        st[o] = z1;
+        st[f + o] = __int_as_float(v1);
+        st[2 * f + o] = z2;
+        st[3 * f + o] = __int_as_float(v2);
+        st[4 * f + o] = sm_m;
+        st[5 * f + o] = sm_s;
+        st[6 * f + o] = l_d;
+      }
     }
   } else {
     // ---------------- converters ------------------------------------------------------
@@ -608,7 +799,11 @@ __global__ void __launch_bounds__(TcRoles<QB>::kThreads, 1)
     tmem_dealloc(tmem, kTmemCols);
   }
 
-  if (MODE != kModeHead) return;
+  if (MODE == kModeY) return;
+  if (MODE == kModeSample) {
+    sample_tail(p, sb + pl.red_off, s_drafts, s_flag, warp, lane, R::kWarps);
+    return;
+  }
   if (threadIdx.x < p.S) {
     const int col = threadIdx.x;
     float bv = best_v[col];
@@ -722,6 +917,9 @@ cudaError_t launch_tc_gemm(int qbits, int mode, const CUtensorMap& tm_codes, con
                            const CUtensorMap& tm_codes2, const CUtensorMap& tm_scales2, const GemmArgs& a,
                            int grid, int smem, cudaStream_t st) {
   const TcMaps m{tm_codes, tm_scales, tm_codes2, tm_scales2};
+  if (mode == kModeSample)
+    return qbits == 8 ? tc_launch_nm<8, kModeSample>(m, a, grid, smem, st)
+                      : tc_launch_nm<4, kModeSample>(m, a, grid, smem, st);
   const bool head = mode == kModeHead;
   if (qbits == 8)
     return head ? tc_launch_nm<8, kModeHead>(m, a, grid, smem, st) : tc_launch_nm<8, kModeY>(m, a, grid, smem, st);

@@ -17,13 +17,13 @@ LIB_PATH = os.path.join(_HERE, "libsdv.so")
 
 SDV_OK, SDV_ERR_INVALID_ARG, SDV_ERR_UNSUPPORTED, SDV_ERR_CUDA, SDV_ERR_TIMEOUT, SDV_ERR_WORKSPACE = range(6)
 SDV_Q8, SDV_Q4 = 8, 4
-SDV_OP_QLINEAR, SDV_OP_QLINEAR_SWIGLU, SDV_OP_VERIFY_HEAD, SDV_OP_MOE = 1, 2, 3, 4
+SDV_OP_QLINEAR, SDV_OP_QLINEAR_SWIGLU, SDV_OP_VERIFY_HEAD, SDV_OP_MOE, SDV_OP_VERIFY_SAMPLE = 1, 2, 3, 4, 5
 
 EXPORTED = (
     "sdv_quantize_block32", "sdv_qlinear", "sdv_qlinear_swiglu", "sdv_verify_head",
     "sdv_greedy_accept", "sdv_moe_gather_qmm", "sdv_workspace_bytes", "sdv_workspace_init",
     "sdv_device_status", "sdv_status_string", "sdv_version", "sdv_verify_head_noalloc", "sdv_set_gemm_path",
-    "sdv_moe_route",
+    "sdv_moe_route", "sdv_verify_sample",
 )
 
 
@@ -57,6 +57,8 @@ def load() -> ctypes.CDLL:
         "sdv_qlinear_swiglu": ([qw, qw, vp, i32, vp, vp, sz, vp], i32),
         "sdv_verify_head": ([qw, vp, i32, vp, i32, vp, vp, vp, vp, vp, sz, vp], i32),
         "sdv_verify_head_noalloc": ([qw, vp, i32, vp, i32, vp, vp, vp, vp, vp], i32),
+        "sdv_verify_sample": ([qw, vp, i32, vp, i32, ctypes.c_float, ctypes.c_uint64, ctypes.c_uint64, vp, vp, vp,
+                               vp, vp, sz, vp], i32),
         "sdv_greedy_accept": ([vp, i32, vp, i32, vp, vp, vp], i32),
         "sdv_moe_gather_qmm": ([qw, qw, qw, i32, i32, i32, i32, vp, vp, i32, vp, vp, vp, vp, sz, vp], i32),
         "sdv_moe_route": ([vp, i32, i32, i32, vp, vp, vp, vp, vp, vp, vp], i32),
@@ -182,6 +184,21 @@ def sdv_verify_head(head: QWeight, x: torch.Tensor, S: int, drafts, n_valid: int
     _check("sdv_verify_head", load().sdv_verify_head(
         ctypes.byref(cw), _ptr(x), S, _ptr(drafts), n_valid, _ptr(logits), _ptr(argmax),
         _ptr(accepted), _ptr(next_a0), _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def sdv_verify_sample(head: QWeight, x: torch.Tensor, S: int, drafts, n_valid: int, temperature: float,
+                      seed: int, counter: int, logits, samples: torch.Tensor, accepted: torch.Tensor,
+                      next_token: torch.Tensor, ws: torch.Tensor, stream=None) -> None:
+    _want(x, torch.float16, "x")
+    _want(drafts, torch.int32, "drafts")
+    _want(logits, torch.float32, "logits")
+    for t, nm in ((samples, "samples"), (accepted, "accepted"), (next_token, "next_token")):
+        _want(t, torch.int32, nm)
+    cw = head.c()
+    _check("sdv_verify_sample", load().sdv_verify_sample(
+        ctypes.byref(cw), _ptr(x), S, _ptr(drafts), n_valid, float(temperature), seed % 2**64, counter % 2**64,
+        _ptr(logits), _ptr(samples), _ptr(accepted), _ptr(next_token), _ptr(ws), ws.numel() * ws.element_size(),
+        _stream(stream)))
 
 
 def sdv_verify_head_noalloc(head: QWeight, x: torch.Tensor, S: int, drafts, n_valid: int, logits,

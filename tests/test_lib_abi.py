@@ -93,6 +93,25 @@ def test_host_validation_rejects_bad_arguments(lib):
     assert lib.sdv_workspace_init(None, 1024, None) == sdv.SDV_ERR_WORKSPACE
 
 
+def test_sampling_verify_validation(lib):
+    from speculative_decode_verify_sdv_gb300 import sdv
+    p16 = ctypes.c_void_p(16)
+    qw = _qw(lib)
+
+    def call(S=9, n_valid=8, T=1.0, drafts=p16, x=p16, ws_bytes=1 << 20):
+        return lib.sdv_verify_sample(ctypes.byref(qw), x, S, drafts, n_valid, T, 1, 2, None, p16, p16, p16,
+                                     p16, ws_bytes, None)
+    for T in (0.0, -1.0, float("nan"), float("inf")):
+        assert call(T=T) == sdv.SDV_ERR_INVALID_ARG
+    assert call(n_valid=9) == sdv.SDV_ERR_INVALID_ARG
+    assert call(S=0, n_valid=0) == sdv.SDV_ERR_INVALID_ARG
+    assert call(S=33, n_valid=0) == sdv.SDV_ERR_UNSUPPORTED
+    assert call(drafts=None, n_valid=3) == sdv.SDV_ERR_INVALID_ARG
+    assert call(x=ctypes.c_void_p(8)) == sdv.SDV_ERR_INVALID_ARG
+    assert lib.sdv_workspace_bytes(sdv.SDV_OP_VERIFY_SAMPLE, 4096, 256, 9, 0, 0) > 0
+    assert lib.sdv_workspace_bytes(sdv.SDV_OP_VERIFY_SAMPLE, 4096, 256, 33, 0, 0) == 0
+
+
 def test_workspace_bytes_rejects_bad_window(lib):
     assert lib.sdv_workspace_bytes(3, 4096, 256, 0, 0, 0) == 0
     assert lib.sdv_workspace_bytes(3, 4096, 256, 33, 0, 0) == 0
