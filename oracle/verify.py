@@ -110,3 +110,39 @@ def verify_head(x, codes, scales, drafts, n_valid):
     acc, nxt = greedy_accept(am, drafts, n_valid)
     return {"logits": logits, "argmax": am, "accepted": acc, "next_a0": nxt,
             "gap": top2_gap(y64)}
+
+
+def tree_accept(argmax: np.ndarray, tokens: np.ndarray, parent: np.ndarray):
+    """Tree verify accept (the tree variant the pages defer: "Stream C -- ...",
+    section "Deferred / harder", EAGLE-3 tree verify; "Spec-decode on GDN
+    hybrids ...", section "S/K SWEEP").
+
+    The window's S rows are the nodes of a draft tree: node 0 is the root (the
+    row of a0); node i > 0 carries the draft ``tokens[i]`` and hangs below
+    ``parent[i]`` (< i), or is absent (pad) when ``parent[i]`` is not in
+    [0, i).  ``argmax[i]`` is the target's prediction after the path root ->
+    i.  Node i is accepted iff its parent is accepted and
+    ``tokens[i] == argmax[parent[i]]`` (the root always is).  The commit is the
+    path to the deepest accepted node, the lowest index among equally deep
+    ones.  Returns ``(path, next_a0)``: the accepted nodes from the root's
+    child down, and ``argmax`` of the deepest one.  A chain (parent[i] = i-1
+    for the n_valid real drafts) gives ``greedy_accept``.
+    """
+    s = len(argmax)
+    acc = [True] + [False] * (s - 1)
+    depth = [0] * s
+    for i in range(1, s):
+        p = int(parent[i])
+        if 0 <= p < i and acc[p] and int(tokens[i]) == int(argmax[p]):
+            acc[i] = True
+            depth[i] = depth[p] + 1
+    best = 0
+    for i in range(1, s):
+        if acc[i] and depth[i] > depth[best]:
+            best = i
+    path = []
+    i = best
+    while i != 0:
+        path.append(i)
+        i = int(parent[i])
+    return path[::-1], int(argmax[best])
