@@ -658,6 +658,51 @@ def run_spec_loop(args, wl, S):
     return 0 if line["lossless"] else 1
 
 
+def run_sweep(args, wl):
+    """Verify-head time per window against the window size S (1..32): the GB300
+    analogue of the pages' c_v(S) = t(S) / t(1).  One JSON line."""
+    import torch
+    from speculative_decode_verify_sdv_gb300 import build, sdv
+    if wl.kind != "head":
+        raise SystemExit("--sweep-S needs a head workload (tiny, q4b, a3b)")
+    build.build()
+    sdv.load()
+    dev = "cuda:0"
+    torch.cuda.set_device(0)
+    w = torch.from_numpy(W.head_weights(wl)).to(dev)
+    head = sdv.quantize(w, wl.bits)
+    del w
+    torch.cuda.synchronize()
+    points = []
+    for S in [int(v) for v in args.sweep_S.split(",")]:
+        x = torch.from_numpy(W.activations(wl, 0, S).view(np.int16)).to(dev).view(torch.float16)
+        dr = torch.zeros(max(S - 1, 1), dtype=torch.int32, device=dev)
+        am = torch.empty(S, dtype=torch.int32, device=dev)
+        acc = torch.empty(1, dtype=torch.int32, device=dev)
+        nxt = torch.empty(1, dtype=torch.int32, device=dev)
+        ws = sdv.workspace(sdv.SDV_OP_VERIFY_HEAD, wl.n, wl.h, S, device=dev)
+        for _ in range(3):
+            sdv.sdv_verify_head(head, x, S, dr, 0, None, am, acc, nxt, ws)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(args.steps):
+            sdv.sdv_verify_head(head, x, S, dr, 0, None, am, acc, nxt, ws)
+        e1.record()
+        torch.cuda.synchronize()
+        points.append({"S": S, "us": e0.elapsed_time(e1) * 1000.0 / args.steps})
+    t1 = next((p["us"] for p in points if p["S"] == 1), points[0]["us"])
+    for p in points:
+        p["c_v"] = p["us"] / t1
+        p["weight_gbs"] = head_bytes(wl, p["S"]) / (p["us"] * 1e-6) / 1e9
+    line = {"metric": "verify-head us per window against S; c_v(S) = t(S) / t(1)", "unit": "us",
+            "config": {"workload": f"{wl.name}: verify head {wl.n}x{wl.h} int{wl.bits}", "steps": args.steps,
+                       "timing": "events around the back-to-back launches, / steps"},
+            "points": points}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -672,6 +717,7 @@ def main(argv=None):
                     help="GEMM implementation (auto: tcgen05 where its plan fits)")
     ap.add_argument("--verify", choices=["greedy", "sample"], default="greedy",
                     help="head workloads: greedy verify (sdv_verify_head) or sampling verify at T = 1")
+    ap.add_argument("--sweep-S", default="", help="comma-separated window sizes: verify-head time per S")
     ap.add_argument("--spec-loop", action="store_true",
                     help="end-to-end n-gram speculative decoding on the head workload instead of the kernel bench")
     ap.add_argument("--gen", type=int, default=512, help="--spec-loop: tokens to generate")
@@ -684,6 +730,8 @@ def main(argv=None):
     S = args.S or wl.s_default
     if args.spec_loop:
         return run_spec_loop(args, wl, S)
+    if args.sweep_S:
+        return run_sweep(args, wl)
     world, rank, local = dist_setup()
     if args.impl == "reference":
         return run_reference(args, wl, S, world, rank)

@@ -146,7 +146,10 @@ SDV_API sdv_status sdv_qlinear_swiglu(const sdv_qweight* gate, const sdv_qweight
  * argmax: int32 [S];  accepted, next_a0: int32 [1] each.
  * One kernel launch: a persistent dequant GEMM whose epilogue reduces each
  * CTA's vocabulary slab to per-row (max, index) partials in `ws`; the last CTA
- * to finish reduces the partials and runs the accept.
+ * to finish reduces the partials and runs the accept.  When the window rows of
+ * a long reduction do not fit one tensor-core launch's shared memory (e.g.
+ * k = 2560 at S >= 17), the rows are verified in two (or more) chunks, each
+ * streaming the head once, and a single-warp launch runs the accept.
  */
 SDV_API sdv_status sdv_verify_head(const sdv_qweight* head, const uint16_t* x, int32_t S,
                            const int32_t* drafts, int32_t n_valid, float* logits_or_null,
@@ -210,6 +213,28 @@ SDV_API sdv_status sdv_verify_head_noalloc(const sdv_qweight* head, const uint16
                                    const int32_t* drafts, int32_t n_valid,
                                    float* logits_or_null, int32_t* argmax, int32_t* accepted,
                                    int32_t* next_a0, sdv_stream_t stream);
+
+/*
+ * Tree accept over the S rows of a tree-shaped window (the tree variant of the
+ * verify that "Stream C -- Speculative decoding: feasibility verdict +
+ * implementation plan" defers, section "Deferred / harder"): node 0 is the root
+ * (the row of a0); node i > 0 carries the draft tokens[i] and hangs below
+ * parent[i], which must lie in [0, i) -- any other value marks an absent (pad)
+ * node, never accepted.  argmax[i] (device int32 [S], e.g. from
+ * sdv_verify_head over the node rows) is the target's prediction after the path
+ * root -> i.  Node i is accepted iff its parent is and tokens[i] ==
+ * argmax[parent[i]].  The commit is the path to the deepest accepted node (the
+ * lowest index among equally deep ones):
+ *   accepted = its depth (accepted drafts), path[0 .. accepted-1] = the node
+ *   indices from the root's child down (entries past it untouched),
+ *   next_a0 = argmax[that node].
+ * A chain (parent[i] = i-1 for the real drafts, -1 for pads) gives the greedy
+ * accept.  tokens, parent: device int32 [S] (entry 0 ignored); path: device
+ * int32 [S-1]; they may be NULL when S == 1.  One single-warp launch.
+ */
+SDV_API sdv_status sdv_tree_accept(const int32_t* argmax, int32_t S, const int32_t* tokens,
+                           const int32_t* parent, int32_t* path, int32_t* accepted,
+                           int32_t* next_a0, sdv_stream_t stream);
 
 /*
  * The greedy accept rule alone, on a given argmax[S] (device, int32), with the

@@ -548,6 +548,7 @@ sdv_status sdv_verify_head(const sdv_qweight* head, const uint16_t* x, int32_t S
   if (n_valid > 0 && drafts == nullptr) return SDV_ERR_INVALID_ARG;
   const size_t need = sdv_workspace_bytes(SDV_OP_VERIFY_HEAD, head->n, head->k, S, 0, 0);
   if (ws == nullptr || !aligned16(ws) || ws_bytes < need) return SDV_ERR_WORKSPACE;
+  const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   GemmArgs a{};
   a.y = logits_or_null;
   a.drafts = drafts;
@@ -555,7 +556,47 @@ sdv_status sdv_verify_head(const sdv_qweight* head, const uint16_t* x, int32_t S
   a.argmax = argmax;
   a.accepted = accepted;
   a.next_a0 = next_a0;
-  return run_gemm(head, x, S, sdv::kModeHead, a, ws, ws_bytes, nullptr, reinterpret_cast<cudaStream_t>(stream));
+  // The window rows of a long reduction may not fit one tcgen05 launch's shared
+  // memory next to its ring.  Two row chunks on the tcgen05 path (each streams
+  // the head once) then beat one launch of the mma.sync path, which streams at
+  // well under half the rate (q4b head, S = 17: 145 us against 209 us).
+  const int path = g_gemm_path.load();
+  int chunk = 0;
+  if (path != 1 && S > 1 && plan_tc(head->qtype, head->n, head->k, S, false).splits == 0 &&
+      plan_tc(head->qtype, head->n, head->k, (S + 1) / 2, false).splits != 0)
+    chunk = (S + 1) / 2;
+  if (chunk == 0) {
+    const sdv_status s = run_gemm(head, x, S, sdv::kModeHead, a, ws, ws_bytes, nullptr, st);
+    if (s != SDV_ERR_UNSUPPORTED || S == 1) return s;
+    // neither path fits the whole window: the largest halving that does
+    chunk = S / 2;
+    while (chunk > 1 && choose_plan(head->qtype, head->n, head->k, chunk, false).splits == 0) chunk /= 2;
+    if (choose_plan(head->qtype, head->n, head->k, chunk, false).splits == 0) return SDV_ERR_UNSUPPORTED;
+  }
+  // verify the rows in chunks, then run the accept over the whole argmax
+  for (int r0 = 0; r0 < S; r0 += chunk) {
+    const int rows = S - r0 < chunk ? S - r0 : chunk;
+    GemmArgs b{};
+    b.y = logits_or_null != nullptr ? logits_or_null + (size_t)r0 * head->n : nullptr;
+    b.drafts = nullptr;
+    b.n_valid = 0;
+    b.argmax = argmax + r0;
+    b.accepted = accepted;  // overwritten by the accept below
+    b.next_a0 = next_a0;
+    const sdv_status c = run_gemm(head, x + (size_t)r0 * head->k, rows, sdv::kModeHead, b, ws, ws_bytes, nullptr, st);
+    if (c != SDV_OK) return c;
+  }
+  return cuda_status(sdv::launch_greedy_accept(argmax, S, drafts, n_valid, accepted, next_a0, st));
+}
+
+sdv_status sdv_tree_accept(const int32_t* argmax, int32_t S, const int32_t* tokens, const int32_t* parent,
+                           int32_t* path, int32_t* accepted, int32_t* next_a0, sdv_stream_t stream) {
+  if (argmax == nullptr || accepted == nullptr || next_a0 == nullptr) return SDV_ERR_INVALID_ARG;
+  if (S < 1) return SDV_ERR_INVALID_ARG;
+  if (S > kMaxS) return SDV_ERR_UNSUPPORTED;
+  if (S > 1 && (tokens == nullptr || parent == nullptr || path == nullptr)) return SDV_ERR_INVALID_ARG;
+  return cuda_status(sdv::launch_tree_accept(argmax, S, tokens, parent, path, accepted, next_a0,
+                                             reinterpret_cast<cudaStream_t>(stream)));
 }
 
 sdv_status sdv_greedy_accept(const int32_t* argmax, int32_t S, const int32_t* drafts, int32_t n_valid,

@@ -115,6 +115,8 @@ cudaError_t launch_moe_route(const float* logits, int S, int E, int top_k, int32
 
 cudaError_t launch_quantize(const float* w, int n, int k, int qbits, void* codes, uint16_t* scales,
                             cudaStream_t st);
+cudaError_t launch_tree_accept(const int32_t* argmax, int S, const int32_t* tokens, const int32_t* parent,
+                               int32_t* path, int32_t* accepted, int32_t* next_a0, cudaStream_t st);
 cudaError_t launch_greedy_accept(const int32_t* argmax, int S, const int32_t* drafts, int n_valid,
                                  int32_t* accepted, int32_t* next_a0, cudaStream_t st);
 

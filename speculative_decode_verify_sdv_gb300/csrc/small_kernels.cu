@@ -58,7 +58,64 @@ __global__ void greedy_accept_kernel(const int32_t* __restrict__ argmax, const i
   *next_a0 = argmax[j];
 }
 
+// Tree accept over S <= 32 nodes, one warp: lane i walks up from node i and
+// finds whether every edge (p -> c) on the way has tokens[c] == argmax[p]; the
+// deepest accepted node (lowest index among equals) wins; lane 0 writes its
+// path from the root's child down and argmax of that node.  A parent index
+// outside [0, i) marks an absent (pad) node.
+__global__ void tree_accept_kernel(const int32_t* __restrict__ argmax, int S, const int32_t* __restrict__ tokens,
+                                   const int32_t* __restrict__ parent, int32_t* path, int32_t* accepted,
+                                   int32_t* next_a0) {
+  __shared__ int s_am[32], s_tok[32], s_par[32];
+  const int lane = threadIdx.x;
+  if (lane < S) {
+    s_am[lane] = argmax[lane];
+    s_tok[lane] = lane > 0 ? tokens[lane] : 0;
+    s_par[lane] = lane > 0 ? parent[lane] : -1;
+  }
+  __syncwarp();
+  int depth = -1;  // -1: not accepted
+  if (lane == 0) {
+    depth = 0;
+  } else if (lane < S) {
+    int j = lane, d = 0;
+    bool ok = true;
+    while (j != 0) {  // at most 31 steps: every step moves to a smaller index
+      const int p = s_par[j];
+      if (p < 0 || p >= j || s_tok[j] != s_am[p]) {
+        ok = false;
+        break;
+      }
+      j = p;
+      ++d;
+    }
+    if (ok) depth = d;
+  }
+  // deepest, then lowest index
+  int best_d = depth, best_i = lane;
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    const int od = __shfl_xor_sync(0xffffffffu, best_d, off);
+    const int oi = __shfl_xor_sync(0xffffffffu, best_i, off);
+    if (od > best_d || (od == best_d && oi < best_i)) {
+      best_d = od;
+      best_i = oi;
+    }
+  }
+  if (lane == 0) {
+    for (int j = best_i, k = best_d - 1; j != 0; j = s_par[j], --k) path[k] = j;
+    *accepted = best_d;
+    *next_a0 = s_am[best_i];
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_tree_accept(const int32_t* argmax, int S, const int32_t* tokens, const int32_t* parent,
+                               int32_t* path, int32_t* accepted, int32_t* next_a0, cudaStream_t st) {
+  tree_accept_kernel<<<1, 32, 0, st>>>(argmax, S, tokens, parent, path, accepted, next_a0);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_quantize(const float* w, int n, int k, int qbits, void* codes, uint16_t* scales,
                             cudaStream_t st) {

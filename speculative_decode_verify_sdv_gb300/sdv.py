@@ -23,7 +23,7 @@ EXPORTED = (
     "sdv_quantize_block32", "sdv_qlinear", "sdv_qlinear_swiglu", "sdv_verify_head",
     "sdv_greedy_accept", "sdv_moe_gather_qmm", "sdv_workspace_bytes", "sdv_workspace_init",
     "sdv_device_status", "sdv_status_string", "sdv_version", "sdv_verify_head_noalloc", "sdv_set_gemm_path",
-    "sdv_moe_route", "sdv_verify_sample",
+    "sdv_moe_route", "sdv_verify_sample", "sdv_tree_accept",
 )
 
 
@@ -60,6 +60,7 @@ def load() -> ctypes.CDLL:
         "sdv_verify_sample": ([qw, vp, i32, vp, i32, ctypes.c_float, ctypes.c_uint64, ctypes.c_uint64, vp, vp, vp,
                                vp, vp, sz, vp], i32),
         "sdv_greedy_accept": ([vp, i32, vp, i32, vp, vp, vp], i32),
+        "sdv_tree_accept": ([vp, i32, vp, vp, vp, vp, vp, vp], i32),
         "sdv_moe_gather_qmm": ([qw, qw, qw, i32, i32, i32, i32, vp, vp, i32, vp, vp, vp, vp, sz, vp], i32),
         "sdv_moe_route": ([vp, i32, i32, i32, vp, vp, vp, vp, vp, vp, vp], i32),
         "sdv_workspace_bytes": ([i32, i32, i32, i32, i32, i32], sz),
@@ -214,6 +215,15 @@ def sdv_verify_head_noalloc(head: QWeight, x: torch.Tensor, S: int, drafts, n_va
     _check("sdv_verify_head_noalloc", load().sdv_verify_head_noalloc(
         ctypes.byref(cw), _ptr(x), S, _ptr(drafts), n_valid, _ptr(logits), _ptr(argmax),
         _ptr(accepted), _ptr(next_a0), _stream(stream)))
+
+
+def sdv_tree_accept(argmax: torch.Tensor, S: int, tokens, parent, path, accepted: torch.Tensor,
+                    next_a0: torch.Tensor, stream=None) -> None:
+    for t, nm in ((argmax, "argmax"), (tokens, "tokens"), (parent, "parent"), (path, "path"),
+                  (accepted, "accepted"), (next_a0, "next_a0")):
+        _want(t, torch.int32, nm)
+    _check("sdv_tree_accept", load().sdv_tree_accept(
+        _ptr(argmax), S, _ptr(tokens), _ptr(parent), _ptr(path), _ptr(accepted), _ptr(next_a0), _stream(stream)))
 
 
 def sdv_greedy_accept(argmax: torch.Tensor, S: int, drafts, n_valid: int, accepted: torch.Tensor,

@@ -120,6 +120,16 @@ def test_int4_long_reduction_wide_windows(sdv, path, S):
     _window(sdv, head, codes, scales, _x(S, k, 70 + S), 70 + S, k)
 
 
+@pytest.mark.parametrize("S", [17, 25, 32])
+def test_int8_long_reduction_wide_windows(sdv, path, S):
+    """int8 at K = 2560 (the q4b head's reduction): the widest windows exceed
+    one launch's shared memory on either path and are verified in row chunks."""
+    n, k = 3000, 2560
+    codes, scales, stored = _synthetic_head(n, k, 8, 11)
+    head = device_weight(stored, scales, 8, n, k)
+    _window(sdv, head, codes, scales, _x(S, k, 90 + S), 90 + S, k)
+
+
 @pytest.mark.parametrize("bits", [8, 4])
 def test_large_block_scales(sdv, path, bits):
     """Some 32-blocks carry weights ~1e4 times larger (int4 block scales of about
