@@ -218,7 +218,11 @@ def oracle_sample(wl, S: int, budget_s: float):
     if wl.kind == "head":
         rows = 4096
         w = W.head_weights(wl, slice(0, rows))
-        codes, scales = quant.quantize_block32(w, wl.bits)
+        if wl.bits == 2:
+            c4, scales = quant.quantize_fp4_block32(w)
+            codes = quant.decode_e2m1(c4)
+        else:
+            codes, scales = quant.quantize_block32(w, wl.bits)
         total = wl.n
         t0 = time.perf_counter()
         while True:
@@ -272,9 +276,13 @@ def oracle_sample(wl, S: int, budget_s: float):
     return 1.0 / per_window, f"{what} ({t_used:.1f} s), scaled to a full window"
 
 
+def wtype(bits: int) -> str:
+    return "fp4 (E2M1)" if bits == 2 else f"int{bits}"
+
+
 def workload_name(wl, S: int) -> str:
     if wl.kind == "head":
-        return f"{wl.name}: verify head {wl.n}x{wl.h} int{wl.bits} per-block-32, S={S}"
+        return f"{wl.name}: verify head {wl.n}x{wl.h} {wtype(wl.bits)} per-block-32, S={S}"
     if wl.kind == "mlp":
         return (f"{wl.name}: SwiGLU MLP gate/up {wl.inter}x{wl.h}, down {wl.h}x{wl.inter} "
                 f"int{wl.bits} per-block-32, S={S}")
@@ -581,13 +589,13 @@ def run_sdv(args, wl, S, world, rank, local):
     value = world * args.steps / (elapsed_ms / 1000.0)
     peak, kind = measured_peak()
     achieved = nbytes / (kernel_ms / 1000.0) / 1e9
-    prof_key = f"{wl.name} S={S}" + (" sample" if sampling else "")
+    prof_key = f"{wl.name} S={S}" + (" sample" if sampling else "") + (" fp4" if wl.bits == 2 else "")
     traffic, traffic_src = (profiled_traffic(prof_key) if wl.kind == "head" else (None, None))
     cpu_rate, cpu_desc = oracle_sample(wl, S, args.cpu_budget) if args.cpu_budget > 0 else (None, "skipped")
     line = {
         "metric": METRIC, "value": value, "unit": "windows/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": elapsed_ms / args.steps, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "f16 x int%d -> f32" % wl.bits, "data": "synthetic",
+        "scaling": "weak", "vs_baseline": None, "dtype": "f16 x %s -> f32" % wtype(wl.bits), "data": "synthetic",
         "config": {"workload": workload_name(wl, S) + (", sampling verify T=1" if sampling else ""), "S": S,
                    "windows": nwin, "bytes_per_window": nbytes,
                    "l2": "inputs larger than L2 (weight stream %.0f MB > 129 MB)" % (nbytes / 1e6),
@@ -718,6 +726,8 @@ def main(argv=None):
     ap.add_argument("--verify", choices=["greedy", "sample"], default="greedy",
                     help="head workloads: greedy verify (sdv_verify_head) or sampling verify at T = 1")
     ap.add_argument("--sweep-S", default="", help="comma-separated window sizes: verify-head time per S")
+    ap.add_argument("--fp4", action="store_true",
+                    help="head workloads: the same head quantised to FP4 (E2M1) instead of its integer type")
     ap.add_argument("--spec-loop", action="store_true",
                     help="end-to-end n-gram speculative decoding on the head workload instead of the kernel bench")
     ap.add_argument("--gen", type=int, default=512, help="--spec-loop: tokens to generate")
@@ -727,6 +737,11 @@ def main(argv=None):
     if args.warmup < 3:
         args.warmup = 3
     wl = W.BY_NAME[args.config]
+    if args.fp4:
+        if wl.kind != "head":
+            raise SystemExit("--fp4 needs a head workload")
+        import dataclasses
+        wl = dataclasses.replace(wl, bits=2)
     S = args.S or wl.s_default
     if args.spec_loop:
         return run_spec_loop(args, wl, S)

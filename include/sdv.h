@@ -73,7 +73,7 @@ typedef enum {
   SDV_ERR_WORKSPACE = 5    /* workspace null, misaligned or smaller than required */
 } sdv_status;
 
-typedef enum { SDV_Q8 = 8, SDV_Q4 = 4 } sdv_qtype;
+typedef enum { SDV_Q8 = 8, SDV_Q4 = 4, SDV_F4 = 2 } sdv_qtype;
 
 /* Operation ids for sdv_workspace_bytes. */
 typedef enum {
@@ -87,14 +87,23 @@ typedef enum {
 /*
  * A per-block-32 quantised weight W[n, k] (n output rows, reduction length k,
  * k % 32 == 0).  Block b of row r covers W[r, 32b .. 32b+31] and has one fp16
- * scale s[r, b]; the weight is q * s with q in [-127, 127] (Q8) or [-7, 7] (Q4).
+ * scale s[r, b]; the weight is q * s with q in [-127, 127] (Q8) or [-7, 7] (Q4),
+ * or an FP4 value (F4).
  *   Q8: codes = int8  [n][k]    (one two's-complement byte per weight)
  *   Q4: codes = uint8 [n][k/2]  (two's-complement nibbles; byte i of a row holds
  *                                 weight 2i in bits 0-3 and weight 2i+1 in bits 4-7)
+ *   F4: codes = uint8 [n][k/2]  (E2M1 nibbles as in the OCP Microscaling spec:
+ *                                 sign bit 3, magnitude index 0..7 for 0, 0.5, 1,
+ *                                 1.5, 2, 3, 4, 6; nibble order as Q4).  The
+ *                                 pages' "FP4 (E2M1)" 4-bit lever ("Flagship
+ *                                 dramatic-speedup plan", Axis 1, lever 1c).
+ *                                 Computed on the tensor-core path only:
+ *                                 SDV_ERR_UNSUPPORTED where its plan does not fit
+ *                                 and no row chunking applies.
  *   scales = fp16 [n][k/32]
  */
 typedef struct {
-  int32_t qtype;          /* SDV_Q8 or SDV_Q4 */
+  int32_t qtype;          /* SDV_Q8, SDV_Q4 or SDV_F4 */
   int32_t n;              /* output rows, >= 1 */
   int32_t k;              /* reduction length, >= 32, multiple of 32 */
   const void* codes;      /* device, 16-byte aligned */
@@ -105,8 +114,10 @@ typedef struct {
  * Quantise fp32 w[n][k] per block of 32 along k:  s32 = max|w| / Q (IEEE fp32
  * division), s = fp16(s32) rounded to nearest even, q = clamp(rint(w / s), -Q, Q)
  * (IEEE fp32 division, ties to even); s == 0 gives q = 0.  Q = 127 (SDV_Q8) or
- * 7 (SDV_Q4).  Writes `codes` in the sdv_qweight layout of `qtype` and `scales`
- * fp16 [n][k/32].  No workspace.
+ * 7 (SDV_Q4).  SDV_F4: s32 = max|w| / 6 and the code of r = w / s is the nearest
+ * E2M1 magnitude, ties to the even mantissa bit, saturating at 6, with the sign
+ * bit set for r < 0 unless the magnitude is 0.  Writes `codes` in the
+ * sdv_qweight layout of `qtype` and `scales` fp16 [n][k/32].  No workspace.
  */
 SDV_API sdv_status sdv_quantize_block32(const float* w, int32_t n, int32_t k, int32_t qtype,
                                 void* codes, uint16_t* scales, sdv_stream_t stream);

@@ -59,7 +59,7 @@ int device_smem_optin() {
 
 bool valid_weight(const sdv_qweight* w) {
   if (w == nullptr || w->codes == nullptr || w->scales == nullptr) return false;
-  if (w->qtype != SDV_Q8 && w->qtype != SDV_Q4) return false;
+  if (w->qtype != SDV_Q8 && w->qtype != SDV_Q4 && w->qtype != SDV_F4) return false;
   if (w->n < 1 || w->k < 32 || (w->k % 32) != 0) return false;
   if (!aligned16(w->codes) || !aligned16(w->scales)) return false;
   return true;
@@ -211,6 +211,8 @@ GemmPlan plan_tc(int qbits, int n, int k, int S, bool allow_split, int unit = 1)
 
 GemmPlan choose_plan(int qbits, int n, int k, int S, bool allow_split) {
   const int path = g_gemm_path.load();
+  if (qbits == SDV_F4)  // FP4 weights exist on the tcgen05 path only
+    return path == 1 ? GemmPlan{} : plan_tc(qbits, n, k, S, allow_split);
   if (path != 1) {
     const GemmPlan t = plan_tc(qbits, n, k, S, allow_split);
     if (t.splits != 0 || path >= 2) return t;
@@ -493,7 +495,7 @@ sdv_status sdv_quantize_block32(const float* w, int32_t n, int32_t k, int32_t qt
                                 uint16_t* scales, sdv_stream_t stream) {
   if (w == nullptr || codes == nullptr || scales == nullptr) return SDV_ERR_INVALID_ARG;
   if (n < 1 || k < 32 || (k % 32) != 0) return SDV_ERR_INVALID_ARG;
-  if (qtype != SDV_Q8 && qtype != SDV_Q4) return SDV_ERR_INVALID_ARG;
+  if (qtype != SDV_Q8 && qtype != SDV_Q4 && qtype != SDV_F4) return SDV_ERR_INVALID_ARG;
   if ((reinterpret_cast<uintptr_t>(w) & 3u) || (reinterpret_cast<uintptr_t>(scales) & 1u))
     return SDV_ERR_INVALID_ARG;
   return cuda_status(sdv::launch_quantize(w, n, k, qtype, codes, scales,

@@ -193,6 +193,21 @@ __device__ __forceinline__ void softmax_merge(float& m, float& s, float m2, floa
   }
 }
 
+// FP4 (E2M1, OCP Microscaling): 8 codes of w (byte j holds codes 2j in its low,
+// 2j + 1 in its high nibble) to f16x2 pairs (k0, k1), (k2, k3), (k4, k5),
+// (k6, k7) by the hardware conversion; every E2M1 value is exact in fp16.
+__device__ __forceinline__ void e2m1x8_to_h2x4(uint32_t w, uint32_t& p0, uint32_t& p1, uint32_t& p2,
+                                               uint32_t& p3) {
+  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+      "mov.b32 {b0, b1, b2, b3}, %4;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %0, b0;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %2, b2;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
+      : "=r"(p0), "=r"(p1), "=r"(p2), "=r"(p3)
+      : "r"(w));
+}
+
 // D = A * B + C, m16n8k16, fp16 inputs, fp32 accumulate.
 __device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
                                           uint32_t a3, uint32_t b0, uint32_t b1, const float (&c)[4]) {

@@ -15,10 +15,13 @@ namespace {
 // section "Quantization on the GPU delegate": per-block-32 absmax symmetric).
 // s32 = max|w| / Q (IEEE fp32 division), s16 = fp16(s32) round-to-nearest-even,
 // q = clamp(rint(w / s16), -Q, Q) with rint ties-to-even; s16 == 0 gives q = 0.
+// QB = 2: FP4 (E2M1) codes -- Q = 6, r = w / s16 rounded to the nearest E2M1
+// magnitude (0, 0.5, 1, 1.5, 2, 3, 4, 6) with ties to the even mantissa bit,
+// saturating; sign bit 8 for r < 0 unless the magnitude is 0.
 template <int QB>
 __global__ void quantize_block32_kernel(const float* __restrict__ w, long nblocks, int k,
                                         uint8_t* __restrict__ codes, __half* __restrict__ scales) {
-  constexpr float kQ = (QB == 8) ? 127.f : 7.f;
+  constexpr float kQ = (QB == 8) ? 127.f : (QB == 4 ? 7.f : 6.f);
   const int lane = threadIdx.x & 31;
   const long warps = (long)gridDim.x * (blockDim.x >> 5);
   const int kb = k / 32;
@@ -32,8 +35,16 @@ __global__ void quantize_block32_kernel(const float* __restrict__ w, long nblock
     const float sf = __half2float(s16);
     int q = 0;
     if (sf != 0.f) {
-      const float r = rintf(__fdiv_rn(v, sf));
-      q = (int)fminf(fmaxf(r, -kQ), kQ);
+      if (QB == 2) {
+        const float r = __fdiv_rn(v, sf), a = fabsf(r);
+        // magnitude index = thresholds passed; a tie rounds to the even mantissa
+        const int idx = (a > 0.25f) + (a >= 0.75f) + (a > 1.25f) + (a >= 1.75f) + (a > 2.5f) + (a >= 3.5f) +
+                        (a > 5.f);
+        q = idx | ((r < 0.f && idx > 0) ? 8 : 0);
+      } else {
+        const float r = rintf(__fdiv_rn(v, sf));
+        q = (int)fminf(fmaxf(r, -kQ), kQ);
+      }
     }
     if (QB == 8) {
       codes[row * k + blk * 32 + lane] = (uint8_t)(int8_t)q;
@@ -125,6 +136,9 @@ cudaError_t launch_quantize(const float* w, int n, int k, int qbits, void* codes
   if (grid > 65535L * 16) grid = 65535L * 16;
   if (qbits == 8)
     quantize_block32_kernel<8><<<(unsigned)grid, threads, 0, st>>>(
+        w, nblocks, k, static_cast<uint8_t*>(codes), reinterpret_cast<__half*>(scales));
+  else if (qbits == 2)
+    quantize_block32_kernel<2><<<(unsigned)grid, threads, 0, st>>>(
         w, nblocks, k, static_cast<uint8_t*>(codes), reinterpret_cast<__half*>(scales));
   else
     quantize_block32_kernel<4><<<(unsigned)grid, threads, 0, st>>>(

@@ -190,12 +190,15 @@ __device__ __noinline__ void sample_tail(const GemmArgs& p, uint8_t* stb, const 
   }
 }
 
-template <int QB, int MODE, int NM>
-__global__ void __launch_bounds__(TcRoles<QB>::kThreads, 1)
+// QT: the weight type -- 8 int8, 4 int4, 2 FP4 (E2M1); QB below is its code
+// width in bits (8 or 4), which sets the byte layout of a stage.
+template <int QT, int MODE, int NM>
+__global__ void __launch_bounds__(TcRoles<(QT == 8 ? 8 : 4)>::kThreads, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_codes,
                    const __grid_constant__ CUtensorMap tm_scales,
                    const __grid_constant__ CUtensorMap tm_codes2,
                    const __grid_constant__ CUtensorMap tm_scales2, const GemmArgs p) {
+  constexpr int QB = (QT == 8) ? 8 : 4;
   using R = TcRoles<QB>;
   // independent fp32 accumulators per tile (MMA m of a stage -> m % kAcc), two
   // tile buffers, in the tensor-memory columns behind the A buffers
@@ -455,7 +458,9 @@ __global__ void __launch_bounds__(TcRoles<QB>::kThreads, 1)
           const int n = v >> 5, g8 = 32 * ks + (v & 31);
           const uint4 x4 = in[u];
           uint4 o;
-          if (QB == 8) {  // per 4 elements: (k0, k2, k1, k3)
+          if (QT == 2) {  // FP4: the converters' pairs are (k0, k1), (k2, k3), ...: as stored
+            o = x4;
+          } else if (QB == 8) {  // per 4 elements: (k0, k2, k1, k3)
             o.x = __byte_perm(x4.x, x4.y, 0x5410);
             o.y = __byte_perm(x4.x, x4.y, 0x7632);
             o.z = __byte_perm(x4.z, x4.w, 0x5410);
@@ -767,11 +772,16 @@ __global__ void __launch_bounds__(TcRoles<QB>::kThreads, 1)
                                       wreg[2 * blk + 1].w};
 #pragma unroll
               for (int j = 0; j < 8; ++j) i8x4_to_h2x2(wv[j], cols[2 * j], cols[2 * j + 1]);
-            } else {
+            } else if (QT == 4) {
               const uint32_t wv[4] = {wreg[blk].x, wreg[blk].y, wreg[blk].z, wreg[blk].w};
 #pragma unroll
               for (int j = 0; j < 4; ++j)
                 i4x8_to_h2x4(wv[j], cols[4 * j], cols[4 * j + 1], cols[4 * j + 2], cols[4 * j + 3]);
+            } else {  // FP4: the hardware E2M1 -> f16x2 conversion, one byte (two codes) at a time
+              const uint32_t wv[4] = {wreg[blk].x, wreg[blk].y, wreg[blk].z, wreg[blk].w};
+#pragma unroll
+              for (int j = 0; j < 4; ++j)
+                e2m1x8_to_h2x4(wv[j], cols[4 * j], cols[4 * j + 1], cols[4 * j + 2], cols[4 * j + 3]);
             }
 #pragma unroll
             for (int j = 0; j < 16; ++j) cols[j] = h2_as_u32(__hmul2(u32_as_h2(cols[j]), s2));
@@ -872,21 +882,21 @@ struct TcMaps {
   const CUtensorMap &c, &s, &c2, &s2;
 };
 
-template <int QB, int MODE, int NM>
+template <int QT, int MODE, int NM>
 cudaError_t tc_launch_t(const TcMaps& m, const GemmArgs& a, int grid, int smem, cudaStream_t st) {
-  auto k = tc_gemm_kernel<QB, MODE, NM>;
+  auto k = tc_gemm_kernel<QT, MODE, NM>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   // the CTAs may be scheduled while the previous kernel drains; they wait for it
   // in griddep_wait()
-  return launch_pdl(k, dim3(grid, a.splits), dim3(TcRoles<QB>::kThreads), (size_t)smem, st, m.c, m.s, m.c2, m.s2,
-                    a);
+  constexpr int kThreads = TcRoles<(QT == 8 ? 8 : 4)>::kThreads;
+  return launch_pdl(k, dim3(grid, a.splits), dim3(kThreads), (size_t)smem, st, m.c, m.s, m.c2, m.s2, a);
 }
 
-template <int QB, int MODE>
+template <int QT, int MODE>
 cudaError_t tc_launch_nm(const TcMaps& m, const GemmArgs& a, int grid, int smem, cudaStream_t st) {
-  return a.S <= 16 ? tc_launch_t<QB, MODE, 16>(m, a, grid, smem, st)
-                   : tc_launch_t<QB, MODE, 32>(m, a, grid, smem, st);
+  return a.S <= 16 ? tc_launch_t<QT, MODE, 16>(m, a, grid, smem, st)
+                   : tc_launch_t<QT, MODE, 32>(m, a, grid, smem, st);
 }
 
 }  // namespace
@@ -917,13 +927,18 @@ cudaError_t launch_tc_gemm(int qbits, int mode, const CUtensorMap& tm_codes, con
                            const CUtensorMap& tm_codes2, const CUtensorMap& tm_scales2, const GemmArgs& a,
                            int grid, int smem, cudaStream_t st) {
   const TcMaps m{tm_codes, tm_scales, tm_codes2, tm_scales2};
-  if (mode == kModeSample)
-    return qbits == 8 ? tc_launch_nm<8, kModeSample>(m, a, grid, smem, st)
-                      : tc_launch_nm<4, kModeSample>(m, a, grid, smem, st);
+  // qbits: 8 int8, 4 int4, 2 FP4 (E2M1)
+  if (mode == kModeSample) {
+    if (qbits == 8) return tc_launch_nm<8, kModeSample>(m, a, grid, smem, st);
+    if (qbits == 4) return tc_launch_nm<4, kModeSample>(m, a, grid, smem, st);
+    return tc_launch_nm<2, kModeSample>(m, a, grid, smem, st);
+  }
   const bool head = mode == kModeHead;
   if (qbits == 8)
     return head ? tc_launch_nm<8, kModeHead>(m, a, grid, smem, st) : tc_launch_nm<8, kModeY>(m, a, grid, smem, st);
-  return head ? tc_launch_nm<4, kModeHead>(m, a, grid, smem, st) : tc_launch_nm<4, kModeY>(m, a, grid, smem, st);
+  if (qbits == 4)
+    return head ? tc_launch_nm<4, kModeHead>(m, a, grid, smem, st) : tc_launch_nm<4, kModeY>(m, a, grid, smem, st);
+  return head ? tc_launch_nm<2, kModeHead>(m, a, grid, smem, st) : tc_launch_nm<2, kModeY>(m, a, grid, smem, st);
 }
 
 }  // namespace sdv

@@ -16,7 +16,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libsdv.so")
 
 SDV_OK, SDV_ERR_INVALID_ARG, SDV_ERR_UNSUPPORTED, SDV_ERR_CUDA, SDV_ERR_TIMEOUT, SDV_ERR_WORKSPACE = range(6)
-SDV_Q8, SDV_Q4 = 8, 4
+SDV_Q8, SDV_Q4, SDV_F4 = 8, 4, 2
 SDV_OP_QLINEAR, SDV_OP_QLINEAR_SWIGLU, SDV_OP_VERIFY_HEAD, SDV_OP_MOE, SDV_OP_VERIFY_SAMPLE = 1, 2, 3, 4, 5
 
 EXPORTED = (
