@@ -114,3 +114,15 @@ def test_mma_path_rejects_fp4(sdv):
         with pytest.raises(sdv.SdvError) as e:
             run_head(qw, x, np.zeros(S - 1, np.int32), 0)
     assert e.value.status == sdv.SDV_ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("n,k,S", [(384, 512, 9), (200, 512, 17)])
+def test_swiglu(sdv, n, k, S):
+    from tests.test_gpu_mlp_moe import _swiglu_case
+    _swiglu_case(sdv, 2, n, k, S, seed=n + S)
+
+
+@pytest.mark.parametrize("S,E,I,H,top_k", [(5, 8, 256, 512, 2), (17, 32, 256, 512, 8)])
+def test_moe(sdv, S, E, I, H, top_k):
+    from tests.test_gpu_mlp_moe import _moe_case
+    _moe_case(sdv, 2, S, E, I, H, top_k, seed=S * 3 + E)
