@@ -532,6 +532,13 @@ __global__ void __launch_bounds__(TcRoles<(QT == 8 ? 8 : 4)>::kThreads, 1)
     // softmax max and sum of L/T, the logit L/T of the row's draft (NaN: not here)
     float z1 = -INFINITY, z2 = -INFINITY, sm_m = -INFINITY, sm_s = 0.f, l_d = __int_as_float(0x7fc00000);
     int v1 = INT_MAX, v2 = INT_MAX;
+    // sampling scans: L lanes per column (32 over the next power of two >= S), so a
+    // small window spreads each column's 32 rows over many lanes; lane cc * L owns
+    // column cc's running state
+    const int s_pow2 = p.S <= 1 ? 1 : p.S <= 2 ? 2 : p.S <= 4 ? 4 : p.S <= 8 ? 8 : p.S <= 16 ? 16 : 32;
+    const int s_lanes = 32 / s_pow2;
+    const int s_col = lane / s_lanes, s_sub = lane % s_lanes;
+    const bool s_act = s_col < p.S, s_own = s_act && s_sub == 0;
     const int tpe = p.rows_per_expert > 0 ? p.rows_per_expert / kTileRows : 1;
     for (int t = 0; t < ntile; ++t) {
       const int tb = t & 1;
@@ -612,32 +619,23 @@ __global__ void __launch_bounds__(TcRoles<(QT == 8 ? 8 : 4)>::kThreads, 1)
         __syncwarp();
         const int row0 = (tile_lo + t) * kTileRows + 32 * q;
         const int nrow = max(0, min(32, p.N - row0));  // rows of this warp's slab inside the vocabulary
-        // (2) lane n: the slab's max of column n, its sum of exp(l - max) and
-        // the draft's l, in four independent chains
-        if (lane < p.S) {
-          const float* const col = red + lane * 33;
-          float m0 = -INFINITY, m1 = -INFINITY, m2 = -INFINITY, m3 = -INFINITY;
-#pragma unroll 1
-          for (int j = 0; j < nrow - 3; j += 4) {
-            m0 = fmaxf(m0, col[j]);
-            m1 = fmaxf(m1, col[j + 1]);
-            m2 = fmaxf(m2, col[j + 2]);
-            m3 = fmaxf(m3, col[j + 3]);
+        // (2) column s_col over its lanes: the slab's max, its sum of exp(l - max)
+        // (butterflies within the lane group), and the draft's l
+        {
+          const float* const col = red + s_col * 33;
+          float m = -INFINITY;
+          if (s_act)
+            for (int j = s_sub; j < nrow; j += s_lanes) m = fmaxf(m, col[j]);
+          for (int o = s_lanes >> 1; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+          float e = 0.f;
+          if (s_act)
+            for (int j = s_sub; j < nrow; j += s_lanes) e += expf(col[j] - m);
+          for (int o = s_lanes >> 1; o > 0; o >>= 1) e += __shfl_xor_sync(0xffffffffu, e, o);
+          if (s_own) {
+            softmax_merge(sm_m, sm_s, m, e);
+            const int dv = (s_col < p.n_valid) ? s_drafts[s_col] : -1;
+            if (dv >= row0 && dv < row0 + nrow) l_d = col[dv - row0];
           }
-          for (int j = nrow & ~3; j < nrow; ++j) m0 = fmaxf(m0, col[j]);
-          const float M = fmaxf(fmaxf(m0, m1), fmaxf(m2, m3));
-          float e0 = 0.f, e1 = 0.f, e2 = 0.f, e3 = 0.f;
-#pragma unroll 1
-          for (int j = 0; j < nrow - 3; j += 4) {
-            e0 += expf(col[j] - M);
-            e1 += expf(col[j + 1] - M);
-            e2 += expf(col[j + 2] - M);
-            e3 += expf(col[j + 3] - M);
-          }
-          for (int j = nrow & ~3; j < nrow; ++j) e0 += expf(col[j] - M);
-          softmax_merge(sm_m, sm_s, M, (e0 + e1) + (e2 + e3));
-          const int dv = (lane < p.n_valid) ? s_drafts[lane] : -1;
-          if (dv >= row0 && dv < row0 + nrow) l_d = col[dv - row0];
         }
         __syncwarp();
         // (3) z = l + g for this thread's row: entry lrow, column n is element
@@ -652,26 +650,23 @@ __global__ void __launch_bounds__(TcRoles<(QT == 8 ? 8 : 4)>::kThreads, 1)
           }
         }
         __syncwarp();
-        // (4) lane n: top 2 of column n's z over the slab, four chains, merged
-        if (lane < p.S) {
-          const float* const col = red + lane * 33;
-          float a1[4], a2[4];
-          int b1[4], b2[4];
-#pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            a1[c] = a2[c] = -INFINITY;
-            b1[c] = b2[c] = INT_MAX;
+        // (4) column s_col over its lanes: the top 2 of z over the slab, merged
+        // across the lane group by a butterfly
+        {
+          const float* const col = red + s_col * 33;
+          float a1 = -INFINITY, a2 = -INFINITY;
+          int b1 = INT_MAX, b2 = INT_MAX;
+          if (s_act)
+            for (int j = s_sub; j < nrow; j += s_lanes) top2_add(a1, b1, a2, b2, col[j], row0 + j);
+          for (int o = s_lanes >> 1; o > 0; o >>= 1) {
+            const float oz1 = __shfl_xor_sync(0xffffffffu, a1, o), oz2 = __shfl_xor_sync(0xffffffffu, a2, o);
+            const int ob1 = __shfl_xor_sync(0xffffffffu, b1, o), ob2 = __shfl_xor_sync(0xffffffffu, b2, o);
+            top2_add(a1, b1, a2, b2, oz1, ob1);
+            top2_add(a1, b1, a2, b2, oz2, ob2);
           }
-#pragma unroll 1
-          for (int j = 0; j < nrow - 3; j += 4) {
-#pragma unroll
-            for (int c = 0; c < 4; ++c) top2_add(a1[c], b1[c], a2[c], b2[c], col[j + c], row0 + j + c);
-          }
-          for (int j = nrow & ~3; j < nrow; ++j) top2_add(a1[0], b1[0], a2[0], b2[0], col[j], row0 + j);
-#pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            top2_add(z1, v1, z2, v2, a1[c], b1[c]);
-            top2_add(z1, v1, z2, v2, a2[c], b2[c]);
+          if (s_own) {
+            top2_add(z1, v1, z2, v2, a1, b1);
+            top2_add(z1, v1, z2, v2, a2, b2);
           }
         }
         __syncwarp();
@@ -686,8 +681,8 @@ __global__ void __launch_bounds__(TcRoles<(QT == 8 ? 8 : 4)>::kThreads, 1)
       // once every epilogue warp is done with its rows of the reduction buffer
       named_bar_sync(1, 4 * 32);
       float* const st = reinterpret_cast<float*>(sb + pl.red_off);
-      if (lane < p.S) {
-        const int o = q * p.S + lane, f = 4 * p.S;
+      if (s_own) {
+        const int o = q * p.S + s_col, f = 4 * p.S;
         st[o] = z1;
         st[f + o] = __int_as_float(v1);
         st[2 * f + o] = z2;
