@@ -248,6 +248,28 @@ SDV_API sdv_status sdv_tree_accept(const int32_t* argmax, int32_t S, const int32
                            int32_t* next_a0, sdv_stream_t stream);
 
 /*
+ * Host-side n-gram drafter ("Stream C -- Speculative decoding: feasibility
+ * verdict + implementation plan", section "The delta": a pure host hashtable over
+ * the prompt + generated stream, the last m tokens mapping to their most recent
+ * continuation).  All pointers are HOST pointers; nothing touches the GPU.
+ *   sdv_ngram_create(m, &d): a drafter of order m (1 <= m <= 64).
+ *   sdv_ngram_append(d, tokens, count): extend the stream.
+ *   sdv_ngram_propose(d, k, drafts, &count): look up the stream's last m tokens;
+ *     if an earlier occurrence with a continuation exists, copy up to k tokens
+ *     from the latest one's continuation into drafts (int32 [k]) and set count,
+ *     else count = 0.  Proposals are read past the stream's last token, so a
+ *     loop appends its anchor token a0 before asking.
+ *   sdv_ngram_destroy(d): free it (NULL is accepted).
+ * Errors: SDV_ERR_INVALID_ARG for null or out-of-range arguments,
+ * SDV_ERR_UNSUPPORTED when a host allocation fails.  Not thread-safe per drafter.
+ */
+typedef struct sdv_ngram sdv_ngram;
+SDV_API sdv_status sdv_ngram_create(int32_t m, sdv_ngram** out);
+SDV_API sdv_status sdv_ngram_destroy(sdv_ngram* d);
+SDV_API sdv_status sdv_ngram_append(sdv_ngram* d, const int32_t* tokens, int32_t count);
+SDV_API sdv_status sdv_ngram_propose(const sdv_ngram* d, int32_t k, int32_t* drafts, int32_t* count);
+
+/*
  * The greedy accept rule alone, on a given argmax[S] (device, int32), with the
  * same definition and outputs as sdv_verify_head.  No workspace.
  */

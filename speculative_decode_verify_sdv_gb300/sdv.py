@@ -24,6 +24,7 @@ EXPORTED = (
     "sdv_greedy_accept", "sdv_moe_gather_qmm", "sdv_workspace_bytes", "sdv_workspace_init",
     "sdv_device_status", "sdv_status_string", "sdv_version", "sdv_verify_head_noalloc", "sdv_set_gemm_path",
     "sdv_moe_route", "sdv_verify_sample", "sdv_tree_accept",
+    "sdv_ngram_create", "sdv_ngram_destroy", "sdv_ngram_append", "sdv_ngram_propose",
 )
 
 
@@ -69,6 +70,10 @@ def load() -> ctypes.CDLL:
         "sdv_status_string": ([i32], ctypes.c_char_p),
         "sdv_version": ([], i32),
         "sdv_set_gemm_path": ([i32], i32),
+        "sdv_ngram_create": ([i32, ctypes.POINTER(vp)], i32),
+        "sdv_ngram_destroy": ([vp], i32),
+        "sdv_ngram_append": ([vp, vp, i32], i32),
+        "sdv_ngram_propose": ([vp, i32, vp, ctypes.POINTER(i32)], i32),
     }
     for name, (args, res) in sig.items():
         f = getattr(lib, name)
@@ -257,6 +262,32 @@ def sdv_moe_route(router_logits: torch.Tensor, S: int, E: int, top_k: int, ids: 
     _check("sdv_moe_route", load().sdv_moe_route(
         _ptr(router_logits), S, E, top_k, _ptr(ids), _ptr(weights), _ptr(offsets), _ptr(pair_rows),
         _ptr(n_hit), _ptr(hit), _stream(stream)))
+
+
+# ---- host n-gram drafter (host pointers; no GPU involved) -------------------------
+
+def sdv_ngram_create(m: int) -> int:
+    """A native drafter of order m; returns its opaque handle."""
+    h = ctypes.c_void_p()
+    _check("sdv_ngram_create", load().sdv_ngram_create(m, ctypes.byref(h)))
+    return h.value
+
+
+def sdv_ngram_destroy(handle: int) -> None:
+    _check("sdv_ngram_destroy", load().sdv_ngram_destroy(ctypes.c_void_p(handle)))
+
+
+def sdv_ngram_append(handle: int, tokens) -> None:
+    arr = (ctypes.c_int32 * len(tokens))(*[int(t) for t in tokens])
+    _check("sdv_ngram_append", load().sdv_ngram_append(ctypes.c_void_p(handle), arr, len(tokens)))
+
+
+def sdv_ngram_propose(handle: int, k: int) -> list[int]:
+    """Up to k drafts continuing the stream's last m tokens (empty when none)."""
+    buf = (ctypes.c_int32 * max(k, 1))()
+    count = ctypes.c_int32(0)
+    _check("sdv_ngram_propose", load().sdv_ngram_propose(ctypes.c_void_p(handle), k, buf, ctypes.byref(count)))
+    return list(buf[:count.value])
 
 
 # ---- small allocation helpers (torch owns the memory) ---------------------------

@@ -19,8 +19,9 @@ hard-won harness lessons": the drafter proposes past a0, and the window is
 padded to exactly S = K + 1 (pads are never accepted).
 
 Every step of a round's arithmetic -- the head GEMM, the per-row argmax, the
-accept -- runs in libsdv (``sdv_verify_head``); this module keeps host state
-only: the token stream, the drafter's table and pinned staging buffers.
+accept -- runs in libsdv (``sdv_verify_head``), and so does the drafter's table
+(``sdv_ngram_*``, host C++); this module keeps the token stream and pinned
+staging buffers.
 """
 from __future__ import annotations
 
@@ -35,33 +36,31 @@ PAD = 0
 
 
 class NgramDrafter:
-    """Prompt-lookup drafter with an incremental table.
+    """Prompt-lookup drafter with an incremental table, held by libsdv
+    (``sdv_ngram_*``: host C++, no GPU).
 
-    ``table[g]`` = the position right after the latest occurrence of the m-gram
-    ``g`` that has a continuation in the stream, i.e. that ends before the last
-    token.  ``propose(k)`` looks up the stream's last m tokens and returns up to
-    ``k`` tokens from that position on (none when the m-gram is new).
+    The table maps each m-gram to the position right after its latest
+    occurrence that has a continuation in the stream, i.e. that ends before the
+    last token.  ``propose(k)`` looks up the stream's last m tokens and returns
+    up to ``k`` tokens from that position on (none when the m-gram is new).
     """
 
     def __init__(self, m: int):
-        if m < 1:
-            raise ValueError("n-gram order must be >= 1")
         self.m = m
-        self.toks: list[int] = []
-        self.table: dict[tuple, int] = {}
+        self._h = None
+        self._h = sdv.sdv_ngram_create(m)
+
+    def __del__(self):
+        if self._h is not None:
+            sdv.sdv_ngram_destroy(self._h)
+            self._h = None
 
     def append(self, tokens: Sequence[int]) -> None:
-        for t in tokens:
-            p = len(self.toks)  # index of the new token: the m-gram ending at p - 1 now continues
-            self.toks.append(int(t))
-            if p >= self.m:
-                self.table[tuple(self.toks[p - self.m:p])] = p
+        if len(tokens):
+            sdv.sdv_ngram_append(self._h, tokens)
 
     def propose(self, k: int) -> list[int]:
-        if k <= 0 or len(self.toks) <= self.m:
-            return []
-        c = self.table.get(tuple(self.toks[-self.m:]))
-        return [] if c is None else self.toks[c:c + k]
+        return sdv.sdv_ngram_propose(self._h, k) if k > 0 else []
 
 
 def expected_tokens_per_round(alpha: float, k: int) -> float:

@@ -16,3 +16,11 @@ def pytest_configure(config):
 @pytest.fixture(scope="session")
 def golden_dir():
     return os.path.join(ROOT, "tests", "golden")
+
+
+@pytest.fixture(scope="session")
+def libsdv():
+    """libsdv.so built in-tree (nvcc cross-compiles without a GPU) and loaded."""
+    from speculative_decode_verify_sdv_gb300 import build, sdv
+    build.build()
+    return sdv.load()

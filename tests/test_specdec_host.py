@@ -21,6 +21,9 @@ from synth.toy_model import ToyHidden
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "ngram_speedup_table.txt")
 
+# the drafter's table lives in libsdv (host C++): build and load it first
+pytestmark = pytest.mark.usefixtures("libsdv")
+
 
 @pytest.mark.parametrize("m", [1, 2, 3])
 def test_drafter_matches_oracle_search(m):
@@ -44,6 +47,45 @@ def test_drafter_examples():
     d.append([1, 2])
     assert d.propose(2) == [9, 1]             # the LATEST earlier (1, 2) wins
     assert specdec.NgramDrafter(3).propose(5) == []
+
+
+def test_drafter_full_int32_range_and_long_stream():
+    # token ids are opaque 32-bit keys; a long stream with a large n-gram order
+    rng = np.random.default_rng(7)
+    base = [int(t) for t in rng.integers(-2**31, 2**31 - 1, 64)]
+    stream = base * 40 + [int(t) for t in rng.integers(-2**31, 2**31 - 1, 50)] + base[:20]
+    for m in (4, 64):
+        d = specdec.NgramDrafter(m)
+        d.append(stream)
+        for k in (1, 17, 100):
+            assert d.propose(k) == spec_loop.ngram_propose(stream, k, m)
+
+
+def test_drafters_are_independent():
+    a, b = specdec.NgramDrafter(1), specdec.NgramDrafter(1)
+    a.append([5, 6, 5])
+    b.append([5, 7, 5])
+    assert a.propose(3) == [6, 5] and b.propose(3) == [7, 5]
+
+
+def test_drafter_rejects_bad_arguments(libsdv):
+    from speculative_decode_verify_sdv_gb300 import sdv
+    for m in (0, -1, 65):
+        with pytest.raises(sdv.SdvError):
+            specdec.NgramDrafter(m)
+    import ctypes
+    h = sdv.sdv_ngram_create(2)
+    try:
+        cnt = ctypes.c_int32(0)
+        assert libsdv.sdv_ngram_propose(ctypes.c_void_p(h), 3, None, ctypes.byref(cnt)) == sdv.SDV_ERR_INVALID_ARG
+        assert libsdv.sdv_ngram_propose(ctypes.c_void_p(h), -1, None, ctypes.byref(cnt)) == sdv.SDV_ERR_INVALID_ARG
+        assert libsdv.sdv_ngram_append(ctypes.c_void_p(h), None, 2) == sdv.SDV_ERR_INVALID_ARG
+        assert libsdv.sdv_ngram_append(ctypes.c_void_p(h), None, 0) == sdv.SDV_OK
+        assert libsdv.sdv_ngram_append(None, None, 0) == sdv.SDV_ERR_INVALID_ARG
+        assert libsdv.sdv_ngram_create(2, None) == sdv.SDV_ERR_INVALID_ARG
+    finally:
+        sdv.sdv_ngram_destroy(h)
+    assert libsdv.sdv_ngram_destroy(None) == sdv.SDV_OK
 
 
 def test_expected_tokens_match_page_table():
