@@ -318,7 +318,8 @@ SDV_API sdv_status sdv_moe_route(const float* router_logits, int32_t S, int32_t 
  * Workspace bytes an operation needs on the current device.
  * `op` is an sdv_op; n, k are the weight's (for SDV_OP_MOE: n = I, k = H);
  * S the window rows; E, top_k for SDV_OP_MOE (ignored otherwise).
- * Returns 0 for invalid arguments; the operation itself reports them.
+ * Returns 0 for invalid arguments (S outside [1, 32], n < 1, k not a positive
+ * multiple of 32, an unknown op); the operation itself reports them.
  */
 SDV_API size_t sdv_workspace_bytes(int32_t op, int32_t n, int32_t k, int32_t S, int32_t E,
                            int32_t top_k);

@@ -4,6 +4,7 @@
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
+#include <climits>
 #include <cmath>
 #include <cstdint>
 #include <cstring>
@@ -57,10 +58,15 @@ int device_smem_optin() {
   return v;
 }
 
+// Shape of a [n, k] weight the launch plans accept: k a positive multiple of 32
+// and both small enough that tile-count roundings stay inside int32.
+constexpr int32_t kMaxDim = INT32_MAX - 1024;
+bool valid_shape(int32_t n, int32_t k) { return n >= 1 && n <= kMaxDim && k >= 32 && k <= kMaxDim && k % 32 == 0; }
+
 bool valid_weight(const sdv_qweight* w) {
   if (w == nullptr || w->codes == nullptr || w->scales == nullptr) return false;
   if (w->qtype != SDV_Q8 && w->qtype != SDV_Q4 && w->qtype != SDV_F4) return false;
-  if (w->n < 1 || w->k < 32 || (w->k % 32) != 0) return false;
+  if (!valid_shape(w->n, w->k)) return false;
   if (!aligned16(w->codes) || !aligned16(w->scales)) return false;
   return true;
 }
@@ -424,8 +430,9 @@ bool moe_args_ok(const sdv_qweight* gate, const sdv_qweight* up, const sdv_qweig
   if (!valid_weight(gate) || !valid_weight(up) || !valid_weight(down)) return false;
   if (E < 1 || I < 32 || H < 32 || top_k < 1 || top_k > E) return false;
   if (gate->qtype != up->qtype || gate->qtype != down->qtype) return false;
-  if (gate->n != E * I || up->n != E * I || gate->k != H || up->k != H) return false;
-  if (down->n != E * H || down->k != I) return false;
+  const long long ei = (long long)E * I, eh = (long long)E * H;
+  if (gate->n != ei || up->n != ei || gate->k != H || up->k != H) return false;
+  if (down->n != eh || down->k != I) return false;
   return true;
 }
 
@@ -454,6 +461,8 @@ const char* sdv_status_string(sdv_status s) {
 
 size_t sdv_workspace_bytes(int32_t op, int32_t n, int32_t k, int32_t S, int32_t E, int32_t top_k) {
   if (S < 1 || S > kMaxS) return 0;
+  // n, k: the weight's [n, k] (for the MoE op, I and H of one expert)
+  if (!valid_shape(n, k)) return 0;
   switch (op) {
     case SDV_OP_QLINEAR: {  // the larger of the two weight types' plans
       const size_t a = qlinear_ws_bytes(8, n, k, S), b = qlinear_ws_bytes(4, n, k, S);

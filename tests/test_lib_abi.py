@@ -116,3 +116,24 @@ def test_workspace_bytes_rejects_bad_window(lib):
     assert lib.sdv_workspace_bytes(3, 4096, 256, 0, 0, 0) == 0
     assert lib.sdv_workspace_bytes(3, 4096, 256, 33, 0, 0) == 0
     assert lib.sdv_workspace_bytes(99, 4096, 256, 9, 0, 0) == 0
+
+
+@pytest.mark.parametrize("op", [1, 2, 3, 4, 5])
+@pytest.mark.parametrize("n,k", [(0, 256), (-5, 256), (4096, 0), (4096, 48), (4096, -256), (2**31 - 1, 256)])
+def test_workspace_bytes_rejects_bad_shapes(lib, op, n, k):
+    # answered before any device query, so no GPU is needed
+    assert lib.sdv_workspace_bytes(op, n, k, 9, 8, 2) == 0
+
+
+def test_moe_shape_products_do_not_wrap(lib):
+    # E * I = 2**32 + 32768 wraps to 32768 in 32-bit arithmetic: must not match gate/up of 32768 rows
+    from speculative_decode_verify_sdv_gb300 import sdv
+    p16 = ctypes.c_void_p(16)
+    E, I, H = 1024, 2**22 + 32, 256
+    gate, up = _qw(lib, n=32768, k=H), _qw(lib, n=32768, k=H)
+    down = _qw(lib, n=E * H, k=I)
+    st = lib.sdv_moe_gather_qmm(ctypes.byref(gate), ctypes.byref(up), ctypes.byref(down), E, I, H, 8, p16, p16, 9,
+                                p16, None, None, p16, 1 << 20, None)
+    assert st == sdv.SDV_ERR_INVALID_ARG
+    big = _qw(lib, n=2**31 - 1)
+    assert lib.sdv_qlinear(ctypes.byref(big), p16, 4, p16, p16, 1 << 20, None) == sdv.SDV_ERR_INVALID_ARG
