@@ -1,0 +1,111 @@
+"""Host logic of bench.py (CPU only): the algorithmic byte counts behind the
+roofline, the committed DRAM-traffic summaries it reads, the clock-record
+summary and the peak lookup."""
+import dataclasses
+import os
+
+import pytest
+
+import bench
+from synth import workloads as W
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def test_head_bytes_by_hand():
+    # q4b, S = 9: int8 codes 151936 x 2560, fp16 scales 151936 x 80, fp16 x 9 x 2560,
+    # 8 drafts, 9 argmax, accepted + next_a0
+    want = 151936 * 2560 + 151936 * 80 * 2 + 9 * 2560 * 2 + 8 * 4 + 9 * 4 + 8
+    assert bench.head_bytes(W.Q4B, 9) == want == 413312076
+    # int4 and FP4 codes are two per byte
+    assert bench.head_bytes(W.A3B, 1) == 248320 * 1024 + 248320 * 64 * 2 + 2048 * 2 + 4 + 8
+    fp4 = dataclasses.replace(W.A3B, bits=2)
+    assert bench.head_bytes(fp4, 17) == bench.head_bytes(W.A3B, 17)
+
+
+def test_weight_and_layer_bytes():
+    assert bench.weight_bytes(64, 256, 8) == 64 * 256 + 64 * 8 * 2
+    assert bench.weight_bytes(64, 256, 4) == 64 * 128 + 64 * 8 * 2
+    # head bytes = its weight + the window's own I/O
+    S = 17
+    assert bench.head_bytes(W.A3B, S) - bench.weight_bytes(W.A3B.n, W.A3B.h, 4) == S * 2048 * 2 + 16 * 4 + S * 4 + 8
+    wl = W.MLP27
+    three = 2 * bench.weight_bytes(17408, 5120, 8) + bench.weight_bytes(5120, 17408, 8)
+    assert bench.mlp_bytes(wl, 1) == three + 5120 * 2 + 2 * 17408 * 2 + 5120 * 4
+    m = W.MOE
+    assert bench.moe_expert_bytes(m) == 3 * bench.weight_bytes(512, 2048, 4)
+    assert bench.moe_bytes(m, 17, 0) == 17 * 2048 * 2 + 17 * 256 * 4 + 17 * 2048 * 4
+
+
+@pytest.mark.parametrize("key,wl,S", [("q4b S=9", W.Q4B, 9), ("a3b S=17", W.A3B, 17),
+                                      ("q4b S=9 sample", W.Q4B, 9),
+                                      ("a3b S=17 fp4", dataclasses.replace(W.A3B, bits=2), 17)])
+def test_committed_traffic_is_near_the_algorithmic_bytes(key, wl, S):
+    # a committed summary for each head workload; its DRAM bytes per launch sit just
+    # above the algorithmic bytes (no wasted re-reads) and never below the weight stream
+    traffic, src = bench.profiled_traffic(key)
+    if traffic is None:
+        assert src is None or "stale" in src, src
+        pytest.skip(f"no current summary for {key}: {src}")
+    alg = bench.head_bytes(wl, S)
+    assert bench.weight_bytes(wl.n, wl.h, wl.bits) <= traffic <= 1.05 * alg, (key, traffic, alg)
+
+
+def _fake_root(tmp_path, hash_line):
+    csrc = tmp_path / "speculative_decode_verify_sdv_gb300" / "csrc"
+    csrc.mkdir(parents=True)
+    for f in bench.KERNEL_SOURCES:
+        (csrc / f).write_text(f"// {f}\n")
+    prof = tmp_path / "profiles"
+    prof.mkdir()
+    (prof / "a_other.md").write_text("workload: other S=1\ntraffic_bytes_per_launch: 5\n")
+    (prof / "b_head.md").write_text(f"# title\n\n{hash_line}\nworkload: q4b S=9\n"
+                                    "traffic_bytes_per_launch: 123456\n")
+
+
+def test_profiled_traffic_reads_current_summary(tmp_path, monkeypatch):
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    _fake_root(tmp_path, "kernel_source_sha256: PLACEHOLDER")
+    cur = bench.kernel_source_hash()
+    p = tmp_path / "profiles" / "b_head.md"
+    p.write_text(p.read_text().replace("PLACEHOLDER", cur))
+    assert bench.profiled_traffic("q4b S=9") == (123456.0, "profiles/b_head.md")
+    assert bench.profiled_traffic("q4b S=9 sample") == (None, None)
+
+
+def test_profiled_traffic_is_dropped_once_the_kernel_changes(tmp_path, monkeypatch):
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    _fake_root(tmp_path, "kernel_source_sha256: 0000000000000000")
+    traffic, src = bench.profiled_traffic("q4b S=9")
+    assert traffic is None and "stale" in src
+
+
+def test_clock_summary():
+    cs = bench.ClockSampler(0)
+    cs.lines = [
+        "0, 1965, 2070, 900.1, 0x0000000000000000, Not Active, Not Active, Not Active, Not Active",
+        "0, 2010, 2070, 950.0, 0x0000000000000004, Not Active, Not Active, Not Active, Active",
+        "0, 1980, 2070, 930.0, 0x0000000000000000, Not Active, Not Active, Not Active, Not Active",
+        "garbage line",
+        "0, [N/A], 2070, 1.0, 0x0, Not Active, Not Active, Not Active, Not Active",
+    ]
+    s = cs.summary()
+    assert s["sm_mhz"] == 1980.0 and s["sm_max_mhz"] == 2070.0
+    assert s["reasons"] == ["sw_power_cap"] and s["samples"] == 3
+    cs.lines = ["0, 1900, 2070, 1.0, 0x0, Active, Not Active, Not Active, Not Active"]
+    assert cs.summary()["reasons"] == ["hw_slowdown"]
+    cs.lines = []
+    assert cs.summary() == {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+
+
+def test_measured_peak(tmp_path, monkeypatch):
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    assert bench.measured_peak() == (6800.0, "fallback")
+    (tmp_path / "MEASURED_PEAKS.json").write_text('{"hbm_gbs": 6783.1, "bf16_tflops": 2000}')
+    assert bench.measured_peak() == (6783.1, "measured")
+
+
+def test_workload_names():
+    assert bench.workload_name(W.Q4B, 9) == "q4b: verify head 151936x2560 int8 per-block-32, S=9"
+    assert "fp4 (E2M1)" in bench.workload_name(dataclasses.replace(W.A3B, bits=2), 17)
+    assert bench.workload_name(W.MOE, 17).startswith("moe: MoE 256 experts")
