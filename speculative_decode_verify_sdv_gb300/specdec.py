@@ -48,12 +48,17 @@ class NgramDrafter:
     def __init__(self, m: int):
         self.m = m
         self._h = None
+        self._destroy = sdv.sdv_ngram_destroy  # held so that teardown at exit still finds it
         self._h = sdv.sdv_ngram_create(m)
 
-    def __del__(self):
+    def close(self) -> None:
+        """Free the native table (also done when the drafter is collected)."""
         if self._h is not None:
-            sdv.sdv_ngram_destroy(self._h)
-            self._h = None
+            h, self._h = self._h, None
+            self._destroy(h)
+
+    def __del__(self):
+        self.close()
 
     def append(self, tokens: Sequence[int]) -> None:
         if len(tokens):

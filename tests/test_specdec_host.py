@@ -61,6 +61,14 @@ def test_drafter_full_int32_range_and_long_stream():
             assert d.propose(k) == spec_loop.ngram_propose(stream, k, m)
 
 
+def test_drafter_close_is_idempotent():
+    d = specdec.NgramDrafter(2)
+    d.append([1, 2, 1])
+    d.close()
+    d.close()
+    del d
+
+
 def test_drafters_are_independent():
     a, b = specdec.NgramDrafter(1), specdec.NgramDrafter(1)
     a.append([5, 6, 5])
