@@ -276,6 +276,23 @@ def oracle_sample(wl, S: int, budget_s: float):
     return 1.0 / per_window, f"{what} ({t_used:.1f} s), scaled to a full window"
 
 
+def oracle_threads() -> int:
+    """Threads the oracle's numpy BLAS runs on: the BLAS pools' own count where
+    threadpoolctl can read it, else the cores this process may run on."""
+    try:
+        from threadpoolctl import threadpool_info
+        n = max((int(i.get("num_threads", 0)) for i in threadpool_info() if i.get("user_api") == "blas"),
+                default=0)
+        if n > 0:
+            return n
+    except Exception:
+        pass
+    try:
+        return len(os.sched_getaffinity(0))
+    except (AttributeError, OSError):
+        return os.cpu_count() or 1
+
+
 def wtype(bits: int) -> str:
     return "fp4 (E2M1)" if bits == 2 else f"int{bits}"
 
@@ -306,7 +323,7 @@ def run_reference(args, wl, S, world, rank):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000.0 / value, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": workload_name(wl, S), "S": S},
-        "cpu_baseline": {"value": value, "unit": "windows/s", "cores": os.cpu_count(), "kind": "oracle",
+        "cpu_baseline": {"value": value, "unit": "windows/s", "cores": oracle_threads(), "kind": "oracle",
                          "sample": desc},
         "e2e": {"value": value, "unit": "windows/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -605,7 +622,7 @@ def run_sdv(args, wl, S, world, rank, local):
                      "traffic": traffic, "traffic_source": traffic_src, "peak_kind": kind, "kernel": f"{job.kernel} ({args.path} path)",
                      "kernel_ms": kernel_ms, "kernel_ms_serialised": iso_ms,
                      "timing": "events around the K back-to-back launches of the timed region, / K"},
-        "cpu_baseline": {"value": cpu_rate, "unit": "windows/s", "cores": os.cpu_count(), "kind": "oracle",
+        "cpu_baseline": {"value": cpu_rate, "unit": "windows/s", "cores": oracle_threads(), "kind": "oracle",
                          "sample": cpu_desc},
         "e2e": {"value": world * args.steps / (e2e_ms / 1000.0), "unit": "windows/s",
                 "h2d_bytes_per_step": job.h2d, "d2h_bytes_per_step": job.d2h},

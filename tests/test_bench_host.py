@@ -109,3 +109,7 @@ def test_workload_names():
     assert bench.workload_name(W.Q4B, 9) == "q4b: verify head 151936x2560 int8 per-block-32, S=9"
     assert "fp4 (E2M1)" in bench.workload_name(dataclasses.replace(W.A3B, bits=2), 17)
     assert bench.workload_name(W.MOE, 17).startswith("moe: MoE 256 experts")
+
+
+def test_oracle_threads_is_positive():
+    assert bench.oracle_threads() >= 1
