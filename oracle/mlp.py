@@ -1,5 +1,8 @@
 """SwiGLU projections and the top-k gathered-expert MoE (oracle).
 
+TEST INFRASTRUCTURE ONLY: imported by tests/, __graft_entry__.smoke() and the
+CPU legs of bench.py, never by the product path; it shares no code with it.
+
 Pages followed:
 
 * "Flagship dramatic-speedup plan -- the full stackable tuning set",

@@ -1,5 +1,8 @@
 """Per-block-32 absmax symmetric weight quantisation (oracle).
 
+TEST INFRASTRUCTURE ONLY: imported by tests/, __graft_entry__.smoke() and the
+CPU legs of bench.py, never by the product path; it shares no code with it.
+
 Follows "Riding Apple's pipelined GPU engine -- 3.5x over a hand-rolled loop,
 zero custom kernels", section "Quantization on the GPU delegate": the ship
 configuration is *int8 linear per-block-32 (no LUT)*, the int4 class is

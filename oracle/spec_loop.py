@@ -1,5 +1,8 @@
 """Toy greedy speculative-decoding loop (oracle-side test machinery).
 
+TEST INFRASTRUCTURE ONLY: imported by tests/, __graft_entry__.smoke() and the
+CPU legs of bench.py, never by the product path; it shares no code with it.
+
 Follows "Stream C -- Speculative decoding: feasibility verdict +
 implementation plan":
 

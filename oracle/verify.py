@@ -1,5 +1,8 @@
 """Verify forward over a static window of S = K+1 rows (oracle).
 
+TEST INFRASTRUCTURE ONLY: imported by tests/, __graft_entry__.smoke() and the
+CPU legs of bench.py, never by the product path; it shares no code with it.
+
 Pages followed:
 
 * "Spec-decode on GDN hybrids (Qwen3.5/3.6 family) -- static-S verify
