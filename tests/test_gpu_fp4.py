@@ -126,3 +126,32 @@ def test_swiglu(sdv, n, k, S):
 def test_moe(sdv, S, E, I, H, top_k):
     from tests.test_gpu_mlp_moe import _moe_case
     _moe_case(sdv, 2, S, E, I, H, top_k, seed=S * 3 + E)
+
+
+def test_full_size_a3b_fp4_head(sdv):
+    """The 35B-A3B-shaped head (248320 x 2048) with FP4 weights at S = 17, in the
+    launch configuration the bench times: quantised on the GPU (bit-exact against
+    the oracle), logits within the bound, ids where the oracle's gap allows, and
+    the timed form (no logits) returning the same ids."""
+    from synth import workloads as W
+    wl, S = W.A3B, 17
+    w = W.head_weights(wl)
+    c4, scales = quant.quantize_fp4_block32(w)
+    qw = sdv.quantize(to_dev(w), sdv.SDV_F4)
+    del w
+    torch.cuda.synchronize()
+    assert np.array_equal(qw.codes.cpu().numpy(), quant.pack_nibbles(c4))
+    assert np.array_equal(qw.scales.cpu().numpy().view(np.uint16), scales.view(np.uint16))
+    table = quant.decode_e2m1(np.arange(16)).astype(np.float32)  # the 16 E2M1 values, exact
+    vals = table[c4]
+    del c4
+    x = W.activations(wl, 0, S)
+    ref0 = verify.verify_head(x, vals, scales, np.zeros(S - 1, np.int32), 0)
+    drafts, n_valid = W.drafts(wl, 0, S, ref0["argmax"])
+    ref = verify.verify_head(x, vals, scales, drafts, n_valid)
+    logits, am, acc, nxt = run_head(qw, x, drafts, n_valid)
+    assert_gemm_close(logits, ref["logits"], wl.h, "a3b fp4 logits")
+    check_head_outputs(ref, am, acc, nxt)
+    _, am2, acc2, nxt2 = run_head(qw, x, drafts, n_valid, want_logits=False)
+    np.testing.assert_array_equal(am2, am)
+    assert (acc2, nxt2) == (acc, nxt)

@@ -158,3 +158,35 @@ def test_deterministic_per_counter(sdv):
     c = _run(sdv, qw, x, drafts, S - 1, 1.0, 5, 18)
     assert np.array_equal(a[1], b[1]) and a[2:] == b[2:]
     assert not np.array_equal(a[1], c[1])
+
+
+def test_full_size_q4b(sdv):
+    """The Qwen3-4B-shaped head (151936 x 2560 int8) at S = 9, T = 1, in the
+    launch configuration the bench times: logits within the bound, every row's
+    draw and the accept where the oracle's margins allow, and the timed form (no
+    logits) returning the same draws."""
+    from synth import workloads as W
+    wl, S, T = W.Q4B, 9, 1.0
+    w = W.head_weights(wl)
+    codes, scales, stored = oracle_weight(w, 8)
+    del w
+    qw = device_weight(stored, scales, 8, wl.n, wl.h)
+    del stored
+    eligible = 0
+    for win in range(2):
+        x = W.activations(wl, win, S)
+        L = verify.dequant_gemm64(x, codes, scales)
+        seed, counter = 4242 + win, 7 * win
+        # drafts: the oracle's own draws for the first rows, then other tokens
+        pre = sample.verify_sample(L, np.zeros(S - 1, np.int64), 0, T, seed, counter)
+        drafts = pre["samples"][:S - 1].astype(np.int32)
+        drafts[4:] = (drafts[4:] + 1 + win) % wl.n
+        ref = sample.verify_sample(L, drafts, S - 1, T, seed, counter)
+        logits, smp, acc, nxt = _run(sdv, qw, x, drafts, S - 1, T, seed, counter, want_logits=True)
+        rms = float(np.sqrt(np.mean(L ** 2)))
+        assert float(np.max(np.abs(logits - L))) <= tol(wl.h) * rms
+        eligible += _check(ref, logits, smp, acc, nxt, wl.h, T, rms)
+        _, smp2, acc2, nxt2 = _run(sdv, qw, x, drafts, S - 1, T, seed, counter)
+        np.testing.assert_array_equal(smp2, smp)
+        assert (acc2, nxt2) == (acc, nxt)
+    assert eligible >= 1
