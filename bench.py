@@ -97,60 +97,158 @@ def profiled_traffic(workload: str):
     return None, None
 
 
+# NVML (the driver's management library, read-only queries) through ctypes: the
+# SM clock, its maximum, power and the clock-event reasons of one GPU.  Used by
+# the poller process below and for single readings before and after a region.
+NVML_POLLER = r"""
+import ctypes, sys, time
+bus, index, interval = sys.argv[1], int(sys.argv[2]), float(sys.argv[3])
+nv = ctypes.CDLL("libnvidia-ml.so.1")
+if nv.nvmlInit_v2() != 0:
+    sys.exit(3)
+h = ctypes.c_void_p()
+if not bus or nv.nvmlDeviceGetHandleByPciBusId_v2(bus.encode(), ctypes.byref(h)) != 0:
+    if nv.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(index), ctypes.byref(h)) != 0:
+        sys.exit(4)
+clk, mx, pw = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_uint()
+rs = ctypes.c_ulonglong()
+nv.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx))
+try:
+    get_reasons = nv.nvmlDeviceGetCurrentClocksEventReasons
+except AttributeError:
+    get_reasons = nv.nvmlDeviceGetCurrentClocksThrottleReasons
+def reading():
+    clk.value = 0; pw.value = 0; rs.value = 0
+    nv.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(clk))
+    nv.nvmlDeviceGetPowerUsage(h, ctypes.byref(pw))
+    get_reasons(h, ctypes.byref(rs))
+    return "%.6f,%d,%d,%d,%d" % (time.time(), clk.value, mx.value, pw.value, rs.value)
+out = sys.stdout
+out.write("ready," + reading() + "\n"); out.flush()
+while True:
+    out.write(reading() + "\n"); out.flush()
+    time.sleep(interval)
+"""
+
+# clock-event reason bits (NVML) and the names the contract uses
+NVML_REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown"}
+
+
+def nvml_bus_id(device_index: int) -> str:
+    """PCI bus id of a CUDA device in NVML's form (domain:bus:device.function)."""
+    try:
+        import torch
+        p = torch.cuda.get_device_properties(device_index)
+        return "%08X:%02X:%02X.0" % (p.pci_domain_id, p.pci_bus_id, p.pci_device_id)
+    except Exception:
+        return ""
+
+
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons, sampled during the timed region."""
+    """SM clocks and clock-event reasons of the timed GPU: one reading right
+    before the timed region, readings every ``interval`` seconds during it
+    (NVML in a separate process, so the launch loop never waits on it), and one
+    right after.  Falls back to ``nvidia-smi -lms`` when NVML cannot be loaded."""
 
-    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    SMI_Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, index: int):
-        self.index = index
+    def __init__(self, index: int, interval: float = 0.002):
+        self.index, self.interval = index, interval
         self.proc = None
-        self.lines = []
+        self.kind = None
+        self.rows = []      # (sm_mhz, max_mhz, reasons set, phase)
+        self.lock = threading.Lock()
+        self.phase = "before"
 
     def __enter__(self):
+        bus = nvml_bus_id(self.index)
         try:
-            self.proc = subprocess.Popen(
-                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
-                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.proc = subprocess.Popen([sys.executable, "-c", NVML_POLLER, bus, str(self.index), str(self.interval)],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            first = self.proc.stdout.readline()
+            if not first.startswith("ready,"):
+                raise RuntimeError("NVML poller did not start")
+            self.kind = "nvml"
+            self._add_nvml(first[len("ready,"):])
+        except Exception:
+            self._stop()
+            self.kind = "nvidia-smi"
+            try:
+                self.proc = subprocess.Popen(
+                    ["nvidia-smi", f"--id={bus or self.index}", f"--query-gpu={self.SMI_Q}",
+                     "--format=csv,noheader,nounits", "-lms", "100"],
+                    stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            except Exception:
+                self.proc = None
+        if self.proc is not None:
             self.t = threading.Thread(target=self._read, daemon=True)
             self.t.start()
-        except Exception:
-            self.proc = None
+        time.sleep(2 * self.interval)
+        with self.lock:
+            self.phase = "during"
         return self
 
-    def _read(self):
-        for line in self.proc.stdout:
-            self.lines.append(line.strip())
+    def _add_nvml(self, line):
+        f = line.strip().split(",")
+        if len(f) < 5:
+            return
+        try:
+            sm, mx, bits = float(f[1]), float(f[2]), int(f[4])
+        except ValueError:
+            return
+        reasons = {nm for b, nm in NVML_REASONS.items() if bits & b}
+        with self.lock:
+            self.rows.append((sm, mx, reasons, self.phase))
 
-    def __exit__(self, *a):
+    def _add_smi(self, line):
+        f = [x.strip() for x in line.split(",")]
+        if len(f) < 9:
+            return
+        try:
+            sm, mx = float(f[1]), float(f[2])
+        except ValueError:
+            return
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = {nm for nm, v in zip(names, f[5:9]) if v.lower() == "active"}
+        with self.lock:
+            self.rows.append((sm, mx, reasons, self.phase))
+
+    def _read(self):
+        add = self._add_nvml if self.kind == "nvml" else self._add_smi
+        for line in self.proc.stdout:
+            add(line)
+
+    def _stop(self):
         if self.proc is not None:
             self.proc.terminate()
             try:
                 self.proc.wait(timeout=5)
             except Exception:
                 self.proc.kill()
+            self.proc = None
+
+    def __exit__(self, *a):
+        with self.lock:
+            self.phase = "after"
+        time.sleep(2 * self.interval)
+        self._stop()
 
     def summary(self):
-        sm, mx, reasons = [], None, set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in self.lines:
-            f = [x.strip() for x in line.split(",")]
-            if len(f) < 9:
-                continue
-            try:
-                sm.append(float(f[1]))
-                mx = float(f[2])
-            except ValueError:
-                continue
-            for nm, v in zip(names, f[5:9]):
-                if v.lower() == "active":
-                    reasons.add(nm)
-        if not sm:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
-        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": mx, "reasons": sorted(reasons),
-                "samples": len(sm)}
+        with self.lock:
+            rows = list(self.rows)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        during = [r for r in rows if r[3] == "during"]
+        use = during if during else rows
+        reasons = set()
+        for r in rows:
+            reasons |= r[2]
+        return {"sm_mhz": float(np.median([r[0] for r in use])), "sm_max_mhz": rows[-1][1],
+                "reasons": sorted(reasons), "samples": len(rows), "samples_during": len(during),
+                "sampler": self.kind,
+                "sm_mhz_before_after": [rows[0][0], rows[-1][0]]}
 
 
 def dist_setup():
@@ -546,7 +644,7 @@ def run_sdv(args, wl, S, world, rank, local):
     stream = torch.cuda.current_stream()
 
     def status_ok():
-        return all(sdv.sdv_device_status(w) == sdv.SDV_OK for w in job.ws_list)
+        return all(sdv.sdv_last_device_status(w) == sdv.SDV_OK for w in job.ws_list)
 
     for i in range(args.warmup):
         job.step(i)

@@ -82,20 +82,42 @@ def test_profiled_traffic_is_dropped_once_the_kernel_changes(tmp_path, monkeypat
 
 def test_clock_summary():
     cs = bench.ClockSampler(0)
-    cs.lines = [
+    cs.kind = "nvidia-smi"
+    for line in (
         "0, 1965, 2070, 900.1, 0x0000000000000000, Not Active, Not Active, Not Active, Not Active",
         "0, 2010, 2070, 950.0, 0x0000000000000004, Not Active, Not Active, Not Active, Active",
         "0, 1980, 2070, 930.0, 0x0000000000000000, Not Active, Not Active, Not Active, Not Active",
         "garbage line",
         "0, [N/A], 2070, 1.0, 0x0, Not Active, Not Active, Not Active, Not Active",
-    ]
+    ):
+        cs._add_smi(line)
     s = cs.summary()
     assert s["sm_mhz"] == 1980.0 and s["sm_max_mhz"] == 2070.0
     assert s["reasons"] == ["sw_power_cap"] and s["samples"] == 3
-    cs.lines = ["0, 1900, 2070, 1.0, 0x0, Active, Not Active, Not Active, Not Active"]
+    cs = bench.ClockSampler(0)
+    cs._add_smi("0, 1900, 2070, 1.0, 0x0, Active, Not Active, Not Active, Not Active")
     assert cs.summary()["reasons"] == ["hw_slowdown"]
-    cs.lines = []
-    assert cs.summary() == {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+    cs = bench.ClockSampler(0)
+    assert cs.summary()["reasons"] == ["unsampled"]
+
+
+def test_clock_summary_nvml_phases():
+    """NVML readings: the median is taken over the readings during the timed
+    region; the readings before and after are kept, and reason bits map to names."""
+    cs = bench.ClockSampler(0)
+    cs.kind = "nvml"
+    cs._add_nvml("1.0,1200,2070,200000,0")        # before: idle clock
+    cs.phase = "during"
+    for sm in (2070, 2055, 2070):
+        cs._add_nvml(f"1.1,{sm},2070,900000,0")
+    cs._add_nvml("1.2,2040,2070,950000,4")         # sw_power_cap bit
+    cs.phase = "after"
+    cs._add_nvml("1.3,2070,2070,800000,0")
+    s = cs.summary()
+    assert s["sm_mhz"] == 2062.5 and s["samples"] == 6 and s["samples_during"] == 4
+    assert s["reasons"] == ["sw_power_cap"] and s["sm_mhz_before_after"] == [1200.0, 2070.0]
+    cs._add_nvml("1.4,1000,2070,0,72")             # 8 | 64: hw_slowdown, hw_thermal_slowdown
+    assert cs.summary()["reasons"] == ["hw_slowdown", "hw_thermal_slowdown", "sw_power_cap"]
 
 
 def test_measured_peak(tmp_path, monkeypatch):
