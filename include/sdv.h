@@ -69,7 +69,7 @@ typedef enum {
   SDV_ERR_INVALID_ARG = 1, /* null/misaligned pointer, bad size, n_valid out of range */
   SDV_ERR_UNSUPPORTED = 2, /* valid but outside what the kernels handle (e.g. S > 32) */
   SDV_ERR_CUDA = 3,        /* a CUDA runtime error while launching */
-  SDV_ERR_TIMEOUT = 4,     /* a bounded device-side wait gave up (see sdv_device_status) */
+  SDV_ERR_TIMEOUT = 4,     /* a bounded device-side wait gave up (see sdv_last_device_status) */
   SDV_ERR_WORKSPACE = 5    /* workspace null, misaligned or smaller than required */
 } sdv_status;
 
@@ -207,18 +207,27 @@ SDV_API sdv_status sdv_verify_sample(const sdv_qweight* head, const uint16_t* x,
  * which owns all device memory and forbids side allocations, or that runs in a
  * latency-critical loop where cudaMalloc (which may synchronise the device) is
  * not allowed.  The pages have no counterpart of this entry point.
- * Same arguments, outputs and definition as sdv_verify_head minus ws/ws_bytes.
+ * Same arguments, outputs, definition and argument errors as sdv_verify_head
+ * minus ws/ws_bytes; every argument is checked before anything is launched.
  * Its scratch (status word, last-CTA ticket, per-CTA argmax partials) is a
  * fixed 65,792-byte device array inside the library, resident on every GPU that
  * loads the library until the process exits.  Limit: the scratch the call needs
  * (256 + 8 * S * number-of-SMs bytes) must fit, else SDV_ERR_WORKSPACE; on a
- * 152-SM GB300 every S <= 32 fits.  The first call on a device looks up the
- * array's device address (cudaGetSymbolAddress) with that device current, so
- * make that first call before any stream capture.  Each call clears the
- * status word and ticket on `stream` first; every call shares the one array, so
- * calls that overlap on the GPU (other streams, other host threads) race and
- * must be serialised by the caller.  sdv_device_status does not apply.
- * Allocates nothing: no cudaMalloc, cudaFree or allocating library routine.
+ * 152-SM GB300 every S <= 32 fits.
+ * Set-up: the first call in a CUDA context looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current.  Under lazy module loading
+ * (CUDA_MODULE_LOADING=LAZY, the default) that lookup may load this library's
+ * module, and the driver then places the array in device memory; make that
+ * first call at set-up, before any stream capture.  A new context (e.g. after
+ * cudaDeviceReset) is detected by its id and the address looked up again.
+ * Every call shares the one array and it keeps the last call's contents: each
+ * call clears the ticket (which must start at zero) on `stream` first, so calls
+ * that overlap on the GPU (other streams, other host threads) race and must be
+ * serialised by the caller.  The status word is not cleared by a call: a bounded
+ * device wait that gave up stays recorded until sdv_noalloc_device_status reads
+ * it (sdv_last_device_status, which takes a workspace, does not apply).
+ * The library itself allocates nothing here: no cudaMalloc, cudaFree or
+ * allocating library routine.
  */
 SDV_API sdv_status sdv_verify_head_noalloc(const sdv_qweight* head, const uint16_t* x, int32_t S,
                                    const int32_t* drafts, int32_t n_valid,
@@ -329,10 +338,26 @@ SDV_API sdv_status sdv_workspace_init(void* ws, size_t ws_bytes, sdv_stream_t st
 
 /*
  * Synchronise `stream`, then read and clear the device status word a kernel
- * leaves in `ws`: SDV_OK, or SDV_ERR_TIMEOUT if a bounded wait for an
- * asynchronous copy gave up (the outputs of that call are then undefined).
+ * leaves in `ws`: SDV_OK, or SDV_ERR_TIMEOUT if a bounded device-side wait gave
+ * up (the outputs of that call are then undefined; later calls on the same
+ * workspace are unaffected).  Any other flag (the tensor-memory allocation was
+ * not where the kernel expects it) reads as SDV_ERR_CUDA.  The status word
+ * collects the flags of every call since the last read.
+ * (The boundary's "bounded-wait / debug-assert flags" read: "Stream C --
+ * Speculative decoding: feasibility verdict + implementation plan", section
+ * "The delta": only ids and a status cross back to the host.)
  */
+SDV_API sdv_status sdv_last_device_status(void* ws, sdv_stream_t stream);
+
+/* The same as sdv_last_device_status (the name earlier versions exported). */
 SDV_API sdv_status sdv_device_status(void* ws, sdv_stream_t stream);
+
+/*
+ * The status read of sdv_verify_head_noalloc's fixed scratch on the current
+ * device: synchronise `stream`, then read and clear its status word, with the
+ * meaning of sdv_last_device_status.  The pages have no counterpart.
+ */
+SDV_API sdv_status sdv_noalloc_device_status(sdv_stream_t stream);
 
 /*
  * Select the implementation of the weight-streaming GEMM behind sdv_qlinear and

@@ -488,7 +488,7 @@ sdv_status sdv_workspace_init(void* ws, size_t ws_bytes, sdv_stream_t stream) {
   return cuda_status(cudaMemsetAsync(ws, 0, ws_bytes, reinterpret_cast<cudaStream_t>(stream)));
 }
 
-sdv_status sdv_device_status(void* ws, sdv_stream_t stream) {
+sdv_status sdv_last_device_status(void* ws, sdv_stream_t stream) {
   if (ws == nullptr) return SDV_ERR_WORKSPACE;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   if (cudaStreamSynchronize(st) != cudaSuccess) return SDV_ERR_CUDA;
@@ -499,6 +499,8 @@ sdv_status sdv_device_status(void* ws, sdv_stream_t stream) {
   if (cudaMemcpy(ws, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess) return SDV_ERR_CUDA;
   return (word & sdv::kDevErrTimeout) ? SDV_ERR_TIMEOUT : SDV_ERR_CUDA;
 }
+
+sdv_status sdv_device_status(void* ws, sdv_stream_t stream) { return sdv_last_device_status(ws, stream); }
 
 sdv_status sdv_quantize_block32(const float* w, int32_t n, int32_t k, int32_t qtype, void* codes,
                                 uint16_t* scales, sdv_stream_t stream) {

@@ -22,7 +22,7 @@ SDV_OP_QLINEAR, SDV_OP_QLINEAR_SWIGLU, SDV_OP_VERIFY_HEAD, SDV_OP_MOE, SDV_OP_VE
 EXPORTED = (
     "sdv_quantize_block32", "sdv_qlinear", "sdv_qlinear_swiglu", "sdv_verify_head",
     "sdv_greedy_accept", "sdv_moe_gather_qmm", "sdv_workspace_bytes", "sdv_workspace_init",
-    "sdv_device_status", "sdv_status_string", "sdv_version", "sdv_verify_head_noalloc", "sdv_set_gemm_path",
+    "sdv_last_device_status", "sdv_device_status", "sdv_noalloc_device_status", "sdv_status_string", "sdv_version", "sdv_verify_head_noalloc", "sdv_set_gemm_path",
     "sdv_moe_route", "sdv_verify_sample", "sdv_tree_accept",
     "sdv_ngram_create", "sdv_ngram_destroy", "sdv_ngram_append", "sdv_ngram_propose",
 )
@@ -66,7 +66,9 @@ def load() -> ctypes.CDLL:
         "sdv_moe_route": ([vp, i32, i32, i32, vp, vp, vp, vp, vp, vp, vp], i32),
         "sdv_workspace_bytes": ([i32, i32, i32, i32, i32, i32], sz),
         "sdv_workspace_init": ([vp, sz, vp], i32),
+        "sdv_last_device_status": ([vp, vp], i32),
         "sdv_device_status": ([vp, vp], i32),
+        "sdv_noalloc_device_status": ([vp], i32),
         "sdv_status_string": ([i32], ctypes.c_char_p),
         "sdv_version": ([], i32),
         "sdv_set_gemm_path": ([i32], i32),
@@ -146,9 +148,19 @@ def sdv_workspace_init(ws: torch.Tensor, stream=None) -> None:
     _check("sdv_workspace_init", load().sdv_workspace_init(_ptr(ws), ws.numel() * ws.element_size(), _stream(stream)))
 
 
-def sdv_device_status(ws: torch.Tensor, stream=None) -> int:
+def sdv_last_device_status(ws: torch.Tensor, stream=None) -> int:
     """Synchronise and return (and clear) the workspace's device status."""
+    return int(load().sdv_last_device_status(_ptr(ws), _stream(stream)))
+
+
+def sdv_device_status(ws: torch.Tensor, stream=None) -> int:
+    """The same as ``sdv_last_device_status`` (the earlier name)."""
     return int(load().sdv_device_status(_ptr(ws), _stream(stream)))
+
+
+def sdv_noalloc_device_status(stream=None) -> int:
+    """Synchronise and return (and clear) the status of the no-workspace head's fixed scratch."""
+    return int(load().sdv_noalloc_device_status(_stream(stream)))
 
 
 def sdv_quantize_block32(w: torch.Tensor, bits: int, codes: torch.Tensor, scales: torch.Tensor,

@@ -105,6 +105,6 @@ def run_head(head, x: np.ndarray, drafts: np.ndarray, n_valid: int, want_logits=
     if ws is None:
         ws = sdv.workspace(sdv.SDV_OP_VERIFY_HEAD, head.n, head.k, S, device=dev)
     sdv.sdv_verify_head(head, xt, S, dt, n_valid, logits, am, acc, nxt, ws)
-    assert sdv.sdv_device_status(ws) == sdv.SDV_OK
+    assert sdv.sdv_last_device_status(ws) == sdv.SDV_OK
     return (logits.cpu().numpy() if want_logits else None, am.cpu().numpy(), int(acc.item()),
             int(nxt.item()))

@@ -84,6 +84,15 @@ cudaError_t __cudaPopCallConfiguration(dim3* grid, dim3* block, size_t* shmem, v
 int __cudaLaunchKernel() { return 0; }
 int __cudaGetKernel() { return 0; }
 
+CUresult fake_ctx_get_current(CUcontext* c) {
+  *c = reinterpret_cast<CUcontext>(0x1000);
+  return CUDA_SUCCESS;
+}
+CUresult fake_ctx_get_id(CUcontext, unsigned long long* id) {
+  *id = 1;
+  return CUDA_SUCCESS;
+}
+
 // ---- the public runtime calls the library makes ----
 cudaError_t cudaGetDevice(int* d) {
   *d = 0;
@@ -97,6 +106,16 @@ cudaError_t cudaGetDriverEntryPointByVersion(const char* sym, void** fn, unsigne
                                              cudaDriverEntryPointQueryResult* q) {
   if (std::strcmp(sym, "cuTensorMapEncodeTiled") == 0) {
     *fn = reinterpret_cast<void*>(&record_tensor_map);
+    *q = cudaDriverEntryPointSuccess;
+    return cudaSuccess;
+  }
+  if (std::strcmp(sym, "cuCtxGetCurrent") == 0) {  // one fixed context
+    *fn = reinterpret_cast<void*>(&fake_ctx_get_current);
+    *q = cudaDriverEntryPointSuccess;
+    return cudaSuccess;
+  }
+  if (std::strcmp(sym, "cuCtxGetId") == 0) {
+    *fn = reinterpret_cast<void*>(&fake_ctx_get_id);
     *q = cudaDriverEntryPointSuccess;
     return cudaSuccess;
   }

@@ -71,7 +71,7 @@ def test_qlinear(sdv, path, bits, n, k, S):
     y = torch.full((S, n), float("nan"), dtype=torch.float32, device="cuda")
     ws = sdv.workspace(sdv.SDV_OP_QLINEAR, n, k, S)
     sdv.sdv_qlinear(qw, to_dev_f16(x), S, y, ws)
-    assert sdv.sdv_device_status(ws) == sdv.SDV_OK
+    assert sdv.sdv_last_device_status(ws) == sdv.SDV_OK
     assert_gemm_close(y.cpu().numpy(), verify.dequant_gemm(x, codes, scales), k, "Y")
 
 

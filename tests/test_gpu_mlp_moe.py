@@ -58,7 +58,7 @@ def _run_swiglu(sdv, gate, up, x):
     h = torch.full((S, gate.n), float("nan"), dtype=torch.float16, device="cuda")
     ws = sdv.workspace(sdv.SDV_OP_QLINEAR_SWIGLU, gate.n, gate.k, S)
     sdv.sdv_qlinear_swiglu(gate, up, to_dev_f16(x), S, h, ws)
-    assert sdv.sdv_device_status(ws) == sdv.SDV_OK
+    assert sdv.sdv_last_device_status(ws) == sdv.SDV_OK
     return h.cpu().numpy().astype(np.float64)
 
 
@@ -192,7 +192,7 @@ def _run_moe(sdv, T, E, I, H, top_k, x, logits):
     ws = sdv.workspace(sdv.SDV_OP_MOE, I, H, S, E, top_k)
     sdv.sdv_moe_gather_qmm(T["gate"][1], T["up"][1], T["down"][1], E, I, H, top_k, to_dev_f16(x),
                            to_dev(np.ascontiguousarray(logits, np.float32)), S, out, ids, wts, ws)
-    assert sdv.sdv_device_status(ws) == sdv.SDV_OK
+    assert sdv.sdv_last_device_status(ws) == sdv.SDV_OK
     return out.cpu().numpy(), ids.cpu().numpy(), wts.cpu().numpy()
 
 

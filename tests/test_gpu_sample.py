@@ -51,7 +51,7 @@ def _run(sdv, qw, x, drafts, n_valid, T, seed, counter, want_logits=False, ws=No
     if ws is None:
         ws = sdv.workspace(sdv.SDV_OP_VERIFY_SAMPLE, qw.n, qw.k, S, device=dev)
     sdv.sdv_verify_sample(qw, xt, S, dt, n_valid, T, seed, counter, logits, smp, acc, nxt, ws)
-    assert sdv.sdv_device_status(ws) == sdv.SDV_OK
+    assert sdv.sdv_last_device_status(ws) == sdv.SDV_OK
     return (logits.cpu().numpy() if want_logits else None), smp.cpu().numpy(), int(acc.item()), int(nxt.item())
 
 
