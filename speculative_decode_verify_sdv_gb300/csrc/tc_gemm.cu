@@ -51,6 +51,7 @@ constexpr uint32_t kTmemCols = 512;
 constexpr int kABufs = 3;        // A operand stage buffers in tensor memory
 constexpr int kMinDepth = 4;     // ring stages (see tc_plan_valid)
 constexpr int kACols = kABufs * 128;
+constexpr uint64_t kDrainLimitNs = 100000000ull;  // 0.1 s: in-flight work at teardown
 
 // Converter groups: group g takes the stages i with i % G == g.  An int4 stage
 // carries twice the weights per byte of an int8 stage, so it gets a third group.
@@ -87,8 +88,8 @@ __host__ __device__ inline TcPlan tc_plan(int qb, int S, int kc, int depth) {
   p.sc_off = p.ring_off + depth * p.code_stage;
   p.red_off = p.sc_off + depth * p.sc_stage;           // epilogue: [4 warps][S][33] floats
   p.bar_off = rup(p.red_off + 4 * S * 33 * 4, 16);
-  // ring full/empty, A buffers afull/afree, tiles tfull/tfree, row slices xready
-  p.best_off = p.bar_off + (2 * depth + 2 * kABufs + 4 + p.kpad / 256) * 8;
+  // ring full/empty, A buffers afull/afree, tiles tfull/tfree, row slices xready, drain
+  p.best_off = p.bar_off + (2 * depth + 2 * kABufs + 4 + p.kpad / 256 + 1) * 8;
   p.misc_off = p.best_off + 4 * 32 * 8;
   p.total = p.misc_off + 16 + 32 * 4 + 32 * 4;  // flags, argmax [32], drafts [32]
   return p;
@@ -267,6 +268,7 @@ __global__ void __launch_bounds__(TcRoles<(QT == 8 ? 8 : 4)>::kThreads, 1)
   const int tile_hi = unit * (int)((long)(blockIdx.x + 1) * (tiles / unit) / gridDim.x);
   const int ntile = tile_hi - tile_lo;
   if (MODE == kModeY && k_len <= 0) {
+    if (!dep_early) griddep_wait();
     // an empty reduction range still owns its split's partial outputs: zeros
     float* const yo = p.y + (size_t)blockIdx.y * p.S * ldy;
     for (int v = threadIdx.x; v < ntile * kTileRows * p.S; v += blockDim.x) {
@@ -291,6 +293,7 @@ __global__ void __launch_bounds__(TcRoles<(QT == 8 ? 8 : 4)>::kThreads, 1)
   const uint32_t bar_tfull = bar_afree + 8 * kABufs;  // [tile buf]
   const uint32_t bar_tfree = bar_tfull + 2 * 8;  // [tile buf]
   const uint32_t bar_xready = bar_tfree + 2 * 8;  // [row slice]: staged (epilogue warps)
+  const uint32_t bar_drain = bar_xready + 8 * (pl.kpad / 256);  // MMA warp: all its tcgen05 work done
   float* const best_v = reinterpret_cast<float*>(sb + pl.best_off);
   int* const best_i = reinterpret_cast<int*>(sb + pl.best_off + 4 * 32 * 4);
   uint32_t* const s_tmem = reinterpret_cast<uint32_t*>(sb + pl.misc_off);
@@ -390,6 +393,7 @@ __global__ void __launch_bounds__(TcRoles<(QT == 8 ? 8 : 4)>::kThreads, 1)
       mbar_init(bar_tfree + 8 * b, 4);
     }
     for (int j = 0; j < pl.kpad / 256; ++j) mbar_init(bar_xready + 8 * j, 4 * 32);
+    mbar_init(bar_drain, 1);
     *s_dead = 0;
     fence_barrier_init();
   }
@@ -401,10 +405,6 @@ __global__ void __launch_bounds__(TcRoles<(QT == 8 ? 8 : 4)>::kThreads, 1)
     best_v[threadIdx.x] = -FLT_MAX;
     best_i[threadIdx.x] = INT_MAX;
   }
-  if (!dep_early) griddep_wait();
-  // the drafts, for the accept at the end (whichever CTA runs it)
-  if (MODE != kModeY && warp == 2 && lane < p.n_valid) s_drafts[lane] = p.drafts[lane];
-
   tc_fence_before();
   __syncthreads();  // barriers initialised, tensor memory allocated
   tc_fence_after();
@@ -413,10 +413,13 @@ __global__ void __launch_bounds__(TcRoles<(QT == 8 ? 8 : 4)>::kThreads, 1)
   // are warp-uniform expressions of the loop counters (a base loaded from shared
   // memory is not provably uniform and each MMA would pay to make it so).
   constexpr uint32_t tmem = 0u;
-  if (threadIdx.x == 0 && *s_tmem != tmem) atomicOr(p.status, kDevErrTmemBase);
 
   // ---- start the weight stream (the TMA unit carries only weights: each TMA
-  // issue costs ~0.15 us at start-up) ----
+  // issue costs ~0.15 us at start-up).  Only this library's kernels release their
+  // dependents before they complete, and none of them writes weights (the
+  // quantiser runs to completion first), so the first stages are requested before
+  // waiting for the previous grid: their issue cost and memory latency overlap
+  // its tail.  (The MoE mappings need the hit list first and have waited.) ----
   if (threadIdx.x == 0) {
     policy = l2_policy_evict_first();
     tma_prefetch_desc(&tm_codes);
@@ -428,6 +431,12 @@ __global__ void __launch_bounds__(TcRoles<(QT == 8 ? 8 : 4)>::kThreads, 1)
     Cursor c = cursor_at(0);
     for (; c.i < depth && c.i < nstages; advance(c)) issue(c);
   }
+  if (!dep_early) griddep_wait();  // everything below may read what the previous grid wrote
+  if (threadIdx.x == 0 && *s_tmem != tmem) atomicOr(p.status, kDevErrTmemBase);
+  // the drafts, for the accept at the end (whichever CTA runs it) and for the
+  // sampling epilogue: the four epilogue warps meet before any of them reads them
+  if (MODE != kModeY && warp == 2 && lane < p.n_valid) s_drafts[lane] = p.drafts[lane];
+  if (MODE != kModeY && warp >= 2 && warp < R::kConv0) named_bar_sync(2, 4 * 32);
   // ---- window rows, slice by slice in this CTA's rotated order: the epilogue
   // warps (idle until the first tile) load each 16-byte chunk, permute it like
   // the converted codes and store it as K-major core matrices (zeros past S and
@@ -482,9 +491,20 @@ __global__ void __launch_bounds__(TcRoles<(QT == 8 ? 8 : 4)>::kThreads, 1)
   if (warp == 0) {
     // ---------------- TMA producer -------------------------------------------------
     if (lane == 0) {
+      int issued = min(depth, nstages);
       for (Cursor c = cursor_at(depth); c.i < nstages; advance(c)) {
         if (!wait(bar_empty + 8 * c.slot, c.phase ^ 1)) break;
+        // a slot released by a converter that gave up (it did not wait for the
+        // slot's copy) is not refilled: every slot keeps at most one copy in flight
+        if (*s_dead) break;
         issue(c);
+        issued = c.i + 1;
+      }
+      if (*s_dead) {
+        // after a timeout, let this CTA's copies still in flight land (bounded):
+        // the latest copy into each slot is the only one that can be pending
+        for (int j = max(0, issued - depth); j < issued; ++j)
+          mbar_wait_bounded(bar_full + 8 * (j % depth), (j / depth) & 1, kDrainLimitNs);
       }
     }
   } else if (warp == 1) {
@@ -492,7 +512,8 @@ __global__ void __launch_bounds__(TcRoles<(QT == 8 ? 8 : 4)>::kThreads, 1)
     // Per stage: uniform bases, then 16 MMAs at compile-time offsets.
     const uint32_t idesc = idesc_f16_f32(kTileRows, NM);
     const uint64_t bdesc0 = smem_desc_kmajor(x_base, 128u, (uint32_t)pl.kpad * 16u);
-    for (Cursor c = cursor_at(0); c.i < nstages; advance(c)) {
+    Cursor c = cursor_at(0);
+    for (; c.i < nstages; advance(c)) {
       const int t = c.t, ks = c.ks, tb = t & 1;
       const int ab = c.ab;
       if (ks == 0 && t >= 2 && !wait_warp(bar_tfree + 8 * tb, ((t >> 1) - 1) & 1)) break;
@@ -513,13 +534,17 @@ __global__ void __launch_bounds__(TcRoles<(QT == 8 ? 8 : 4)>::kThreads, 1)
       if (ks == kst - 1) tc_commit_elect(bar_tfull + 8 * tb);
     }
     // No asynchronous arrive may outlive the CTA (a late one would land in the
-    // shared memory of the next CTA on this SM): wait for the A-buffer releases of
-    // the last stages, which no converter waits for.  The epilogue waits for every
-    // tile's commit.
-    for (int d = max(0, nstages - kABufs); d < nstages; ++d) {
+    // shared memory of the next CTA on this SM), and no MMA may run into freed
+    // tensor memory: one more commit tracks every MMA and commit this thread
+    // issued, and the warp waits for it -- bounded, and also after a timeout,
+    // when the loop above stopped early (c.i stages issued).
+    for (int d = max(0, c.i - kABufs); d < c.i; ++d) {  // the last A-buffer releases
       const Cursor cd = cursor_at(d);
-      if (!wait_warp(bar_afree + 8 * cd.ab, cd.abphase)) break;
+      mbar_wait_bounded(bar_afree + 8 * cd.ab, cd.abphase, kDrainLimitNs);
     }
+    tc_commit_elect(bar_drain);
+    mbar_wait_bounded(bar_drain, 0, kDrainLimitNs);
+    __syncwarp();
   } else if (warp < R::kConv0) {
     // ---------------- tile epilogue (one warp per tensor-memory lane quarter) --------
     const int q = warp & 3;
