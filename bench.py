@@ -317,8 +317,7 @@ def oracle_sample(wl, S: int, budget_s: float):
         rows = 4096
         w = W.head_weights(wl, slice(0, rows))
         if wl.bits == 2:
-            c4, scales = quant.quantize_fp4_block32(w)
-            codes = quant.decode_e2m1(c4)
+            codes, scales = quant.quantize_fp4_block32(w)  # E2M1 codes, decoded by the oracle's GEMM
         else:
             codes, scales = quant.quantize_block32(w, wl.bits)
         total = wl.n

@@ -2,6 +2,8 @@
 
 TEST INFRASTRUCTURE ONLY: imported by tests/, __graft_entry__.smoke() and the
 CPU legs of bench.py, never by the product path; it shares no code with it.
+The arithmetic is in the plain C++ oracle (``oracle/src/oracle.cpp``); this
+module only marshals arrays.
 
 Pages followed:
 
@@ -20,7 +22,8 @@ Readings where the pages are silent:
   MoE it stays float64.
 * Routing: per row, the k experts with the largest router logits, ties to
   the lower expert id; weights = softmax over the k selected logits
-  (identical to renormalising the full softmax over those k).
+  (identical to renormalising the full softmax over those k), the sum taken
+  over the selection in selection order.
 * Grouping: the (row, expert) pairs ordered by expert, and by row within an
   expert (each row picks an expert at most once, so the order is total).
 * Combine: out[s] = sum over the row's k selections, in selection order, of
@@ -30,27 +33,44 @@ from __future__ import annotations
 
 import numpy as np
 
-from .quant import dequantize
-from .verify import dequant_gemm64
+from . import _native as N
+
+BLOCK = 32
 
 
 def silu(t):
     """SiLU(t) = t / (1 + exp(-t)) in float64."""
-    t = np.asarray(t, dtype=np.float64)
-    with np.errstate(over="ignore"):
-        return t / (1.0 + np.exp(-t))
+    shape = np.shape(t)
+    a = N.as_c(np.reshape(t, -1), np.float64)
+    out = np.empty(a.shape, dtype=np.float64)
+    N.lib().orc_silu(N.ptr(a), a.size, N.ptr(out))
+    return out.reshape(shape) if shape else float(out[0])
+
+
+def _swiglu(x, gate_codes, gate_scales, up_codes, up_scales, want16: bool):
+    kg, gc = N.code_kind(gate_codes)
+    ku, uc = N.code_kind(up_codes)
+    if kg != ku or gc.shape != uc.shape:
+        raise ValueError("gate and up must have the same shape and code type")
+    n, k = gc.shape
+    xb = N.half_bits(x)
+    S = xb.shape[0]
+    h = np.empty((S, n), dtype=np.float64)
+    h16 = np.empty((S, n), dtype=np.uint16) if want16 else None
+    N.check(N.lib().orc_swiglu64(kg, N.ptr(gc), N.ptr(N.half_bits(gate_scales)), N.ptr(uc),
+                                 N.ptr(N.half_bits(up_scales)), n, k, N.ptr(xb), S, N.ptr(h), N.ptr(h16),
+                                 N.threads()), "swiglu64")
+    return h, h16
 
 
 def swiglu64(x, gate_codes, gate_scales, up_codes, up_scales):
     """h = SiLU(x G^T) * (x U^T), float64 ``[S, N]``."""
-    g = dequant_gemm64(x, gate_codes, gate_scales)
-    u = dequant_gemm64(x, up_codes, up_scales)
-    return silu(g) * u
+    return _swiglu(x, gate_codes, gate_scales, up_codes, up_scales, False)[0]
 
 
 def qlinear_swiglu(x, gate_codes, gate_scales, up_codes, up_scales):
-    """The fused gate/up projection's API output: ``swiglu64`` rounded to fp16."""
-    return swiglu64(x, gate_codes, gate_scales, up_codes, up_scales).astype(np.float16)
+    """The fused gate/up projection's API output: ``swiglu64`` rounded once to fp16."""
+    return _swiglu(x, gate_codes, gate_scales, up_codes, up_scales, True)[1].view(np.float16)
 
 
 def route_topk(router_logits, k: int):
@@ -59,18 +79,13 @@ def route_topk(router_logits, k: int):
     Returns ``(ids int32 [S, k], weights float64 [S, k])``; ids are listed in
     selection order (largest logit first).
     """
-    r = np.asarray(router_logits, dtype=np.float32)
+    r = N.as_c(router_logits, np.float32)
     s_rows, e = r.shape
     if not (1 <= k <= e):
         raise ValueError("top_k must lie in [1, E]")
     ids = np.empty((s_rows, k), dtype=np.int32)
     w = np.empty((s_rows, k), dtype=np.float64)
-    for s in range(s_rows):
-        order = sorted(range(e), key=lambda j: (-float(r[s, j]), j))[:k]
-        ids[s] = order
-        l = r[s, order].astype(np.float64)
-        p = np.exp(l - l.max())
-        w[s] = p / p.sum()
+    N.check(N.lib().orc_route_topk(N.ptr(r), s_rows, e, k, N.ptr(ids), N.ptr(w)), "route_topk")
     return ids, w
 
 
@@ -81,24 +96,21 @@ def group_by_expert(ids, n_experts: int):
     expert e's selections are entries ``offsets[e] .. offsets[e+1]-1``, in
     increasing row order.
     """
-    ids = np.asarray(ids)
-    s_rows, k = ids.shape
-    counts = np.zeros(n_experts, dtype=np.int64)
-    for s in range(s_rows):
-        for j in range(k):
-            counts[ids[s, j]] += 1
-    offsets = np.zeros(n_experts + 1, dtype=np.int32)
-    offsets[1:] = np.cumsum(counts)
-    fill = offsets[:-1].astype(np.int64).copy()
+    a = N.as_c(ids, np.int32)
+    s_rows, k = a.shape
+    offsets = np.empty(n_experts + 1, dtype=np.int32)
     rows = np.empty(s_rows * k, dtype=np.int32)
     slots = np.empty(s_rows * k, dtype=np.int32)
-    for s in range(s_rows):
-        for j in range(k):
-            e = ids[s, j]
-            rows[fill[e]] = s
-            slots[fill[e]] = j
-            fill[e] += 1
+    N.check(N.lib().orc_group_by_expert(N.ptr(a), s_rows, k, n_experts, N.ptr(offsets), N.ptr(rows),
+                                        N.ptr(slots)), "group_by_expert")
     return offsets, rows, slots
+
+
+def _stacked(gate, up, down):
+    kinds = [N.code_kind(t[0]) for t in (gate, up, down)]
+    if len({k for k, _ in kinds}) != 1:
+        raise ValueError("gate, up and down must share a code type")
+    return kinds[0][0], [c for _, c in kinds], [N.half_bits(t[1]) for t in (gate, up, down)]
 
 
 def expert_swiglu64(x_rows, e, inter, hidden, gate, up, down):
@@ -108,23 +120,27 @@ def expert_swiglu64(x_rows, e, inter, hidden, gate, up, down):
     gate/up ``[E*I, H]``, down ``[E*H, I]``; expert e owns rows
     ``e*I .. (e+1)*I-1`` of gate/up and ``e*H .. (e+1)*H-1`` of down.
     """
-    gs = slice(e * inter, (e + 1) * inter)
-    ds = slice(e * hidden, (e + 1) * hidden)
-    g = dequant_gemm64(x_rows, gate[0][gs], gate[1][gs])
-    u = dequant_gemm64(x_rows, up[0][gs], up[1][gs])
-    h = silu(g) * u
-    return h @ dequantize(down[0][ds], down[1][ds]).T
+    kind, c, s = _stacked(gate, up, down)
+    xb = N.half_bits(x_rows)
+    R = xb.shape[0]
+    y = np.empty((R, hidden), dtype=np.float64)
+    N.check(N.lib().orc_expert_swiglu64(kind, N.ptr(c[0]), N.ptr(s[0]), N.ptr(c[1]), N.ptr(s[1]), N.ptr(c[2]),
+                                        N.ptr(s[2]), int(e), inter, hidden, N.ptr(xb), R, N.ptr(y), N.threads()),
+            "expert_swiglu64")
+    return y
 
 
 def moe_forward(x, router_logits, gate, up, down, n_experts, inter, hidden, top_k):
     """Gathered-expert SwiGLU MoE over the window: returns
     ``(out float32 [S, H], ids int32 [S, k], weights float64 [S, k])``."""
-    x = np.asarray(x, dtype=np.float16)
-    ids, w = route_topk(router_logits, top_k)
-    s_rows = x.shape[0]
-    out = np.zeros((s_rows, hidden), dtype=np.float64)
-    for s in range(s_rows):
-        for j in range(top_k):
-            y = expert_swiglu64(x[s:s + 1], int(ids[s, j]), inter, hidden, gate, up, down)
-            out[s] += w[s, j] * y[0]
-    return out.astype(np.float32), ids, w
+    kind, c, s = _stacked(gate, up, down)
+    xb = N.half_bits(x)
+    S = xb.shape[0]
+    r = N.as_c(router_logits, np.float32)
+    out = np.empty((S, hidden), dtype=np.float32)
+    ids = np.empty((S, top_k), dtype=np.int32)
+    w = np.empty((S, top_k), dtype=np.float64)
+    N.check(N.lib().orc_moe_forward(kind, N.ptr(c[0]), N.ptr(s[0]), N.ptr(c[1]), N.ptr(s[1]), N.ptr(c[2]),
+                                    N.ptr(s[2]), n_experts, inter, hidden, top_k, N.ptr(xb), N.ptr(r), S, N.ptr(out),
+                                    N.ptr(ids), N.ptr(w), N.threads()), "moe_forward")
+    return out, ids, w

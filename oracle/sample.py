@@ -36,60 +36,50 @@ published by Vigna) keyed by (seed, counter):
     acceptance uniform, row i:   e = 32 * V + i
 
 -log(u) is taken as -log1p(-(1 - u)) (1 - u is exact), which keeps the large-g
-tail (u near 1) accurate.  Everything here is fp64.
+tail (u near 1) accurate.  Everything here is fp64.  The arithmetic is in the
+plain C++ oracle (``oracle/src/oracle.cpp``); this module only marshals arrays.
 """
 from __future__ import annotations
 
 import numpy as np
 
+from . import _native as N
+
 G = np.uint64(0x9E3779B97F4A7C15)
-_M1 = np.uint64(0xBF58476D1CE4E5B9)
-_M2 = np.uint64(0x94D049BB133111EB)
 MAX_ROWS = 32
 
 
 def mix(z):
     """SplitMix64 finaliser on uint64 (array or scalar), mod 2**64."""
-    z = np.asarray(z, dtype=np.uint64).copy()
-    with np.errstate(over="ignore"):
-        z ^= z >> np.uint64(30)
-        z *= _M1
-        z ^= z >> np.uint64(27)
-        z *= _M2
-        z ^= z >> np.uint64(31)
-    return z
+    a = np.asarray(z, dtype=np.uint64)
+    c = np.ascontiguousarray(a.reshape(-1))
+    out = np.empty(c.shape, dtype=np.uint64)
+    N.lib().orc_mix_array(N.ptr(c), c.size, N.ptr(out))
+    return out.reshape(a.shape)
 
 
 def rng_key(seed: int, counter: int) -> np.uint64:
-    with np.errstate(over="ignore"):
-        return mix(np.uint64(seed % 2**64) + (np.uint64(counter % 2**64) + np.uint64(1)) * G)[()]
+    return np.uint64(N.lib().orc_rng_key(seed % 2**64, counter % 2**64))
 
 
 def uniforms(key, idx) -> np.ndarray:
     """u(e) for the element indices ``idx`` (float64 values exact in fp32)."""
-    idx = np.asarray(idx, dtype=np.uint64)
-    with np.errstate(over="ignore"):
-        w = mix(np.uint64(key) + ((idx >> np.uint64(1)) + np.uint64(1)) * G)
-    half = np.where((idx & np.uint64(1)) == 1, w >> np.uint64(32), w & np.uint64(0xFFFFFFFF))
-    k = (half >> np.uint64(9)).astype(np.float64)
-    return (2.0 * k + 1.0) * 2.0 ** -24
+    a = np.asarray(idx, dtype=np.uint64)
+    c = np.ascontiguousarray(a.reshape(-1))
+    out = np.empty(c.shape, dtype=np.float64)
+    N.lib().orc_uniforms(int(key), N.ptr(c), c.size, N.ptr(out))
+    return out.reshape(a.shape)
 
 
 def gumbel(key, S: int, V: int) -> np.ndarray:
     """Standard Gumbel noise ``[S, V]``: row i, entry v uses element 32 * v + i."""
-    e = np.arange(V, dtype=np.uint64)[None, :] * np.uint64(MAX_ROWS) + np.arange(S, dtype=np.uint64)[:, None]
-    u = uniforms(key, e)
-    w = -np.log1p(-(1.0 - u))     # -log(u)
-    return -np.log(w)
+    out = np.empty((S, V), dtype=np.float64)
+    N.lib().orc_gumbel(int(key), S, V, N.ptr(out))
+    return out
 
 
 def accept_uniforms(key, S: int, V: int) -> np.ndarray:
     return uniforms(key, np.uint64(MAX_ROWS) * np.uint64(V) + np.arange(S, dtype=np.uint64))
-
-
-def _first_argmax(z: np.ndarray) -> int:
-    """Largest value, ties to the lowest index."""
-    return int(np.argmax(z))  # numpy returns the first occurrence
 
 
 def verify_sample(logits: np.ndarray, drafts, n_valid: int, temperature: float, seed: int, counter: int):
@@ -105,35 +95,21 @@ def verify_sample(logits: np.ndarray, drafts, n_valid: int, temperature: float, 
     """
     if not temperature > 0.0:
         raise ValueError("temperature must be > 0")
-    L = np.asarray(logits, dtype=np.float64)
+    L = N.as_c(logits, np.float64)
     S, V = L.shape
     if not 1 <= S <= MAX_ROWS or not 0 <= n_valid <= S - 1:
         raise ValueError("bad window")
-    key = rng_key(seed, counter)
-    l = L / temperature
-    z = l + gumbel(key, S, V)
-    u = accept_uniforms(key, S, V)
-    samples = np.array([_first_argmax(z[i]) for i in range(S)], dtype=np.int32)
-    m = l.max(axis=1, keepdims=True)
-    p = np.exp(l - m)
-    p /= p.sum(axis=1, keepdims=True)
-    d = np.asarray(drafts, dtype=np.int64)[:n_valid]
-    p_draft = np.array([p[i, d[i]] for i in range(n_valid)])
-
-    def top2_gap(row):
-        s = np.sort(row)
-        return float(s[-1] - s[-2]) if row.size > 1 else np.inf
-
-    z_gap = np.array([top2_gap(z[i]) for i in range(S)])
-    z_gap_res = np.full(S, np.inf)
-    j, token, margin = n_valid, int(samples[n_valid]), np.inf
-    for i in range(n_valid):
-        margin = min(margin, abs(u[i] - p_draft[i]))
-        zr = z[i].copy()
-        zr[d[i]] = -np.inf
-        z_gap_res[i] = top2_gap(zr)
-        if not u[i] < p_draft[i]:
-            j, token = i, _first_argmax(zr)
-            break
-    return {"accepted": j, "token": token, "samples": samples, "p_draft": p_draft, "u": u,
-            "z_gap": z_gap, "z_gap_res": z_gap_res, "u_margin": margin, "probs": p}
+    d = N.as_c(drafts if drafts is not None and len(drafts) else np.zeros(1, np.int32), np.int32)
+    acc, tok = np.zeros(1, np.int32), np.zeros(1, np.int32)
+    samples = np.empty(S, dtype=np.int32)
+    p_draft = np.empty(max(n_valid, 1), dtype=np.float64)
+    u = np.empty(S, dtype=np.float64)
+    z_gap, z_gap_res = np.empty(S, dtype=np.float64), np.empty(S, dtype=np.float64)
+    margin = np.zeros(1, dtype=np.float64)
+    probs = np.empty((S, V), dtype=np.float64)
+    N.check(N.lib().orc_verify_sample(N.ptr(L), S, V, N.ptr(d), n_valid, float(temperature), seed % 2**64,
+                                      counter % 2**64, N.ptr(acc), N.ptr(tok), N.ptr(samples), N.ptr(p_draft),
+                                      N.ptr(u), N.ptr(z_gap), N.ptr(z_gap_res), N.ptr(margin), N.ptr(probs)),
+            "verify_sample")
+    return {"accepted": int(acc[0]), "token": int(tok[0]), "samples": samples, "p_draft": p_draft[:n_valid],
+            "u": u, "z_gap": z_gap, "z_gap_res": z_gap_res, "u_margin": float(margin[0]), "probs": probs}

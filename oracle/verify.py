@@ -22,9 +22,12 @@ Pages followed:
   section "Baseline byte model": the lm_head is a quantised matvec over the
   whole vocabulary (the single biggest one).
 
-Readings: the dequantised GEMM accumulates in float64 (every product
-x * q * s is exact in float64) and is rounded once to float32, the dtype of
-the logits.  The argmax is taken on those float32 logits, the precision the
+The arithmetic is in the plain C++ oracle (``oracle/src/oracle.cpp``); this
+module only marshals arrays.
+
+Readings: the dequantised GEMM accumulates in float64, term by term in
+reduction order (every product x * q * s is exact in float64), and is rounded
+once to float32, the dtype of the logits.  The argmax is taken on those float32 logits, the precision the
 GPU decides in; ties go to the lowest index.  The top-2 gap that decides
 which rows are compared exactly is taken from the float64 values.
 """
@@ -32,29 +35,35 @@ from __future__ import annotations
 
 import numpy as np
 
-from .quant import BLOCK
+from . import _native as N
 
-_ROW_CHUNK = 8192  # output rows per float64 matmul (bounds memory only)
+BLOCK = 32
 
 
 def dequant_gemm64(x: np.ndarray, codes: np.ndarray, scales: np.ndarray) -> np.ndarray:
-    """Y[s, n] = sum_h x[s, h] * q[n, h] * s16[n, h // 32], in float64.
+    """Y[s, n] = sum_h x[s, h] * q[n, h] * s16[n, h // 32], in float64, h in order.
 
-    ``x`` fp16 ``[S, H]``; ``codes`` int8 ``[N, H]`` (unpacked); ``scales``
-    fp16 ``[N, H/32]``.  The matmul is a library float64 product; output rows
-    are processed in chunks only to bound memory (no element's arithmetic
-    depends on the chunking).
+    ``x`` fp16 ``[S, H]`` (or float64 values, e.g. inside the MoE); ``codes``
+    ``[N, H]`` unpacked: int8 integer codes, uint8 E2M1 codes (0..15) or float64
+    values; ``scales`` fp16 ``[N, H/32]``.
     """
-    x64 = np.asarray(x, dtype=np.float16).astype(np.float64)
-    n, h = codes.shape
-    if x64.shape[1] != h or scales.shape != (n, h // BLOCK):
+    kind, c = N.code_kind(codes)
+    n, h = c.shape
+    s = N.half_bits(scales)
+    if s.shape != (n, h // BLOCK) or h % BLOCK:
         raise ValueError("shape mismatch")
-    s64 = np.asarray(scales, dtype=np.float16).astype(np.float64)
-    y = np.empty((x64.shape[0], n), dtype=np.float64)
-    for r0 in range(0, n, _ROW_CHUNK):
-        r1 = min(n, r0 + _ROW_CHUNK)
-        w = codes[r0:r1].astype(np.float64) * np.repeat(s64[r0:r1], BLOCK, axis=1)
-        y[:, r0:r1] = x64 @ w.T
+    xa = np.asarray(x)
+    if xa.ndim != 2 or xa.shape[1] != h:
+        raise ValueError("shape mismatch")
+    y = np.empty((xa.shape[0], n), dtype=np.float64)
+    if xa.dtype == np.float16:
+        xb = N.half_bits(xa)
+        N.check(N.lib().orc_dequant_gemm64(kind, N.ptr(c), N.ptr(s), n, h, N.ptr(xb), xa.shape[0], N.ptr(y),
+                                           N.threads()), "dequant_gemm64")
+    else:
+        xd = N.as_c(xa, np.float64)
+        N.check(N.lib().orc_dequant_gemm64_x64(kind, N.ptr(c), N.ptr(s), n, h, N.ptr(xd), xa.shape[0], N.ptr(y),
+                                               N.threads()), "dequant_gemm64")
     return y
 
 
@@ -65,7 +74,17 @@ def dequant_gemm(x: np.ndarray, codes: np.ndarray, scales: np.ndarray) -> np.nda
 
 def argmax_rows(logits: np.ndarray) -> np.ndarray:
     """Per-row argmax, lowest index among equal maxima (int32 ``[S]``)."""
-    return np.argmax(np.asarray(logits), axis=1).astype(np.int32)
+    a = np.asarray(logits)
+    if a.ndim != 2:
+        raise ValueError("expected [S, N]")
+    out = np.empty(a.shape[0], dtype=np.int32)
+    if a.dtype == np.float64:
+        a = N.as_c(a, np.float64)
+        N.lib().orc_argmax_rows_f64(N.ptr(a), a.shape[0], a.shape[1], N.ptr(out))
+    else:
+        a = N.as_c(a, np.float32)
+        N.lib().orc_argmax_rows_f32(N.ptr(a), a.shape[0], a.shape[1], N.ptr(out))
+    return out
 
 
 def top2_gap(logits64: np.ndarray) -> np.ndarray:
@@ -74,11 +93,10 @@ def top2_gap(logits64: np.ndarray) -> np.ndarray:
     The second largest is taken over the other indices, so a duplicated
     maximum gives a gap of 0.
     """
-    l = np.asarray(logits64, dtype=np.float64)
-    if l.shape[1] < 2:
-        return np.full(l.shape[0], np.inf)
-    part = -np.partition(-l, 1, axis=1)[:, :2]
-    return part[:, 0] - part[:, 1]
+    a = N.as_c(logits64, np.float64)
+    out = np.empty(a.shape[0], dtype=np.float64)
+    N.lib().orc_top2_gap(N.ptr(a), a.shape[0], a.shape[1], N.ptr(out))
+    return out
 
 
 def greedy_accept(argmax: np.ndarray, drafts: np.ndarray, n_valid: int):
@@ -92,13 +110,16 @@ def greedy_accept(argmax: np.ndarray, drafts: np.ndarray, n_valid: int):
     with ``next_a0 = argmax[accepted]``: the correction on a miss, the bonus
     token when every real draft was accepted.
     """
-    s = len(argmax)
+    am = N.as_c(argmax, np.int32)
+    s = am.shape[0]
     if not (0 <= n_valid <= s - 1):
         raise ValueError("n_valid must lie in [0, S-1]")
-    j = 0
-    while j < n_valid and int(drafts[j]) == int(argmax[j]):
-        j += 1
-    return j, int(argmax[j])
+    d = N.as_c(drafts if drafts is not None and len(drafts) else np.zeros(1, np.int32), np.int32)
+    if d.shape[0] < n_valid:
+        raise ValueError("fewer drafts than n_valid")
+    acc, nxt = np.zeros(1, np.int32), np.zeros(1, np.int32)
+    N.check(N.lib().orc_greedy_accept(N.ptr(am), s, N.ptr(d), n_valid, N.ptr(acc), N.ptr(nxt)), "greedy_accept")
+    return int(acc[0]), int(nxt[0])
 
 
 def verify_head(x, codes, scales, drafts, n_valid):
@@ -107,12 +128,24 @@ def verify_head(x, codes, scales, drafts, n_valid):
     Returns a dict with ``logits`` (float32 ``[S, N]``), ``argmax`` (int32
     ``[S]``), ``accepted``, ``next_a0`` and ``gap`` (float64 ``[S]``).
     """
-    y64 = dequant_gemm64(x, codes, scales)
-    logits = y64.astype(np.float32)
-    am = argmax_rows(logits)
-    acc, nxt = greedy_accept(am, drafts, n_valid)
-    return {"logits": logits, "argmax": am, "accepted": acc, "next_a0": nxt,
-            "gap": top2_gap(y64)}
+    kind, c = N.code_kind(codes)
+    n, h = c.shape
+    s = N.half_bits(scales)
+    xb = N.half_bits(x)
+    S = xb.shape[0]
+    if xb.shape[1] != h or s.shape != (n, h // BLOCK):
+        raise ValueError("shape mismatch")
+    if not (0 <= n_valid <= S - 1):
+        raise ValueError("n_valid must lie in [0, S-1]")
+    d = N.as_c(drafts if drafts is not None and len(drafts) else np.zeros(1, np.int32), np.int32)
+    logits = np.empty((S, n), dtype=np.float32)
+    am = np.empty(S, dtype=np.int32)
+    gap = np.empty(S, dtype=np.float64)
+    acc, nxt = np.zeros(1, np.int32), np.zeros(1, np.int32)
+    N.check(N.lib().orc_verify_head(kind, N.ptr(c), N.ptr(s), n, h, N.ptr(xb), S, N.ptr(d), n_valid,
+                                    N.ptr(logits), N.ptr(am), N.ptr(gap), N.ptr(acc), N.ptr(nxt), N.threads()),
+            "verify_head")
+    return {"logits": logits, "argmax": am, "accepted": int(acc[0]), "next_a0": int(nxt[0]), "gap": gap}
 
 
 def tree_accept(argmax: np.ndarray, tokens: np.ndarray, parent: np.ndarray):
@@ -131,21 +164,12 @@ def tree_accept(argmax: np.ndarray, tokens: np.ndarray, parent: np.ndarray):
     child down, and ``argmax`` of the deepest one.  A chain (parent[i] = i-1
     for the n_valid real drafts) gives ``greedy_accept``.
     """
-    s = len(argmax)
-    acc = [True] + [False] * (s - 1)
-    depth = [0] * s
-    for i in range(1, s):
-        p = int(parent[i])
-        if 0 <= p < i and acc[p] and int(tokens[i]) == int(argmax[p]):
-            acc[i] = True
-            depth[i] = depth[p] + 1
-    best = 0
-    for i in range(1, s):
-        if acc[i] and depth[i] > depth[best]:
-            best = i
-    path = []
-    i = best
-    while i != 0:
-        path.append(i)
-        i = int(parent[i])
-    return path[::-1], int(argmax[best])
+    am = N.as_c(argmax, np.int32)
+    s = am.shape[0]
+    tok = N.as_c(tokens, np.int32) if s > 1 else np.zeros(1, np.int32)
+    par = N.as_c(parent, np.int32) if s > 1 else np.zeros(1, np.int32)
+    path = np.zeros(max(s, 1), dtype=np.int32)
+    depth, nxt = np.zeros(1, np.int32), np.zeros(1, np.int32)
+    N.check(N.lib().orc_tree_accept(N.ptr(am), s, N.ptr(tok), N.ptr(par), N.ptr(path), N.ptr(depth), N.ptr(nxt)),
+            "tree_accept")
+    return [int(v) for v in path[: int(depth[0])]], int(nxt[0])

@@ -35,11 +35,12 @@ def to_dev(a: np.ndarray, dev="cuda") -> torch.Tensor:
 def oracle_weight(w: np.ndarray, bits: int):
     """Oracle quantisation: (unpacked codes, scales fp16, stored codes).
 
-    bits 8 / 4: integer codes; bits 2: FP4 (E2M1) -- the unpacked codes are the
-    decoded float values, the stored codes the packed nibbles."""
+    bits 8 / 4: integer codes (int8); bits 2: FP4 -- the unpacked codes are the
+    E2M1 codes, one per byte (uint8, which the oracle's GEMM reads as E2M1),
+    the stored codes the packed nibbles."""
     if bits == 2:
         c4, scales = quant.quantize_fp4_block32(w)
-        return quant.decode_e2m1(c4), scales, quant.pack_nibbles(c4)
+        return c4, scales, quant.pack_nibbles(c4)
     codes, scales = quant.quantize_block32(w, bits)
     stored = codes if bits == 8 else quant.pack_int4(codes)
     return codes, scales, stored

@@ -33,7 +33,7 @@ def _fp4_weight(sdv, w):
     packed = quant.pack_nibbles(c4)
     codes_t = to_dev(packed)
     scales_t = torch.from_numpy(np.ascontiguousarray(scales.view(np.int16))).cuda().view(torch.float16)
-    return quant.decode_e2m1(c4), scales, sdv.QWeight(codes_t, scales_t, sdv.SDV_F4, n, k)
+    return c4, scales, sdv.QWeight(codes_t, scales_t, sdv.SDV_F4, n, k)
 
 
 def test_quantize_bit_exact(sdv):
@@ -142,9 +142,7 @@ def test_full_size_a3b_fp4_head(sdv):
     torch.cuda.synchronize()
     assert np.array_equal(qw.codes.cpu().numpy(), quant.pack_nibbles(c4))
     assert np.array_equal(qw.scales.cpu().numpy().view(np.uint16), scales.view(np.uint16))
-    table = quant.decode_e2m1(np.arange(16)).astype(np.float32)  # the 16 E2M1 values, exact
-    vals = table[c4]
-    del c4
+    vals = c4  # E2M1 codes: the oracle's GEMM decodes them exactly
     x = W.activations(wl, 0, S)
     ref0 = verify.verify_head(x, vals, scales, np.zeros(S - 1, np.int32), 0)
     drafts, n_valid = W.drafts(wl, 0, S, ref0["argmax"])

@@ -51,8 +51,15 @@ def test_oracle_never_reaches_the_package():
         assert PKG not in mods and "bench" not in mods, path
         text = open(path).read()
         assert "csrc" not in text and "libsdv" not in text, path
-    for path in files_under("oracle", (".c", ".h", ".cpp")):
-        assert "sdv_kernels" not in open(path).read(), path
+    cpp = files_under("oracle", (".c", ".h", ".cpp", ".hpp"))
+    assert cpp, "the oracle's C++ sources are missing"
+    for path in cpp:
+        text = open(path).read()
+        assert "sdv_kernels" not in text and "sdv_device" not in text and "sdv.h" not in text, path
+        # standard headers only: nothing of the CUDA path, no CUDA, no BLAS
+        for inc in re.findall(r'#include\s*([<"][^>"]+[>"])', text):
+            assert inc.startswith("<"), (path, inc)
+            assert not any(b in inc for b in ("cuda", "cublas", "cblas", "mkl", "immintrin", "arm_neon")), (path, inc)
 
 
 def test_generators_import_neither_side():
