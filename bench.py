@@ -307,10 +307,20 @@ def moe_bytes(wl, S: int, n_hit: int) -> int:
 
 # ---- CPU oracle (the reference arm and the cpu_baseline leg) ----------------------
 
-def oracle_sample(wl, S: int, budget_s: float):
-    """Time the CPU oracle on a bounded sample of one window and scale to a
-    full window.  Returns (windows/s, description)."""
+def oracle_sample(wl, S: int, budget_s: float, threads: int = 0):
+    """Time the CPU oracle (the plain C++ one) on a bounded sample of one window
+    with ``threads`` OpenMP threads (0: every core) and scale to a full window.
+    Returns (windows/s, description)."""
+    import oracle
     from oracle import mlp, quant, verify
+    prev = oracle.set_threads(threads)
+    try:
+        return _oracle_sample(wl, S, budget_s, mlp, quant, verify)
+    finally:
+        oracle.set_threads(prev)
+
+
+def _oracle_sample(wl, S, budget_s, mlp, quant, verify):
     x = W.activations(wl, 0, S)
     done, t_used, total = 0, 0.0, 0
     if wl.kind == "head":
@@ -374,20 +384,38 @@ def oracle_sample(wl, S: int, budget_s: float):
 
 
 def oracle_threads() -> int:
-    """Threads the oracle's numpy BLAS runs on: the BLAS pools' own count where
-    threadpoolctl can read it, else the cores this process may run on."""
+    """OpenMP threads the C++ oracle runs on when all cores are used."""
+    import oracle
+    prev = oracle.set_threads(0)
+    n = oracle.threads()
+    oracle.set_threads(prev)
+    return n
+
+
+def cpu_model() -> str:
     try:
-        from threadpoolctl import threadpool_info
-        n = max((int(i.get("num_threads", 0)) for i in threadpool_info() if i.get("user_api") == "blas"),
-                default=0)
-        if n > 0:
-            return n
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
     except Exception:
         pass
-    try:
-        return len(os.sched_getaffinity(0))
-    except (AttributeError, OSError):
-        return os.cpu_count() or 1
+    import platform
+    return platform.processor() or platform.machine()
+
+
+def cpu_baseline(wl, S: int, budget_s: float):
+    """The C++ oracle as it stands, all cores and one thread, each on a bounded
+    sample of the workload (budget_s of CPU time each), scaled to windows/s."""
+    if budget_s <= 0:
+        return {"value": None, "unit": "windows/s", "cores": None, "kind": "oracle", "sample": "skipped"}
+    cores = oracle_threads()
+    r_all, d_all = oracle_sample(wl, S, budget_s, cores)
+    r_one, d_one = oracle_sample(wl, S, budget_s, 1)
+    return {"value": r_all, "unit": "windows/s", "cores": cores, "kind": "oracle",
+            "sample": f"plain C++ oracle (fp64, OpenMP over output rows) on {cores} threads: {d_all}",
+            "single_thread": {"value": r_one, "unit": "windows/s", "cores": 1, "sample": d_one},
+            "cpu_model": cpu_model()}
 
 
 def wtype(bits: int) -> str:
@@ -411,7 +439,7 @@ def run_reference(args, wl, S, world, rank):
     rates = []
     desc = ""
     for i in range(args.warmup + args.steps):
-        r, desc = oracle_sample(wl, S, budget)
+        r, desc = oracle_sample(wl, S, budget, 0)
         if i >= args.warmup:
             rates.append(r)
     value = float(np.mean(rates))
@@ -421,7 +449,8 @@ def run_reference(args, wl, S, world, rank):
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": workload_name(wl, S), "S": S},
         "cpu_baseline": {"value": value, "unit": "windows/s", "cores": oracle_threads(), "kind": "oracle",
-                         "sample": desc},
+                         "sample": "plain C++ oracle (fp64, OpenMP over output rows), each step: " + desc,
+                         "cpu_model": cpu_model()},
         "e2e": {"value": value, "unit": "windows/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line))
@@ -705,7 +734,7 @@ def run_sdv(args, wl, S, world, rank, local):
     achieved = nbytes / (kernel_ms / 1000.0) / 1e9
     prof_key = f"{wl.name} S={S}" + (" sample" if sampling else "") + (" fp4" if wl.bits == 2 else "")
     traffic, traffic_src = (profiled_traffic(prof_key) if wl.kind == "head" else (None, None))
-    cpu_rate, cpu_desc = oracle_sample(wl, S, args.cpu_budget) if args.cpu_budget > 0 else (None, "skipped")
+    cpu = cpu_baseline(wl, S, args.cpu_budget)
     line = {
         "metric": METRIC, "value": value, "unit": "windows/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": elapsed_ms / args.steps, "higher_is_better": True,
@@ -719,8 +748,7 @@ def run_sdv(args, wl, S, world, rank, local):
                      "traffic": traffic, "traffic_source": traffic_src, "peak_kind": kind, "kernel": f"{job.kernel} ({args.path} path)",
                      "kernel_ms": kernel_ms, "kernel_ms_serialised": iso_ms,
                      "timing": "events around the K back-to-back launches of the timed region, / K"},
-        "cpu_baseline": {"value": cpu_rate, "unit": "windows/s", "cores": oracle_threads(), "kind": "oracle",
-                         "sample": cpu_desc},
+        "cpu_baseline": cpu,
         "e2e": {"value": world * args.steps / (e2e_ms / 1000.0), "unit": "windows/s",
                 "h2d_bytes_per_step": job.h2d, "d2h_bytes_per_step": job.d2h},
         "gpu_launches": args.steps * job.launches,

@@ -268,7 +268,6 @@ __global__ void __launch_bounds__(TcRoles<(QT == 8 ? 8 : 4)>::kThreads, 1)
   const int tile_hi = unit * (int)((long)(blockIdx.x + 1) * (tiles / unit) / gridDim.x);
   const int ntile = tile_hi - tile_lo;
   if (MODE == kModeY && k_len <= 0) {
-    if (!dep_early) griddep_wait();
     // an empty reduction range still owns its split's partial outputs: zeros
     float* const yo = p.y + (size_t)blockIdx.y * p.S * ldy;
     for (int v = threadIdx.x; v < ntile * kTileRows * p.S; v += blockDim.x) {
@@ -405,6 +404,10 @@ __global__ void __launch_bounds__(TcRoles<(QT == 8 ? 8 : 4)>::kThreads, 1)
     best_v[threadIdx.x] = -FLT_MAX;
     best_i[threadIdx.x] = INT_MAX;
   }
+  if (!dep_early) griddep_wait();
+  // the drafts, for the accept at the end (whichever CTA runs it)
+  if (MODE != kModeY && warp == 2 && lane < p.n_valid) s_drafts[lane] = p.drafts[lane];
+
   tc_fence_before();
   __syncthreads();  // barriers initialised, tensor memory allocated
   tc_fence_after();
@@ -413,13 +416,10 @@ __global__ void __launch_bounds__(TcRoles<(QT == 8 ? 8 : 4)>::kThreads, 1)
   // are warp-uniform expressions of the loop counters (a base loaded from shared
   // memory is not provably uniform and each MMA would pay to make it so).
   constexpr uint32_t tmem = 0u;
+  if (threadIdx.x == 0 && *s_tmem != tmem) atomicOr(p.status, kDevErrTmemBase);
 
   // ---- start the weight stream (the TMA unit carries only weights: each TMA
-  // issue costs ~0.15 us at start-up).  Only this library's kernels release their
-  // dependents before they complete, and none of them writes weights (the
-  // quantiser runs to completion first), so the first stages are requested before
-  // waiting for the previous grid: their issue cost and memory latency overlap
-  // its tail.  (The MoE mappings need the hit list first and have waited.) ----
+  // issue costs ~0.15 us at start-up) ----
   if (threadIdx.x == 0) {
     policy = l2_policy_evict_first();
     tma_prefetch_desc(&tm_codes);
@@ -431,12 +431,6 @@ __global__ void __launch_bounds__(TcRoles<(QT == 8 ? 8 : 4)>::kThreads, 1)
     Cursor c = cursor_at(0);
     for (; c.i < depth && c.i < nstages; advance(c)) issue(c);
   }
-  if (!dep_early) griddep_wait();  // everything below may read what the previous grid wrote
-  if (threadIdx.x == 0 && *s_tmem != tmem) atomicOr(p.status, kDevErrTmemBase);
-  // the drafts, for the accept at the end (whichever CTA runs it) and for the
-  // sampling epilogue: the four epilogue warps meet before any of them reads them
-  if (MODE != kModeY && warp == 2 && lane < p.n_valid) s_drafts[lane] = p.drafts[lane];
-  if (MODE != kModeY && warp >= 2 && warp < R::kConv0) named_bar_sync(2, 4 * 32);
   // ---- window rows, slice by slice in this CTA's rotated order: the epilogue
   // warps (idle until the first tile) load each 16-byte chunk, permute it like
   // the converted codes and store it as K-major core matrices (zeros past S and

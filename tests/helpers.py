@@ -11,6 +11,8 @@ Comparison rules (from the stated tolerances):
 """
 from __future__ import annotations
 
+import os
+
 import numpy as np
 import torch
 
@@ -109,3 +111,23 @@ def run_head(head, x: np.ndarray, drafts: np.ndarray, n_valid: int, want_logits=
     assert sdv.sdv_last_device_status(ws) == sdv.SDV_OK
     return (logits.cpu().numpy() if want_logits else None, am.cpu().numpy(), int(acc.item()),
             int(nxt.item()))
+
+
+GOLDEN_DIR = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+def load_windows(prefix: str, name: str, S: int):
+    """(header dict, window records) of tests/golden/<prefix>_<name>_s<S>.jsonl, a
+    file of the oracle's per-window results written by a committed generator
+    that calls only oracle/ (make_head_windows.py, make_mlp_windows.py)."""
+    import json
+    head, recs = {}, []
+    with open(os.path.join(GOLDEN_DIR, f"{prefix}_{name}_s{S}.jsonl")) as f:
+        for line in f:
+            if line.startswith("#"):
+                if ":" in line:
+                    k, v = line[1:].split(":", 1)
+                    head[k.strip()] = v.strip()
+            elif line.strip():
+                recs.append(json.loads(line))
+    return head, recs
