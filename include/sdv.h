@@ -370,6 +370,21 @@ SDV_API sdv_status sdv_noalloc_device_status(sdv_stream_t stream);
  */
 SDV_API int32_t sdv_set_gemm_path(int32_t path);
 
+/*
+ * Test hook of the timeout path (process-wide; every later launch of the
+ * tcgen05 path uses it until it is reset with (-1, 0)).  withhold_stage >= 0:
+ * in every CTA the weight copy of that stage of the CTA's stage sequence is
+ * never issued, so the converters waiting for it give up after the wait limit
+ * -- a wait on a barrier that nothing completes, with no copy in flight behind
+ * it; the kernel then drains what it issued, writes undefined outputs and sets
+ * the status word (sdv_last_device_status / sdv_noalloc_device_status return
+ * SDV_ERR_TIMEOUT); later calls are unaffected.  wait_limit_ns: the limit of
+ * every bounded device wait (0 = the built-in 2 s; else at least 100000).
+ * -1 and 0 switch both off.  Returns SDV_ERR_INVALID_ARG for other values.
+ * For the library's own tests; no production caller needs it.
+ */
+SDV_API sdv_status sdv_debug_fault(int32_t withhold_stage, uint64_t wait_limit_ns);
+
 /* A static, human-readable name of a status code. */
 SDV_API const char* sdv_status_string(sdv_status status);
 

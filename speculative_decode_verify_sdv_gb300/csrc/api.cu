@@ -165,6 +165,15 @@ GemmPlan plan_gemm(int qbits, int n, int k, int S, bool allow_split) {
 // mma.sync path, 2 = the tcgen05 path only.
 std::atomic<int> g_gemm_path{0};
 
+// Timeout-path test hooks (sdv_debug_fault): applied to every tcgen05 launch.
+std::atomic<unsigned long long> g_debug_wait_ns{0};
+std::atomic<int> g_debug_withhold{0};
+
+void apply_debug(GemmArgs& a) {
+  a.wait_ns = g_debug_wait_ns.load();
+  a.debug_withhold = g_debug_withhold.load();
+}
+
 // tcgen05 path plan: 128-row tiles, at most one CTA per SM.  Without split-K
 // (the verify head, the MoE gate/up) one split covers the full reduction.
 // With split-K every split count whose window rows fit next to a ring of at
@@ -301,6 +310,7 @@ sdv_status run_gemm(const sdv_qweight* w, const uint16_t* x, int S, int mode, Ge
       a.y = y_final;
     }
   }
+  if (pl.tc) apply_debug(a);
   cudaError_t e = pl.tc ? sdv::launch_tc_gemm(w->qtype, mode, tc, tsc, tc, tsc, a, pl.grid, pl.smem, st)
                         : sdv::launch_dq_gemm(w->qtype, mode, tc, tsc, a, pl.grid, pl.smem, st);
   if (e == cudaSuccess && part != nullptr)
@@ -337,6 +347,7 @@ sdv_status launch_tc_y(const sdv_qweight* w, const sdv_qweight* w2, const GemmPl
   a.depth = pl.depth;
   a.status = static_cast<int*>(ws);
   a.ticket = reinterpret_cast<unsigned*>(static_cast<char*>(ws) + 4);
+  apply_debug(a);
   return cuda_status(sdv::launch_tc_gemm(w->qtype, sdv::kModeY, tc, tsc, tc2, tsc2, a, pl.grid, pl.smem, st));
 }
 
@@ -441,6 +452,13 @@ bool moe_args_ok(const sdv_qweight* gate, const sdv_qweight* up, const sdv_qweig
 extern "C" {
 
 int32_t sdv_version(void) { return 100; }
+
+sdv_status sdv_debug_fault(int32_t withhold_stage, uint64_t wait_limit_ns) {
+  if (withhold_stage < -1 || (wait_limit_ns != 0 && wait_limit_ns < 100000ull)) return SDV_ERR_INVALID_ARG;
+  g_debug_withhold.store(withhold_stage < 0 ? 0 : withhold_stage + 1);
+  g_debug_wait_ns.store(wait_limit_ns);
+  return SDV_OK;
+}
 
 int32_t sdv_set_gemm_path(int32_t path) {
   if (path < 0 || path > 2) return -1;

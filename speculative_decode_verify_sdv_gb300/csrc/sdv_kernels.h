@@ -81,6 +81,10 @@ struct GemmArgs {
   int ldh;
   const float* row_w;
   int ldw;
+  // ---- timeout-path test hooks of the tcgen05 path (zero = off) ----
+  unsigned long long wait_ns;  // limit of every bounded wait (0: kWaitLimitNs)
+  int debug_withhold;          // 1 + the stage index whose weight copy the producer never
+                               //    issues (its ring slot then never fills), 0 = none
 };
 
 int gemm_tile_mt(int qbits);

@@ -310,7 +310,9 @@ __global__ void __launch_bounds__(TcRoles<(QT == 8 ? 8 : 4)>::kThreads, 1)
 
   auto wait = [&](uint32_t bar, uint32_t parity) -> bool {
     if (*s_dead) return false;
-    if (mbar_wait_bounded(bar, parity)) return true;
+    if (mbar_try_wait(bar, parity)) return true;
+    // the limit is read only on the slow path (a test may shorten it)
+    if (mbar_wait_bounded(bar, parity, p.wait_ns != 0 ? p.wait_ns : kWaitLimitNs)) return true;
     *s_dead = 1;
     atomicOr(p.status, kDevErrTimeout);
     return false;
@@ -348,6 +350,9 @@ __global__ void __launch_bounds__(TcRoles<(QT == 8 ? 8 : 4)>::kThreads, 1)
   };
   uint64_t policy = 0;
   auto issue = [&](const Cursor& c) {  // TMA of stage c.i into ring slot c.slot
+    // the timeout-path test withholds one stage: its slot never fills, and the
+    // slot's previous copy has been consumed, so nothing is in flight there
+    if (p.debug_withhold == c.i + 1) return;
     const int slot = c.slot, ks = c.kx;
     int mat, lt;
     int row0 = tile_map(tile_lo + c.t, mat, lt);
@@ -494,12 +499,15 @@ __global__ void __launch_bounds__(TcRoles<(QT == 8 ? 8 : 4)>::kThreads, 1)
         issue(c);
         issued = c.i + 1;
       }
-      if (*s_dead) {
-        // after a timeout, let this CTA's copies still in flight land (bounded):
-        // the latest copy into each slot is the only one that can be pending
-        for (int j = max(0, issued - depth); j < issued; ++j)
+      // No copy may outlive the CTA.  The latest copy into each slot is the only
+      // one that can still be pending: an earlier one was waited for by the
+      // converter that released the slot, or the slot was not refilled.  Wait for
+      // them (bounded) whatever happens to the rest of the CTA: in a normal run
+      // they land and are consumed anyway; after a timeout a converter may have
+      // stopped waiting for them.
+      for (int j = max(0, issued - depth); j < issued; ++j)
+        if (p.debug_withhold != j + 1)  // a withheld stage has no copy to wait for
           mbar_wait_bounded(bar_full + 8 * (j % depth), (j / depth) & 1, kDrainLimitNs);
-      }
     }
   } else if (warp == 1) {
     // ---------------- MMA issuer (warp-uniform loop, one elected lane issues) ------

@@ -23,7 +23,7 @@ EXPORTED = (
     "sdv_quantize_block32", "sdv_qlinear", "sdv_qlinear_swiglu", "sdv_verify_head",
     "sdv_greedy_accept", "sdv_moe_gather_qmm", "sdv_workspace_bytes", "sdv_workspace_init",
     "sdv_last_device_status", "sdv_device_status", "sdv_noalloc_device_status", "sdv_status_string", "sdv_version", "sdv_verify_head_noalloc", "sdv_set_gemm_path",
-    "sdv_moe_route", "sdv_verify_sample", "sdv_tree_accept",
+    "sdv_moe_route", "sdv_verify_sample", "sdv_tree_accept", "sdv_debug_fault",
     "sdv_ngram_create", "sdv_ngram_destroy", "sdv_ngram_append", "sdv_ngram_propose",
 )
 
@@ -72,6 +72,7 @@ def load() -> ctypes.CDLL:
         "sdv_status_string": ([i32], ctypes.c_char_p),
         "sdv_version": ([], i32),
         "sdv_set_gemm_path": ([i32], i32),
+        "sdv_debug_fault": ([i32, ctypes.c_uint64], i32),
         "sdv_ngram_create": ([i32, ctypes.POINTER(vp)], i32),
         "sdv_ngram_destroy": ([vp], i32),
         "sdv_ngram_append": ([vp, vp, i32], i32),
@@ -134,6 +135,12 @@ def sdv_set_gemm_path(path: int) -> int:
     if prev < 0:
         raise ValueError(f"invalid GEMM path {path}")
     return prev
+
+
+def sdv_debug_fault(withhold_stage: int, wait_limit_ns: int) -> None:
+    """Timeout-path test hook: withhold one weight stage of every tcgen05 launch
+    and shorten the bounded waits (-1, 0 switches it off)."""
+    _check("sdv_debug_fault", load().sdv_debug_fault(withhold_stage, wait_limit_ns))
 
 
 def sdv_status_string(status: int) -> str:

@@ -13,9 +13,8 @@ import numpy as np
 import pytest
 import torch
 
-from oracle import mlp, quant, verify
+from oracle import mlp, verify
 from synth import generator as G
-from synth import workloads as W
 from tests.helpers import device_weight, gemm_path, oracle_weight, to_dev, to_dev_f16, tol
 
 pytestmark = pytest.mark.gpu
@@ -99,31 +98,6 @@ def test_swiglu_integer_exact(sdv, path):
     ref = mlp.qlinear_swiglu(x, cg, sc, cu, sc).astype(np.float64)
     ulp = np.spacing(np.abs(ref).astype(np.float16)).astype(np.float64)
     assert (np.abs(h - ref) <= ulp + 1e-30).all()
-
-
-_MLP = {}
-
-
-@pytest.mark.parametrize("S", [1, 9, 17])
-def test_swiglu_full_mlp27(sdv, S):
-    """The 27B-shaped gate/up projection (17408 x 5120 int8 each)."""
-    wl = W.MLP27
-    if "gu" not in _MLP:
-        out = []
-        for which in ("gate", "up"):
-            w = W.mlp_weights(wl, which)
-            dw = sdv.quantize(to_dev(w), 8)
-            codes, scales = quant.quantize_block32(w, 8)
-            del w
-            torch.cuda.synchronize()
-            np.testing.assert_array_equal(dw.codes.cpu().numpy().view(np.uint8), codes.view(np.uint8))
-            out.append((dw, codes, scales))
-        _MLP["gu"] = out
-    (gate, cg, sg), (up, cu, su) = _MLP["gu"]
-    x = W.activations(wl, 0, S)
-    h = _run_swiglu(sdv, gate, up, x)
-    assert_swiglu_close(h, verify.dequant_gemm64(x, cg, sg), verify.dequant_gemm64(x, cu, su), wl.h,
-                        f"mlp27 S={S}")
 
 
 # ---------------------------------------------------------------- MoE ----
@@ -238,25 +212,3 @@ def test_moe_identical_experts(sdv):
     x = G.normal(G.stream_seed(721, 902, S), (S, H), 1.0, dtype=np.float64).astype(np.float16)
     one = mlp.expert_swiglu64(x, 0, I, H, T["gate"][0], T["up"][0], T["down"][0])
     assert _rel_l2(out, one) <= 1e-3
-
-
-def test_moe_full_config(sdv):
-    """The 35B-A3B-shaped MoE layer: 256 experts (512 x 2048) int4, top-8, S = 17."""
-    wl = W.MOE
-    E, I, H, k, S = wl.experts, wl.inter, wl.h, wl.top_k, 17
-    T = {}
-    for which in ("gate", "up", "down"):
-        w = W.moe_weights(wl, which)
-        dw = sdv.quantize(to_dev(w), wl.bits)
-        codes, scales = quant.quantize_block32(w, wl.bits)
-        del w
-        torch.cuda.synchronize()
-        stored = quant.pack_int4(codes)
-        np.testing.assert_array_equal(dw.codes.cpu().numpy().view(np.uint8), stored.view(np.uint8))
-        T[which] = ((codes, scales), dw)
-    x = W.activations(wl, 0, S)
-    logits = W.router_logits(wl, 0, S)
-    out, ids, wts = _run_moe(sdv, T, E, I, H, k, x, logits)
-    ref, rid, rw = mlp.moe_forward(x, logits, T["gate"][0], T["up"][0], T["down"][0], E, I, H, k)
-    np.testing.assert_array_equal(ids, rid)
-    assert _rel_l2(out, ref) <= 1e-3

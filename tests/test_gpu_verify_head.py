@@ -3,18 +3,18 @@
 Covers the tiny head over all 1000 seeded windows, window sizes S = 1 .. 32,
 ragged vocabulary (not a multiple of the 16-row tile) and ragged reduction
 length (not a multiple of the 256-element stage), int8 and int4, planted ties
-and maxima in the last tile, and the two full-size heads in the launch
-configuration the benchmark times.
+and maxima in the last tile.  The two full-size heads run every seeded window
+in test_gpu_windows.py.
 """
 import numpy as np
 import pytest
 import torch
 
-from oracle import quant, verify
+from oracle import verify
 from synth import generator as G
 from synth import workloads as W
 from tests.helpers import (GAP, assert_gemm_close, check_head_outputs, device_weight, gemm_path,
-                           oracle_weight, run_head, to_dev)
+                           oracle_weight, run_head)
 
 pytestmark = pytest.mark.gpu
 
@@ -212,46 +212,3 @@ def test_workspace_reused_across_calls(sdv, path):
         logits, am, acc, nxt = run_head(head, x, np.zeros(S - 1, np.int32), 0, ws=ws)
         check_head_outputs(ref, am, acc, nxt)
     assert int(ws[4:8].view(torch.int32).item()) == 0  # ticket counter back at zero
-
-
-_FULL = {}
-
-
-def _full_state(sdv, wl):
-    if wl.name not in _FULL:
-        _FULL.clear()
-        w = W.head_weights(wl)
-        head = sdv.quantize(to_dev(w), wl.bits)
-        codes, scales = quant.quantize_block32(w, wl.bits)
-        del w
-        torch.cuda.synchronize()
-        stored = codes if wl.bits == 8 else quant.pack_int4(codes)
-        np.testing.assert_array_equal(head.codes.cpu().numpy().view(np.uint8), stored.view(np.uint8))
-        np.testing.assert_array_equal(head.scales.cpu().numpy().view(np.uint16), scales.view(np.uint16))
-        _FULL[wl.name] = (head, codes, scales)
-    return _FULL[wl.name]
-
-
-def _full_size(sdv, wl, S, windows):
-    head, codes, scales = _full_state(sdv, wl)
-    for win in windows:
-        x = W.activations(wl, win, S)
-        ref0 = verify.verify_head(x, codes, scales, np.zeros(S - 1, np.int32), 0)
-        drafts, n_valid = W.drafts(wl, win, S, ref0["argmax"])
-        ref = verify.verify_head(x, codes, scales, drafts, n_valid)
-        logits, am, acc, nxt = run_head(head, x, drafts, n_valid)
-        assert_gemm_close(logits, ref["logits"], wl.h, f"{wl.name} window {win}")
-        check_head_outputs(ref, am, acc, nxt)
-        # the timed configuration (no logits) gives the same ids
-        _, am2, acc2, nxt2 = run_head(head, x, drafts, n_valid, want_logits=False)
-        np.testing.assert_array_equal(am2, am)
-        assert (acc2, nxt2) == (acc, nxt)
-
-
-def test_full_size_q4b_head(sdv, path):
-    _full_size(sdv, W.Q4B, 9, [0, 1])
-
-
-@pytest.mark.parametrize("S", [1, 2, 9, 17])
-def test_full_size_a3b_head(sdv, path, S):
-    _full_size(sdv, W.A3B, S, [0])

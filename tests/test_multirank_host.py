@@ -34,7 +34,7 @@ def _worker(rank, world, port, out):
 
 def test_rank_helpers_over_gloo():
     world = 2
-    mgr = mp.Manager()
+    mgr = mp.get_context("spawn").Manager()  # no fork of a process that may hold OpenMP threads
     out = mgr.dict()
     mp.spawn(_worker, args=(world, _free_port(), out), nprocs=world, join=True)
     assert dict(out) == {0: (2, 0, 20.0), 1: (2, 1, 20.0)}
