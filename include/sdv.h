@@ -158,9 +158,14 @@ SDV_API sdv_status sdv_qlinear_swiglu(const sdv_qweight* gate, const sdv_qweight
  * One kernel launch: a persistent dequant GEMM whose epilogue reduces each
  * CTA's vocabulary slab to per-row (max, index) partials in `ws`; the last CTA
  * to finish reduces the partials and runs the accept.  When the window rows of
- * a long reduction do not fit one tensor-core launch's shared memory (e.g.
- * k = 2560 at S >= 17), the rows are verified in two (or more) chunks, each
- * streaming the head once, and a single-warp launch runs the accept.
+ * a long reduction do not fit one tensor-core launch's shared memory next to
+ * its ring (e.g. k = 2560 at S >= 17), each CTA takes part of the reduction: one
+ * pass over the head writes fp32 partial logits into `ws` (the workspace size
+ * sdv_workspace_bytes gives for such a shape includes them), and a second
+ * launch sums them in split order, takes the argmax and runs the accept.  With
+ * a workspace too small for the partials (at least the size for a one-row head)
+ * the rows are verified in chunks instead, each streaming the head once, and a
+ * single-warp launch runs the accept.
  */
 SDV_API sdv_status sdv_verify_head(const sdv_qweight* head, const uint16_t* x, int32_t S,
                            const int32_t* drafts, int32_t n_valid, float* logits_or_null,
@@ -365,7 +370,9 @@ SDV_API sdv_status sdv_noalloc_device_status(sdv_stream_t stream);
  *   0 = automatic: the tcgen05 path (tensor-memory accumulators, 128-row tiles)
  *       whenever its shared-memory plan fits, else the mma.sync path;
  *   1 = the mma.sync path (m16n8k16 tensor-core MMA from registers);
- *   2 = the tcgen05 path only (SDV_ERR_UNSUPPORTED where its plan does not fit).
+ *   2 = the tcgen05 path only (SDV_ERR_UNSUPPORTED where its plan does not fit);
+ *   3 = the CUDA-core GEMV (fp32 FMAs, no tensor cores) for windows of one or
+ *       two rows -- sdv_qlinear and sdv_verify_head with S <= 2 -- else as 0.
  * Returns the previous selection, or -1 for an invalid value (nothing changes).
  */
 SDV_API int32_t sdv_set_gemm_path(int32_t path);

@@ -126,9 +126,13 @@ extern "C" SDV_API sdv_status sdv_verify_head_noalloc(const sdv_qweight* head, c
   const sdv_status bad = check_args(head, x, S, drafts, n_valid, argmax, accepted, next_a0);
   if (bad != SDV_OK) return bad;
   // the weight is valid here, so 0 can only mean a shape the plans reject
-  const size_t need = sdv_workspace_bytes(SDV_OP_VERIFY_HEAD, head->n, head->k, S, 0, 0);
-  if (need == 0) return SDV_ERR_INVALID_ARG;
-  if (need > kScratchBytes) return SDV_ERR_WORKSPACE;  // beyond the fixed scratch
+  if (sdv_workspace_bytes(SDV_OP_VERIFY_HEAD, head->n, head->k, S, 0, 0) == 0) return SDV_ERR_INVALID_ARG;
+  // The least scratch a head call uses -- status word, ticket and per-CTA argmax
+  // partials, the same for every weight (a one-row head asks for exactly that).
+  // Windows whose rows need the reduction split for the tensor-core plan run in
+  // row chunks here instead: the fixed scratch cannot hold partial logits.
+  const size_t need = sdv_workspace_bytes(SDV_OP_VERIFY_HEAD, 1, 32, S, 0, 0);
+  if (need == 0 || need > kScratchBytes) return SDV_ERR_WORKSPACE;  // beyond the fixed scratch
   void* ws = nullptr;
   const sdv_status st = scratch_address(&ws);
   if (st != SDV_OK) return st;

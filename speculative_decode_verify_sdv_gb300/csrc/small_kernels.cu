@@ -1,10 +1,13 @@
-// Small kernels of the verify path: the per-block-32 quantiser and the
-// stand-alone greedy accept.
+// Small kernels of the verify path: the per-block-32 quantiser, the
+// stand-alone greedy and tree accepts, and the tail of the split-reduction head.
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
+#include <cfloat>
+#include <climits>
 #include <cstdint>
 
+#include "sdv_device.cuh"
 #include "sdv_kernels.h"
 
 namespace sdv {
@@ -120,7 +123,127 @@ __global__ void tree_accept_kernel(const int32_t* __restrict__ argmax, int S, co
   }
 }
 
+// Tail of the verify head when the window's rows fit the tensor-core plan only
+// with the reduction split (e.g. k = 2560 at S >= 17): the split GEMM has written
+// fp32 partial logits part[split][s][v]; here logits[s][v] = their sum in split
+// order (written when `logits` is not null), each CTA reduces its slab of the
+// vocabulary to per-row (max, lowest index) partials, and the last CTA to finish
+// (acquire-release ticket) merges them, writes argmax[S] and runs the greedy accept
+// ("Stream C -- Speculative decoding: feasibility verdict + implementation plan",
+// section "The delta").
+constexpr int kSplitSumThreads = 256;
+
+__global__ void __launch_bounds__(kSplitSumThreads) head_splitsum_kernel(
+    const float* __restrict__ part, int splits, int S, int n, float* __restrict__ logits, float* part_v, int* part_i,
+    const int32_t* __restrict__ drafts, int n_valid, int32_t* argmax, int32_t* accepted, int32_t* next_a0,
+    unsigned* ticket) {
+  griddep_wait();
+  griddep_launch_dependents();
+  __shared__ float s_v[kSplitSumThreads / 32][32];
+  __shared__ int s_i[kSplitSumThreads / 32][32];
+  __shared__ int s_am[32], s_dr[32], s_flag;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int c0 = (int)((long)blockIdx.x * n / gridDim.x), c1 = (int)((long)(blockIdx.x + 1) * n / gridDim.x);
+  const long plane = (long)S * n;  // one split's partials
+  float bv[32];
+  int bi[32];
+#pragma unroll
+  for (int s = 0; s < 32; ++s) {
+    bv[s] = -FLT_MAX;
+    bi[s] = INT_MAX;
+  }
+  for (int v = c0 + threadIdx.x; v < c1; v += kSplitSumThreads) {
+#pragma unroll
+    for (int s = 0; s < 32; ++s) {
+      if (s < S) {
+        const float* pp = part + (long)s * n + v;
+        float val = __ldcg(pp);
+        for (int sp = 1; sp < splits; ++sp) val += __ldcg(pp + sp * plane);
+        if (logits != nullptr) logits[(long)s * n + v] = val;
+        argmax_merge(bv[s], bi[s], val, v);
+      }
+    }
+  }
+  // per row: the warp's best, then the block's (one warp per row group of 32)
+#pragma unroll
+  for (int s = 0; s < 32; ++s) {
+    if (s < S) {
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, bv[s], off);
+        const int oi = __shfl_xor_sync(0xffffffffu, bi[s], off);
+        argmax_merge(bv[s], bi[s], ov, oi);
+      }
+      if (lane == 0) {
+        s_v[warp][s] = bv[s];
+        s_i[warp][s] = bi[s];
+      }
+    }
+  }
+  __syncthreads();
+  if (threadIdx.x < S) {
+    const int s = threadIdx.x;
+    float v = s_v[0][s];
+    int i = s_i[0][s];
+    for (int w = 1; w < kSplitSumThreads / 32; ++w) argmax_merge(v, i, s_v[w][s], s_i[w][s]);
+    __stcg(part_v + (long)blockIdx.x * S + s, v);
+    __stcg(part_i + (long)blockIdx.x * S + s, i);
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    // publishes this CTA's partials (cumulative over the block's stores before the
+    // barrier) and, for the last CTA, acquires everyone else's
+    unsigned tk;
+    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(tk) : "l"(ticket) : "memory");
+    s_flag = (tk == gridDim.x - 1) ? 1 : 0;
+  }
+  __syncthreads();
+  if (s_flag == 0) return;
+  for (int s = warp; s < S; s += kSplitSumThreads / 32) {
+    float v = -FLT_MAX;
+    int i = INT_MAX;
+    for (int j = lane; j < (int)gridDim.x; j += 32)
+      argmax_merge(v, i, __ldcg(part_v + (long)j * S + s), __ldcg(part_i + (long)j * S + s));
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, v, off);
+      const int oi = __shfl_xor_sync(0xffffffffu, i, off);
+      argmax_merge(v, i, ov, oi);
+    }
+    if (lane == 0) {
+      s_am[s] = i;
+      argmax[s] = i;
+    }
+  }
+  if (threadIdx.x < n_valid) s_dr[threadIdx.x] = drafts[threadIdx.x];
+  __syncthreads();
+  if (warp == 0) {  // accepted = the first window position whose draft misses (n_valid <= 31)
+    const bool hit = lane < n_valid && s_dr[lane] == s_am[lane];
+    const unsigned miss = ~__ballot_sync(0xffffffffu, hit);
+    const int j = __ffs(miss) - 1;
+    if (lane == 0) {
+      *accepted = j;
+      *next_a0 = s_am[j];
+      *ticket = 0u;
+    }
+  }
+}
+
 }  // namespace
+
+int head_splitsum_grid(int n, int sms) {
+  int g = (n + kSplitSumThreads - 1) / kSplitSumThreads;
+  const int cap = 2 * (sms > 0 ? sms : 1);
+  return g < cap ? g : cap;
+}
+
+cudaError_t launch_head_splitsum(const float* part, int splits, int S, int n, float* logits, float* part_v,
+                                 int* part_i, const int32_t* drafts, int n_valid, int32_t* argmax, int32_t* accepted,
+                                 int32_t* next_a0, unsigned* ticket, int grid, cudaStream_t st) {
+  if (S < 1 || S > 32 || n_valid < 0 || n_valid > S - 1 || grid < 1) return cudaErrorInvalidValue;
+  return launch_pdl(head_splitsum_kernel, dim3((unsigned)grid), dim3(kSplitSumThreads), 0, st, part, splits, S, n,
+                    logits, part_v, part_i, drafts, n_valid, argmax, accepted, next_a0, ticket);
+}
 
 cudaError_t launch_tree_accept(const int32_t* argmax, int S, const int32_t* tokens, const int32_t* parent,
                                int32_t* path, int32_t* accepted, int32_t* next_a0, cudaStream_t st) {

@@ -105,10 +105,22 @@ def test_moe_plan(tracer):
     assert "splitk_reduce" in red["name"]
 
 
-def test_q4b_head_beyond_one_launch_is_row_chunked(tracer):
+def test_q4b_head_beyond_one_launch_splits_the_reduction(tracer):
     # int8, k = 2560: S = 17 window rows leave no room for a 4-stage ring next to
-    # them, so the head runs as row chunks on the tcgen05 path, then one accept
+    # them; with a full workspace each CTA takes part of the reduction (one pass
+    # over the head writing partial logits), then the split-sum tail
     (c,) = trace(tracer, "head 8 151936 2560 17 16 0")
+    assert c["status"] == OK and len(c["launches"]) == 2
+    gemm, tail = c["launches"]
+    assert tc_args(gemm) == (8, 0, 32) and int(gemm["splits"]) >= 2 and gemm["S"] == "17"
+    assert int(gemm["k_chunk"]) * (int(gemm["splits"]) - 1) < 2560 <= int(gemm["k_chunk"]) * int(gemm["splits"])
+    assert "head_splitsum_kernel" in tail["name"] and int(tail["grid"].split(",")[0]) <= 2 * SMS
+
+
+def test_q4b_head_beyond_one_launch_without_room_is_row_chunked(tracer):
+    # the same window through the fixed scratch of the no-workspace head, which
+    # cannot hold partial logits: row chunks on the tcgen05 path, then one accept
+    (c,) = trace(tracer, "noalloc 8 151936 2560 17 16")
     gemms = [l for l in c["launches"] if tc_args(l)]
     assert c["status"] == OK and [int(l["S"]) for l in gemms] == [9, 8]
     assert all(l["n_valid"] == "0" for l in gemms)

@@ -4,10 +4,12 @@ It serves callers that cannot allocate device memory themselves (a host
 framework owns every byte of device memory, or the call sits in a loop where
 an allocation is not allowed): the scratch lives in a fixed device array
 inside the library.  Two calls in a row must match the workspace entry point
-(sdv_verify_head) -- identical ids, logits within the parity tolerance -- and
-the oracle.  The cases cover a plain window, the widest window (S = 32, the
-largest scratch need) and the row-chunked int8 head with k = 2560 at S = 17,
-where several launches reuse the array in sequence.  This file is collected
+(sdv_verify_head) -- bit for bit where both run the same plan, within the
+parity tolerance where the workspace entry point splits the reduction and the
+fixed scratch runs row chunks -- and the oracle.  The cases cover a plain
+window, the widest window (S = 32, the largest scratch need) and the
+row-chunked int8 head with k = 2560 at S = 17, where several launches reuse
+the array in sequence.  This file is collected
 last so that a run stopping at the first failure has already run every other
 test; it also passes alone in a fresh process.
 """
@@ -59,10 +61,17 @@ def test_noalloc_matches_workspace_entry_point(sdv, bits, n, k, S):
         sdv.sdv_verify_head_noalloc(head, xt, S, dt, S - 1, lg_b, am_b, acc_b, nx_b)
         assert sdv.sdv_noalloc_device_status() == sdv.SDV_OK
         assert sdv.sdv_last_device_status(ws) == sdv.SDV_OK
-        # the same kernel and plan: the two entry points agree exactly
-        np.testing.assert_array_equal(lg_b.cpu().numpy(), lg_a.cpu().numpy())
-        np.testing.assert_array_equal(am_b.cpu().numpy(), am_a.cpu().numpy())
-        assert (int(acc_b.item()), int(nx_b.item())) == (int(acc_a.item()), int(nx_a.item()))
+        if S <= 16 or bits == 4:
+            # the same kernel and plan: the two entry points agree exactly
+            np.testing.assert_array_equal(lg_b.cpu().numpy(), lg_a.cpu().numpy())
+            np.testing.assert_array_equal(am_b.cpu().numpy(), am_a.cpu().numpy())
+            assert (int(acc_b.item()), int(nx_b.item())) == (int(acc_a.item()), int(nx_a.item()))
+        else:
+            # int8 with k = 2560 at S = 17: the workspace entry point splits the
+            # reduction, the fixed scratch runs row chunks: agreement within the
+            # parity tolerance, ids exact where the oracle's gap allows
+            assert_gemm_close(lg_b.cpu().numpy(), lg_a.cpu().numpy(), k, f"call {call} logits, the two forms")
+            check_head_outputs(ref, am_a.cpu().numpy(), int(acc_a.item()), int(nx_a.item()))
         # and both match the oracle under the parity rules
         assert_gemm_close(lg_b.cpu().numpy(), ref["logits"], k, f"call {call} logits")
         check_head_outputs(ref, am_b.cpu().numpy(), int(acc_b.item()), int(nx_b.item()))
