@@ -663,7 +663,7 @@ def run_sdv(args, wl, S, world, rank, local):
 
     build.build()
     sdv.load()
-    sdv.sdv_set_gemm_path({"auto": 0, "mma": 1, "tc": 2}[args.path])
+    sdv.sdv_set_gemm_path({"auto": 0, "mma": 1, "tc": 2, "gemv": 3}[args.path])
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     nwin = min(wl.windows, max(1, args.windows))
@@ -863,8 +863,8 @@ def main(argv=None):
     ap.add_argument("--S", type=int, default=0)
     ap.add_argument("--windows", type=int, default=200)
     ap.add_argument("--cpu-budget", type=float, default=10.0)
-    ap.add_argument("--path", choices=["auto", "mma", "tc"], default="auto",
-                    help="GEMM implementation (auto: tcgen05 where its plan fits)")
+    ap.add_argument("--path", choices=["auto", "mma", "tc", "gemv"], default="auto",
+                    help="GEMM implementation (auto: tcgen05 where its plan fits; gemv: CUDA cores for S <= 2)")
     ap.add_argument("--verify", choices=["greedy", "sample"], default="greedy",
                     help="head workloads: greedy verify (sdv_verify_head) or sampling verify at T = 1")
     ap.add_argument("--sweep-S", default="", help="comma-separated window sizes: verify-head time per S")

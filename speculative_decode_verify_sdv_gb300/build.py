@@ -24,7 +24,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libsdv.so")
 
-SOURCES = ["api.cu", "dq_gemm.cu", "tc_gemm.cu", "small_kernels.cu", "moe_kernels.cu", "noalloc.cu",
+SOURCES = ["api.cu", "dq_gemm.cu", "tc_gemm.cu", "gemv.cu", "small_kernels.cu", "moe_kernels.cu", "noalloc.cu",
            "ngram_drafter.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",

@@ -162,7 +162,8 @@ GemmPlan plan_gemm(int qbits, int n, int k, int S, bool allow_split) {
 }
 
 // GEMM implementation: 0 = choose (tcgen05 when its plan fits), 1 = the
-// mma.sync path, 2 = the tcgen05 path only.
+// mma.sync path, 2 = the tcgen05 path only, 3 = the CUDA-core GEMV for windows
+// of one or two rows (else as 0).
 std::atomic<int> g_gemm_path{0};
 
 // Timeout-path test hooks (sdv_debug_fault): applied to every tcgen05 launch.
@@ -230,7 +231,7 @@ GemmPlan choose_plan(int qbits, int n, int k, int S, bool allow_split) {
     return path == 1 ? GemmPlan{} : plan_tc(qbits, n, k, S, allow_split);
   if (path != 1) {
     const GemmPlan t = plan_tc(qbits, n, k, S, allow_split);
-    if (t.splits != 0 || path >= 2) return t;
+    if (t.splits != 0 || path == 2) return t;
   }
   return plan_gemm(qbits, n, k, S, allow_split);
 }
@@ -238,6 +239,25 @@ GemmPlan choose_plan(int qbits, int n, int k, int S, bool allow_split) {
 size_t head_ws_bytes(int S) {
   const int sms = device_sms();
   return kWsHeader + (size_t)(sms > 0 ? sms : 1024) * (size_t)S * 8;
+}
+
+size_t align256(size_t b) { return (b + 255) / 256 * 256; }
+
+// Verify head whose window rows fit the tcgen05 plan only with the reduction
+// split (e.g. k = 2560 at S >= 17): plan of the split pass (splits >= 2), or
+// splits == 0 where the whole-window plan fits or no split plan does.
+GemmPlan plan_head_split(int qbits, int n, int k, int S) {
+  if (S < 2 || g_gemm_path.load() == 1) return GemmPlan{};
+  if (plan_tc(qbits, n, k, S, false).splits != 0) return GemmPlan{};
+  const GemmPlan pl = plan_tc(qbits, n, k, S, true);
+  return pl.splits >= 2 ? pl : GemmPlan{};
+}
+
+// Its workspace: header, fp32 partial logits [splits][S][n], then the tail's
+// per-CTA (max, index) partials [grid][S] of each kind.
+size_t head_split_ws_bytes(const GemmPlan& pl, int n, int S) {
+  const int grid = sdv::head_splitsum_grid(n, device_sms());
+  return kWsHeader + align256((size_t)pl.splits * S * n * sizeof(float)) + align256((size_t)grid * S * 4) * 2;
 }
 
 // [grid][S][8] floats of per-CTA sampling partials behind the header
@@ -264,6 +284,25 @@ size_t qlinear_ws_bytes(int qbits, int n, int k, int S) {
 sdv_status run_gemm(const sdv_qweight* w, const uint16_t* x, int S, int mode, GemmArgs& a, void* ws,
                     size_t ws_bytes, float* y_final, cudaStream_t st, char* part_area = nullptr,
                     size_t part_bytes = 0) {
+  if (g_gemm_path.load() == 3 && (mode == sdv::kModeY || mode == sdv::kModeHead)) {
+    const int g = sdv::gemv_plan(w->qtype, w->k, S);
+    const int sms = device_sms();
+    if (g > 0 && sms > 0) {
+      // the CUDA-core GEMV: one pass, no split; head partials as for the GEMM
+      a.codes = w->codes;
+      a.x = reinterpret_cast<const __half*>(x);
+      a.scales = w->scales;
+      a.S = S;
+      a.N = w->n;
+      a.K = w->k;
+      a.status = static_cast<int*>(ws);
+      a.ticket = reinterpret_cast<unsigned*>(static_cast<char*>(ws) + 4);
+      if (mode == sdv::kModeY) a.y = y_final;
+      a.part_v = reinterpret_cast<float*>(static_cast<char*>(ws) + kWsHeader);
+      a.part_i = reinterpret_cast<int*>(static_cast<char*>(ws) + kWsHeader + (size_t)sms * S * 4);
+      return cuda_status(sdv::launch_gemv(w->qtype, mode, a, g, sms, st));
+    }
+  }
   const GemmPlan pl = choose_plan(w->qtype, w->n, w->k, S, mode == sdv::kModeY);
   if (pl.splits == 0) return SDV_ERR_UNSUPPORTED;
   if (mode == sdv::kModeHead) {
@@ -350,8 +389,6 @@ sdv_status launch_tc_y(const sdv_qweight* w, const sdv_qweight* w2, const GemmPl
   apply_debug(a);
   return cuda_status(sdv::launch_tc_gemm(w->qtype, sdv::kModeY, tc, tsc, tc2, tsc2, a, pl.grid, pl.smem, st));
 }
-
-size_t align256(size_t b) { return (b + 255) / 256 * 256; }
 
 // Fused SwiGLU gate/up: one tcgen05 launch over both matrices (dual tiles,
 // split-K when the window rows of the full reduction do not fit), fp32 partials
@@ -461,7 +498,7 @@ sdv_status sdv_debug_fault(int32_t withhold_stage, uint64_t wait_limit_ns) {
 }
 
 int32_t sdv_set_gemm_path(int32_t path) {
-  if (path < 0 || path > 2) return -1;
+  if (path < 0 || path > 3) return -1;
   return g_gemm_path.exchange(path);
 }
 
@@ -490,7 +527,17 @@ size_t sdv_workspace_bytes(int32_t op, int32_t n, int32_t k, int32_t S, int32_t 
       const size_t a = swiglu_ws_bytes(8, n, k, S), b = swiglu_ws_bytes(4, n, k, S);
       return a > b ? a : b;
     }
-    case SDV_OP_VERIFY_HEAD: return head_ws_bytes(S);
+    case SDV_OP_VERIFY_HEAD: {  // the larger of the weight types' split plans, if any
+      size_t b = head_ws_bytes(S);
+      for (int q : {8, 4}) {
+        const GemmPlan pl = plan_head_split(q, n, k, S);
+        if (pl.splits >= 2) {
+          const size_t bs = head_split_ws_bytes(pl, n, S);
+          if (bs > b) b = bs;
+        }
+      }
+      return b;
+    }
     case SDV_OP_VERIFY_SAMPLE: return sample_ws_bytes(S);
     case SDV_OP_MOE: {  // n = I, k = H
       if (E < 1 || top_k < 1 || top_k > E) return 0;
@@ -577,9 +624,37 @@ sdv_status sdv_verify_head(const sdv_qweight* head, const uint16_t* x, int32_t S
   if (S > kMaxS) return SDV_ERR_UNSUPPORTED;
   if (n_valid < 0 || n_valid > S - 1) return SDV_ERR_INVALID_ARG;
   if (n_valid > 0 && drafts == nullptr) return SDV_ERR_INVALID_ARG;
-  const size_t need = sdv_workspace_bytes(SDV_OP_VERIFY_HEAD, head->n, head->k, S, 0, 0);
-  if (ws == nullptr || !aligned16(ws) || ws_bytes < need) return SDV_ERR_WORKSPACE;
+  // the least a head call needs (the row-chunked form below); the split form
+  // needs more and runs when the workspace is large enough for it
+  if (ws == nullptr || !aligned16(ws) || ws_bytes < head_ws_bytes(S)) return SDV_ERR_WORKSPACE;
   const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  {
+    // The window rows of a long reduction may not fit one tcgen05 launch next
+    // to its ring.  Then each CTA takes half (or a smaller share) of the
+    // reduction, whose rows fit: one pass over the head writes fp32 partial
+    // logits (a few % of the weight bytes), and the split-sum tail adds them in
+    // order, takes the argmax and runs the accept.
+    const GemmPlan sp = plan_head_split(head->qtype, head->n, head->k, S);
+    if (sp.splits >= 2 && ws_bytes >= head_split_ws_bytes(sp, head->n, S)) {
+      char* const w8 = static_cast<char*>(ws);
+      float* const part = reinterpret_cast<float*>(w8 + kWsHeader);
+      const int grid = sdv::head_splitsum_grid(head->n, device_sms());
+      const size_t pbytes = align256((size_t)sp.splits * S * head->n * sizeof(float));
+      float* const pv = reinterpret_cast<float*>(w8 + kWsHeader + pbytes);
+      int* const pi = reinterpret_cast<int*>(w8 + kWsHeader + pbytes + align256((size_t)grid * S * 4));
+      GemmArgs a{};
+      a.x = reinterpret_cast<const __half*>(x);
+      a.S = S;
+      a.N = head->n;
+      a.K = head->k;
+      a.y = part;
+      sdv_status s = launch_tc_y(head, nullptr, sp, a, ws, st);
+      if (s != SDV_OK) return s;
+      return cuda_status(sdv::launch_head_splitsum(part, sp.splits, S, head->n, logits_or_null, pv, pi, drafts,
+                                                   n_valid, argmax, accepted, next_a0,
+                                                   reinterpret_cast<unsigned*>(w8 + 4), grid, st));
+    }
+  }
   GemmArgs a{};
   a.y = logits_or_null;
   a.drafts = drafts;

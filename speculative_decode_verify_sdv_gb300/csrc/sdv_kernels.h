@@ -36,6 +36,7 @@ constexpr int kModeHead = 1;  // verify head: argmax partials + last-CTA reduce 
 constexpr int kModeSample = 2;  // sampling verify: Gumbel-max draws + softmax partials + last-CTA accept
 
 struct GemmArgs {
+  const void* codes;        // weight codes (read directly by the CUDA-core GEMV)
   const __half* x;          // fp16 [S][K]
   const uint16_t* scales;   // fp16 [N][K/32] (read directly when scales_tma == 0)
   int S, N, K;              // window rows, weight rows, reduction length
@@ -101,6 +102,10 @@ cudaError_t launch_tc_gemm(int qbits, int mode, const CUtensorMap& tm_codes,
                            const CUtensorMap& tm_scales2, const GemmArgs& a, int grid, int smem,
                            cudaStream_t st);
 
+// CUDA-core GEMV for S <= 2: warps per row (0 = not covered), one CTA per SM.
+int gemv_plan(int qbits, int k, int S);
+cudaError_t launch_gemv(int qbits, int mode, const GemmArgs& a, int warps_per_row, int grid, cudaStream_t st);
+
 cudaError_t launch_splitk_reduce(const float* part, int splits, long count, float* y, cudaStream_t st);
 
 // h[s][c] = fp16(SiLU(g) * u [* row_w[s][c / seg]]) for c < n (or c < *n_dev * seg
@@ -121,6 +126,13 @@ cudaError_t launch_quantize(const float* w, int n, int k, int qbits, void* codes
                             cudaStream_t st);
 cudaError_t launch_tree_accept(const int32_t* argmax, int S, const int32_t* tokens, const int32_t* parent,
                                int32_t* path, int32_t* accepted, int32_t* next_a0, cudaStream_t st);
+// The split-reduction head's tail: logits = sum over splits of part[split][s][v]
+// (written when logits is not null), argmax per row, accept; grid CTAs of per-row
+// partials part_v/part_i [grid][S]; the last CTA resets *ticket.
+int head_splitsum_grid(int n, int sms);
+cudaError_t launch_head_splitsum(const float* part, int splits, int S, int n, float* logits, float* part_v,
+                                 int* part_i, const int32_t* drafts, int n_valid, int32_t* argmax, int32_t* accepted,
+                                 int32_t* next_a0, unsigned* ticket, int grid, cudaStream_t st);
 cudaError_t launch_greedy_accept(const int32_t* argmax, int S, const int32_t* drafts, int n_valid,
                                  int32_t* accepted, int32_t* next_a0, cudaStream_t st);
 

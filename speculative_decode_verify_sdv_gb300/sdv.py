@@ -126,11 +126,12 @@ def sdv_version() -> int:
     return int(load().sdv_version())
 
 
-SDV_PATH_AUTO, SDV_PATH_MMA_SYNC, SDV_PATH_TCGEN05 = 0, 1, 2
+SDV_PATH_AUTO, SDV_PATH_MMA_SYNC, SDV_PATH_TCGEN05, SDV_PATH_GEMV = 0, 1, 2, 3
 
 
 def sdv_set_gemm_path(path: int) -> int:
-    """Select the GEMM implementation (0 auto, 1 mma.sync, 2 tcgen05); returns the previous one."""
+    """Select the GEMM implementation (0 auto, 1 mma.sync, 2 tcgen05, 3 CUDA-core GEMV for S <= 2);
+    returns the previous one."""
     prev = int(load().sdv_set_gemm_path(path))
     if prev < 0:
         raise ValueError(f"invalid GEMM path {path}")

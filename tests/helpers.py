@@ -76,7 +76,7 @@ def check_head_outputs(ref: dict, am: np.ndarray, acc: int, nxt: int):
     return int(elig.sum())
 
 
-PATHS = {"mma": 1, "tc": 2}
+PATHS = {"mma": 1, "tc": 2, "gemv": 3}
 
 
 class gemm_path:

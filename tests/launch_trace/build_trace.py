@@ -17,7 +17,7 @@ ROOT = os.path.dirname(os.path.dirname(HERE))
 CSRC = os.path.join(ROOT, "speculative_decode_verify_sdv_gb300", "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 OUT = os.path.join(ROOT, "_build", "launch_trace")
-SOURCES = ["api.cu", "dq_gemm.cu", "tc_gemm.cu", "small_kernels.cu", "moe_kernels.cu", "noalloc.cu"]
+SOURCES = ["api.cu", "dq_gemm.cu", "tc_gemm.cu", "gemv.cu", "small_kernels.cu", "moe_kernels.cu", "noalloc.cu"]
 HOST = ["stub_runtime.cpp", "trace_main.cpp"]
 
 

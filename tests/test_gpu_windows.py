@@ -4,7 +4,7 @@ test_gpu_verify_head.py).
 
 * Verify heads -- the Qwen3-4B-shaped head (151936 x 2560 int8, S = 9) and the
   35B-A3B-shaped head (248320 x 2048 int4, S = 1, 2, 9, 17), 200 windows each,
-  on both GEMM implementations.  Every window: argmax bit-exact on every row
+  on both tensor-core implementations (and on the CUDA-core GEMV at S = 1, 2).  Every window: argmax bit-exact on every row
   whose oracle top-2 gap exceeds 1e-2, accepted and next_a0 bit-exact when
   every row the accept scan read is eligible, the window's drafts rebuilt from
   the oracle's argmax chain by the seeded draft rule.  The oracle's per-window
@@ -76,8 +76,9 @@ def _head(sdv, wl):
     return _HEADS[wl.name]
 
 
-HEAD_CASES = [(name, S, p) for name, s_list in (("q4b", (9,)), ("a3b", (1, 2, 9, 17)))
-              for S in s_list for p in ("tc", "mma")]
+HEAD_CASES = ([(name, S, p) for name, s_list in (("q4b", (9,)), ("a3b", (1, 2, 9, 17)))
+               for S in s_list for p in ("tc", "mma")]
+              + [("a3b", 1, "gemv"), ("a3b", 2, "gemv")])
 
 
 @pytest.mark.parametrize("name,S,path_name", HEAD_CASES)
