@@ -84,7 +84,7 @@ def test_a3b_head_plan(tracer, qt):
 
 
 def test_mlp27_plans(tracer):
-    # profiles/mlp_moe_s17_launches.md: gate/up 4 splits x 38 CTAs + SwiGLU reduce,
+    # profiles/tc_gemm_mlp27_s17.md: gate/up 4 splits x 38 CTAs + SwiGLU reduce,
     # down 14 splits x 10 CTAs + split-K sum
     sw, dn = trace(tracer, "swiglu 8 17408 5120 17", "qlinear 8 5120 17408 17")
     assert [grid(l) for l in sw["launches"][:1]] == [(38, 4)] and "swiglu_reduce" in sw["launches"][1]["name"]
@@ -94,7 +94,7 @@ def test_mlp27_plans(tracer):
 
 
 def test_moe_plan(tracer):
-    # profiles/mlp_moe_s17_launches.md: route (one block), gate/up over the hit list
+    # profiles/moe_s17_launches.md: route (one block), gate/up over the hit list
     # with the SwiGLU epilogue, down over 38 expert-segment slots x 4 CTAs, split sum
     (c,) = trace(tracer, "moe 4 256 512 2048 8 17")
     route, gu, dn, red = c["launches"]
