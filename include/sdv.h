@@ -392,6 +392,13 @@ SDV_API int32_t sdv_set_gemm_path(int32_t path);
  */
 SDV_API sdv_status sdv_debug_fault(int32_t withhold_stage, uint64_t wait_limit_ns);
 
+/*
+ * Number of kernels this library has launched in this process (every device
+ * and stream, counted when the launch is issued); the difference of two reads
+ * brackets a region.  For measurement; the pages have no counterpart.
+ */
+SDV_API uint64_t sdv_launch_count(void);
+
 /* A static, human-readable name of a status code. */
 SDV_API const char* sdv_status_string(sdv_status status);
 

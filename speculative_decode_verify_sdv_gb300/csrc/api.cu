@@ -169,6 +169,7 @@ std::atomic<int> g_gemm_path{0};
 // Timeout-path test hooks (sdv_debug_fault): applied to every tcgen05 launch.
 std::atomic<unsigned long long> g_debug_wait_ns{0};
 std::atomic<int> g_debug_withhold{0};
+std::atomic<uint64_t> g_launches{0};  // kernels launched by this library (sdv_launch_count)
 
 void apply_debug(GemmArgs& a) {
   a.wait_ns = g_debug_wait_ns.load();
@@ -486,6 +487,10 @@ bool moe_args_ok(const sdv_qweight* gate, const sdv_qweight* up, const sdv_qweig
 
 }  // namespace
 
+namespace sdv {
+void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+}  // namespace sdv
+
 extern "C" {
 
 int32_t sdv_version(void) { return 100; }
@@ -496,6 +501,8 @@ sdv_status sdv_debug_fault(int32_t withhold_stage, uint64_t wait_limit_ns) {
   g_debug_wait_ns.store(wait_limit_ns);
   return SDV_OK;
 }
+
+uint64_t sdv_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 
 int32_t sdv_set_gemm_path(int32_t path) {
   if (path < 0 || path > 3) return -1;

@@ -434,7 +434,7 @@ cudaError_t launch_t(const CUtensorMap& tc, const CUtensorMap& tsc, const GemmAr
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   k<<<dim3(grid, a.splits), kWarps * 32, smem, st>>>(tc, tsc, a);
-  return cudaGetLastError();
+  return counted(cudaGetLastError());
 }
 
 template <int QB, int MT, int MODE>

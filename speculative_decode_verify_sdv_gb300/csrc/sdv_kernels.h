@@ -8,6 +8,14 @@
 
 namespace sdv {
 
+// Counts one kernel launch of this library (process-wide; read through
+// sdv_launch_count).  Every launch site calls it once its launch succeeded.
+void count_launch();
+inline cudaError_t counted(cudaError_t e) {
+  if (e == cudaSuccess) count_launch();
+  return e;
+}
+
 // Launch with programmatic stream serialisation: the kernel may be scheduled
 // while the previous kernel in the stream drains, and must call
 // griddepcontrol.wait before reading anything that kernel wrote.
@@ -24,7 +32,7 @@ cudaError_t launch_pdl(void (*kernel)(Params...), dim3 grid, dim3 block, size_t 
   cfg.stream = st;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
+  return counted(cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...));
 }
 
 // Device status word bits (first word of every workspace).

@@ -248,7 +248,7 @@ cudaError_t launch_head_splitsum(const float* part, int splits, int S, int n, fl
 cudaError_t launch_tree_accept(const int32_t* argmax, int S, const int32_t* tokens, const int32_t* parent,
                                int32_t* path, int32_t* accepted, int32_t* next_a0, cudaStream_t st) {
   tree_accept_kernel<<<1, 32, 0, st>>>(argmax, S, tokens, parent, path, accepted, next_a0);
-  return cudaGetLastError();
+  return counted(cudaGetLastError());
 }
 
 cudaError_t launch_quantize(const float* w, int n, int k, int qbits, void* codes, uint16_t* scales,
@@ -266,14 +266,14 @@ cudaError_t launch_quantize(const float* w, int n, int k, int qbits, void* codes
   else
     quantize_block32_kernel<4><<<(unsigned)grid, threads, 0, st>>>(
         w, nblocks, k, static_cast<uint8_t*>(codes), reinterpret_cast<__half*>(scales));
-  return cudaGetLastError();
+  return counted(cudaGetLastError());
 }
 
 cudaError_t launch_greedy_accept(const int32_t* argmax, int S, const int32_t* drafts, int n_valid,
                                  int32_t* accepted, int32_t* next_a0, cudaStream_t st) {
   (void)S;
   greedy_accept_kernel<<<1, 32, 0, st>>>(argmax, drafts, n_valid, accepted, next_a0);
-  return cudaGetLastError();
+  return counted(cudaGetLastError());
 }
 
 }  // namespace sdv

@@ -22,7 +22,7 @@ SDV_OP_QLINEAR, SDV_OP_QLINEAR_SWIGLU, SDV_OP_VERIFY_HEAD, SDV_OP_MOE, SDV_OP_VE
 EXPORTED = (
     "sdv_quantize_block32", "sdv_qlinear", "sdv_qlinear_swiglu", "sdv_verify_head",
     "sdv_greedy_accept", "sdv_moe_gather_qmm", "sdv_workspace_bytes", "sdv_workspace_init",
-    "sdv_last_device_status", "sdv_device_status", "sdv_noalloc_device_status", "sdv_status_string", "sdv_version", "sdv_verify_head_noalloc", "sdv_set_gemm_path",
+    "sdv_last_device_status", "sdv_device_status", "sdv_noalloc_device_status", "sdv_status_string", "sdv_version", "sdv_launch_count", "sdv_verify_head_noalloc", "sdv_set_gemm_path",
     "sdv_moe_route", "sdv_verify_sample", "sdv_tree_accept", "sdv_debug_fault",
     "sdv_ngram_create", "sdv_ngram_destroy", "sdv_ngram_append", "sdv_ngram_propose",
 )
@@ -71,6 +71,7 @@ def load() -> ctypes.CDLL:
         "sdv_noalloc_device_status": ([vp], i32),
         "sdv_status_string": ([i32], ctypes.c_char_p),
         "sdv_version": ([], i32),
+        "sdv_launch_count": ([], ctypes.c_uint64),
         "sdv_set_gemm_path": ([i32], i32),
         "sdv_debug_fault": ([i32, ctypes.c_uint64], i32),
         "sdv_ngram_create": ([i32, ctypes.POINTER(vp)], i32),
@@ -120,6 +121,11 @@ class QWeight:
 
     def c(self) -> sdv_qweight:
         return sdv_qweight(self.bits, self.n, self.k, _ptr(self.codes), _ptr(self.scales))
+
+
+def sdv_launch_count() -> int:
+    """Kernels the library has launched in this process (see the header)."""
+    return int(load().sdv_launch_count())
 
 
 def sdv_version() -> int:

@@ -132,10 +132,13 @@ cudaError_t cudaLaunchKernelExC(const cudaLaunchConfig_t* c, const void* fn, voi
   if (name.find("tc_gemm_kernel") != std::string::npos) {
     const sdv::GemmArgs& a = *static_cast<const sdv::GemmArgs*>(args[4]);
     std::printf(" S=%d N=%d K=%d k_chunk=%d splits=%d depth=%d scales_tma=%d n_valid=%d dual=%d seg_k=%d"
-                " rows_per_expert=%d y=%llx h=%llx part_v=%llx part_s=%llx",
+                " rows_per_expert=%d y=%llx h=%llx part_v=%llx part_s=%llx x=%llx",
                 a.S, a.N, a.K, a.k_chunk, a.splits, a.depth, a.scales_tma, a.n_valid, a.dual, a.seg_k,
-                a.rows_per_expert, low(a.y), low(a.h), low(a.part_v), low(a.part_s));
+                a.rows_per_expert, low(a.y), low(a.h), low(a.part_v), low(a.part_s), low(a.x));
   }
+  if (name.find("splitk_reduce_kernel") != std::string::npos ||
+      name.find("swiglu_reduce_kernel") != std::string::npos)  // first argument: the partials
+    std::printf(" part=%llx", low(*static_cast<const float* const*>(args[0])));
   std::printf("\n");
   return cudaSuccess;
 }

@@ -10,6 +10,7 @@
 //   moe <qtype> <E> <I> <H> <top_k> <S>
 //   noalloc <qtype> <n> <k> <S> <n_valid>
 //   ws <op> <n> <k> <S> <E> <top_k>
+//   count   (prints sdv_launch_count())
 // Output: "call <command>", the call's trace lines, then "status <code>" (or
 // "ws bytes=<n>").  Pointers are distinct 16-byte-aligned addresses that are
 // never dereferenced.
@@ -90,6 +91,8 @@ int main() {
     } else if (c == "noalloc") {
       const sdv_qweight w = weight(a[0], a[1], a[2], 0x1000);
       st = sdv_verify_head_noalloc(&w, X, a[3], DRAFTS, a[4], nullptr, ARGMAX, ACCEPTED, NEXT, nullptr);
+    } else if (c == "count") {  // the library's own launch counter
+      std::printf("count n=%llu\n", static_cast<unsigned long long>(sdv_launch_count()));
     } else if (c == "ws") {
       std::printf("ws bytes=%zu\n", sdv_workspace_bytes(a[0], a[1], a[2], a[3], a[4], a[5]));
       continue;

@@ -15,7 +15,7 @@ import torch
 
 from oracle import mlp, verify
 from synth import generator as G
-from tests.helpers import device_weight, gemm_path, oracle_weight, to_dev, to_dev_f16, tol
+from tests.helpers import assert_gemm_close, device_weight, gemm_path, oracle_weight, to_dev, to_dev_f16, tol
 
 pytestmark = pytest.mark.gpu
 
@@ -80,6 +80,38 @@ def _swiglu_case(sdv, bits, n, k, S, seed):
                                    (256, 96, 5), (1000, 1024, 16)])
 def test_swiglu_shapes(sdv, path, bits, n, k, S):
     _swiglu_case(sdv, bits, n, k, S, seed=n * 7 + k + S + bits)
+
+
+@pytest.mark.parametrize("op", ["swiglu", "qlinear"])
+def test_split_k_repeated_calls_one_workspace(sdv, op):
+    """Split-K plans (the partials in the workspace, then the reduce): three
+    consecutive calls on one workspace each write every output again (outputs
+    refilled with NaN between calls) and match the oracle."""
+    n, k, S = (1024, 5120, 17) if op == "swiglu" else (640, 17408, 17)
+    w = [G.normal(G.stream_seed(730, m, n, k), (n, k), 0.02) for m in range(2)]
+    q = [oracle_weight(wm, 8) for wm in w]
+    dw = [device_weight(st, sc, 8, n, k) for _, sc, st in q]
+    with gemm_path("tc"):
+        if op == "swiglu":
+            ws = sdv.workspace(sdv.SDV_OP_QLINEAR_SWIGLU, n, k, S)
+            out = torch.empty((S, n), dtype=torch.float16, device="cuda")
+        else:
+            ws = sdv.workspace(sdv.SDV_OP_QLINEAR, n, k, S)
+            out = torch.empty((S, n), dtype=torch.float32, device="cuda")
+        for call in range(3):
+            x = G.normal(G.stream_seed(731, call, n, k), (S, k), 1.0, dtype=np.float64).astype(np.float16)
+            out.fill_(float("nan"))
+            if op == "swiglu":
+                sdv.sdv_qlinear_swiglu(dw[0], dw[1], to_dev_f16(x), S, out, ws)
+            else:
+                sdv.sdv_qlinear(dw[0], to_dev_f16(x), S, out, ws)
+            assert sdv.sdv_last_device_status(ws) == sdv.SDV_OK
+            got = out.cpu().numpy().astype(np.float64)
+            g64 = verify.dequant_gemm64(x, q[0][0], q[0][1])
+            if op == "swiglu":
+                assert_swiglu_close(got, g64, verify.dequant_gemm64(x, q[1][0], q[1][1]), k, f"h, call {call}")
+            else:
+                assert_gemm_close(got, g64, k, f"y, call {call}")
 
 
 def test_swiglu_integer_exact(sdv, path):

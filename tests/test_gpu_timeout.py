@@ -105,9 +105,39 @@ def test_qlinear_split_timeout_reported_then_next_call_correct(sdv):
         with fault(sdv, 0):  # 16 splits of one 256-column stage per CTA: stage 0 is every CTA's only one
             sdv.sdv_qlinear(qw, to_dev_f16(x), S, y, ws)
         assert sdv.sdv_last_device_status(ws) == sdv.SDV_ERR_TIMEOUT
+        # every output is written again (a skipped one would stay NaN)
+        y.fill_(float("nan"))
         sdv.sdv_qlinear(qw, to_dev_f16(x), S, y, ws)
         assert sdv.sdv_last_device_status(ws) == sdv.SDV_OK
     assert_gemm_close(y.cpu().numpy(), verify.dequant_gemm64(x, codes, scales), k, "Y after a timeout")
+
+
+def test_swiglu_split_timeout_reported_then_next_calls_correct(sdv):
+    """Gate/up with split-K partials (then the SwiGLU reduce): after the
+    timeout, the next calls on the same workspace write every h value again,
+    correctly."""
+    from tests.test_gpu_mlp_moe import assert_swiglu_close
+    n, k, S = 1024, 5120, 17
+    ws = sdv.workspace(sdv.SDV_OP_QLINEAR_SWIGLU, n, k, S)
+    mats = []
+    for m in range(2):
+        w = G.normal(G.stream_seed(1220, m, n, k), (n, k), 0.02)
+        codes, scales, stored = oracle_weight(w, 8)
+        mats.append((codes, scales, device_weight(stored, scales, 8, n, k)))
+    (cg, sg, gate), (cu, su, up) = mats
+    h = torch.full((S, n), float("nan"), dtype=torch.float16, device="cuda")
+    with gemm_path("tc"):
+        x0 = G.normal(G.stream_seed(1221, n, k), (S, k), 1.0, dtype=np.float64).astype(np.float16)
+        with fault(sdv, 0):
+            sdv.sdv_qlinear_swiglu(gate, up, to_dev_f16(x0), S, h, ws)
+        assert sdv.sdv_last_device_status(ws) == sdv.SDV_ERR_TIMEOUT
+        for call in range(2):
+            x = G.normal(G.stream_seed(1222, call, n, k), (S, k), 1.0, dtype=np.float64).astype(np.float16)
+            h.fill_(float("nan"))
+            sdv.sdv_qlinear_swiglu(gate, up, to_dev_f16(x), S, h, ws)
+            assert sdv.sdv_last_device_status(ws) == sdv.SDV_OK
+            assert_swiglu_close(h.cpu().numpy().astype(np.float64), verify.dequant_gemm64(x, cg, sg),
+                                verify.dequant_gemm64(x, cu, su), k, f"h, call {call} after a timeout")
 
 
 def test_noalloc_timeout_reported_then_next_call_correct(sdv):

@@ -93,6 +93,19 @@ def test_mlp27_plans(tracer):
     assert dn["launches"][0]["k_chunk"] == "1280"
 
 
+def test_launch_counter_counts_every_launch(tracer):
+    # sdv_launch_count (the bench's gpu_launches) against the launches the
+    # stand-in runtime records, over calls that use every launch site
+    cmds = ["count", "head 8 151936 2560 9 8 0", "head 8 151936 2560 17 16 0", "sample 8 151936 2560 9 8",
+            "qlinear 8 5120 17408 17", "swiglu 8 17408 5120 17", "swiglu 8 17408 5120 1",
+            "moe 4 256 512 2048 8 17", "noalloc 8 151936 2560 17 16"]
+    calls = build_trace.run(tracer, [f"device {SMS} {SMEM}", "path 0", *cmds, "path 1", "qlinear 8 5120 17408 17",
+                                     "swiglu 8 17408 5120 17", "count"])
+    counts = [int(c["other"][0].split("=")[1]) for c in calls if c["cmd"] == "count"]
+    launched = sum(len(c["launches"]) for c in calls if c["cmd"] != "count")
+    assert len(counts) == 2 and counts[1] - counts[0] == launched and launched > 10
+
+
 def test_moe_plan(tracer):
     # profiles/moe_s17_launches.md: route (one block), gate/up over the hit list
     # with the SwiGLU epilogue, down over 38 expert-segment slots x 4 CTAs, split sum
