@@ -138,7 +138,6 @@ __global__ void __launch_bounds__(kSplitSumThreads) head_splitsum_kernel(
     const int32_t* __restrict__ drafts, int n_valid, int32_t* argmax, int32_t* accepted, int32_t* next_a0,
     unsigned* ticket) {
   griddep_wait();
-  griddep_launch_dependents();
   __shared__ float s_v[kSplitSumThreads / 32][32];
   __shared__ int s_i[kSplitSumThreads / 32][32];
   __shared__ int s_am[32], s_dr[32], s_flag;
@@ -189,6 +188,10 @@ __global__ void __launch_bounds__(kSplitSumThreads) head_splitsum_kernel(
     __stcg(part_v + (long)blockIdx.x * S + s, v);
     __stcg(part_i + (long)blockIdx.x * S + s, i);
   }
+  // The next kernel in the stream may launch once every block is past its
+  // share of the sum: triggered earlier, its CTAs (which wait for this grid to
+  // complete) would take SMs that blocks of this grid have yet to run on.
+  griddep_launch_dependents();
   __syncthreads();
   if (threadIdx.x == 0) {
     // publishes this CTA's partials (cumulative over the block's stores before the
