@@ -730,8 +730,13 @@ __global__ void __launch_bounds__(TcRoles<(QT == 8 ? 8 : 4)>::kThreads, 1)
     const int r = 32 * q + lane;  // row within the tile (= TMEM lane)
     const uint32_t lane_base = (uint32_t)(32 * q) << 16;
     const int ks_per_row = p.K / 32;
-    constexpr int kHalves = (QB == 8) ? 2 : 1;   // 128-byte code loads per row and stage
-    constexpr int kHalfBlocks = 8 / kHalves;     // 32-blocks per load
+    // A row's codes of a stage are loaded in parts of kHalfBlocks blocks: int8
+    // two halves (a 128-byte row of each half of the stage); int4 two halves of
+    // its 128-byte row (fewer registers held by the codes); FP4 the whole row at
+    // once (measured faster for its shorter conversion).
+    constexpr int kHalves = (QT == 2) ? 1 : 2;
+    constexpr int kHalfBlocks = 8 / kHalves;               // 32-blocks per part
+    constexpr int kLoads = (QB == 8) ? 8 : kHalfBlocks;    // 16-byte loads per part
     const int sw = r & 7;
     Cursor c = cursor_at(0);
     for (int j = 0; j < g; ++j) advance(c);
@@ -744,38 +749,37 @@ __global__ void __launch_bounds__(TcRoles<(QT == 8 ? 8 : 4)>::kThreads, 1)
       if (c.i >= kABufs) ok = wait_warp(bar_afree + 8 * ab, c.abphase ^ 1);
       if (ok) ok = wait_warp(bar_full + 8 * slot, c.phase);
       const uint8_t* const cb = sb + pl.ring_off + slot * pl.code_stage;
-      // the 8 block scales of row r; blocks past the reduction length get zero, so
-      // their A columns are zero (the padded window rows are zero too)
-      uint32_t sc_h[8];
-#pragma unroll
-      for (int blk = 0; blk < 8; ++blk) sc_h[blk] = 0u;
+      // the 8 block scales of row r, two per word (block 2j in the low half);
+      // blocks past the reduction length get zero, so their A columns are zero
+      // (the padded window rows are zero too)
+      uint32_t sc_w[4] = {0u, 0u, 0u, 0u};
       if (ok) {
         if (p.scales_tma) {
           const uint4 sv = *reinterpret_cast<const uint4*>(sb + pl.sc_off + slot * pl.sc_stage + r * 16);
-          const uint32_t w4[4] = {sv.x, sv.y, sv.z, sv.w};
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            sc_h[2 * j] = w4[j] & 0xFFFFu;
-            sc_h[2 * j + 1] = w4[j] >> 16;
-          }
+          sc_w[0] = sv.x;
+          sc_w[1] = sv.y;
+          sc_w[2] = sv.z;
+          sc_w[3] = sv.w;
         } else {
           const int row = (tile_lo + c.t) * kTileRows + r;
           const int ks = c.kx;
 #pragma unroll
           for (int blk = 0; blk < 8; ++blk)
-            sc_h[blk] = (blk < nb && row < p.N)
-                            ? (uint32_t)__ldg(p.scales + (size_t)row * ks_per_row + k_begin / 32 + ks * 8 + blk)
-                            : 0u;
+            if (blk < nb && row < p.N)
+              sc_w[blk >> 1] |= (uint32_t)__ldg(p.scales + (size_t)row * ks_per_row + k_begin / 32 + ks * 8 + blk)
+                                << (16 * (blk & 1));
         }
       }
 #pragma unroll
       for (int h = 0; h < kHalves; ++h) {
-        // 128 code bytes of row r (int8: half h of the stage; int4: the whole stage)
-        uint4 wreg[8];
+        uint4 wreg[kLoads];
         if (ok) {
-          const uint8_t* const row_p = cb + h * kTileRows * 128 + r * 128;
+          const uint8_t* const row_p = cb + (QB == 8 ? h * kTileRows * 128 : 0) + r * 128;
 #pragma unroll
-          for (int w = 0; w < 8; ++w) wreg[w] = *reinterpret_cast<const uint4*>(row_p + ((w ^ sw) << 4));
+          for (int w = 0; w < kLoads; ++w) {
+            const int chunk = (QB == 8) ? w : kLoads * h + w;
+            wreg[w] = *reinterpret_cast<const uint4*>(row_p + ((chunk ^ sw) << 4));
+          }
         }
         if (h == kHalves - 1) {  // the ring slot goes back to the producer
           __syncwarp();
@@ -786,7 +790,8 @@ __global__ void __launch_bounds__(TcRoles<(QT == 8 ? 8 : 4)>::kThreads, 1)
 #pragma unroll
           for (int blk = 0; blk < kHalfBlocks; ++blk) {
             const int sblk = h * kHalfBlocks + blk;  // block within the stage
-            const __half2 s2 = u32_as_h2(sc_h[sblk] | (sc_h[sblk] << 16));
+            // the block's scale in both halves of a pair: one byte permute
+            const __half2 s2 = u32_as_h2(__byte_perm(sc_w[sblk >> 1], 0u, (sblk & 1) ? 0x3232u : 0x1010u));
             uint32_t cols[16];
             if (QB == 8) {
               const uint32_t wv[8] = {wreg[2 * blk].x, wreg[2 * blk].y, wreg[2 * blk].z, wreg[2 * blk].w,
