@@ -603,13 +603,19 @@ __global__ void __launch_bounds__(TcRoles<(QT == 8 ? 8 : 4)>::kThreads, 1)
           for (int n = 0; n < 32; ++n)
             if (n < p.S) red[n * 33 + lane] = acc[n];
         } else if (valid) {
+          // the routing weights of this tile's expert slot (written by the router
+          // before this grid started): all loaded before the first store of h,
+          // which the compiler could not otherwise move them past
           const float* const rw = (p.row_w != nullptr) ? p.row_w + lt / tpe : nullptr;
+          float wv[32];
+#pragma unroll
+          for (int n = 0; n < 32; ++n) wv[n] = (rw != nullptr && n < p.S) ? __ldg(rw + (size_t)n * p.ldw) : 1.f;
 #pragma unroll
           for (int n = 0; n < 32; ++n) {
             if (n < p.S) {
               const float g = red[n * 33 + lane];
               float v = g / (1.f + expf(-g)) * acc[n];
-              if (rw != nullptr) v *= rw[(size_t)n * p.ldw];
+              if (rw != nullptr) v *= wv[n];
               p.h[(size_t)n * p.ldh + lrow] = __float2half_rn(v);
             }
           }
