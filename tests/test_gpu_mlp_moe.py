@@ -114,6 +114,15 @@ def test_split_k_repeated_calls_one_workspace(sdv, op):
                 assert_gemm_close(got, g64, k, f"y, call {call}")
 
 
+@pytest.mark.parametrize("bits", [8, 4])
+@pytest.mark.parametrize("n,k,S", [(3000, 3328, 9), (5000, 4352, 17), (7000, 4352, 9), (3000, 5376, 17)])
+def test_swiglu_uneven_splits_ragged_rows(sdv, path, bits, n, k, S):
+    """Split gate/up plans whose last reduction split is shorter than the others,
+    whose tiles do not divide evenly over the CTAs, and whose last tile of rows
+    is ragged."""
+    _swiglu_case(sdv, bits, n, k, S, seed=n + k + S + bits)
+
+
 def test_swiglu_integer_exact(sdv, path):
     """Scales 1 and small integer x: g and u are exact integers on both sides,
     so h differs from the oracle's fp16 at most by the last-bit of an fp32
