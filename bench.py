@@ -654,6 +654,82 @@ class MoeJob:
 JOBS = {"head": HeadJob, "mlp": MlpJob, "moe": MoeJob}
 
 
+def timed_region(job, steps, world, local, sdv, torch):
+    """K back-to-back windows between two events on the launching stream, with
+    the clocks sampled during the region and this library's kernel launches
+    counted.  A window's GEMM is a programmatic dependent launch, so its start-up
+    overlaps the previous window's tail; an event between windows would
+    serialise them, so the per-launch duration is the region / K.
+    Returns (region ms, launches, the clock sampler)."""
+    stream = torch.cuda.current_stream()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        n0 = sdv.sdv_launch_count()
+        t0.record(stream)
+        for i in range(steps):
+            job.step(i)
+        t1.record(stream)
+        n_launched = sdv.sdv_launch_count() - n0
+        torch.cuda.synchronize()
+    barrier(world)
+    return t0.elapsed_time(t1), n_launched, clk
+
+
+# The other full-size workloads a default single-GPU run measures beside the
+# headline one (name:S), so that one driver run records every config's number
+# with its own clocks: the int4 head at the window the pages' cliff is quoted on
+# and at one row, the dense MLP stack and the MoE layer.
+ALSO_DEFAULT = "a3b:17,a3b:1,mlp27:17,moe:17"
+
+
+def also_specs(args, world) -> list:
+    """(workload, S) pairs of --also: "auto" is ALSO_DEFAULT on the default
+    single-GPU run (q4b greedy, integer weights) and nothing otherwise."""
+    spec = args.also
+    if spec == "auto":
+        default_run = args.config == "q4b" and not args.fp4 and args.verify == "greedy" and args.path == "auto"
+        spec = ALSO_DEFAULT if (default_run and world == 1) else ""
+    out = []
+    for item in filter(None, (t.strip() for t in spec.split(","))):
+        if item == "none":
+            return []
+        name, _, s = item.partition(":")
+        if name not in W.BY_NAME:
+            raise SystemExit(f"--also: unknown workload {name!r}")
+        wl = W.BY_NAME[name]
+        out.append((wl, int(s) if s else wl.s_default))
+    return out
+
+
+def measure_also(args, specs, sdv, torch, dev, local) -> list:
+    """Each (workload, S): warm-up, the timed region (as the headline line),
+    a status check; one compact record per workload."""
+    peak, kind = measured_peak()
+    out = []
+    for wl, S in specs:
+        nwin = min(wl.windows, max(1, args.windows))
+        job = JOBS[wl.kind](sdv, torch, wl, S, dev, nwin)
+        for i in range(args.warmup):
+            job.step(i)
+        torch.cuda.synchronize()
+        ms, n_launched, clk = timed_region(job, args.steps, 1, local, sdv, torch)
+        if not all(sdv.sdv_last_device_status(w) == sdv.SDV_OK for w in job.ws_list):
+            raise RuntimeError(f"device status reported an error measuring {wl.name} S={S}")
+        nbytes = float(np.mean([job.bytes(i) for i in range(args.steps)]))
+        per = ms / args.steps
+        achieved = nbytes / (per / 1000.0) / 1e9
+        out.append({"workload": workload_name(wl, S), "S": S, "value": 1000.0 / per, "unit": "windows/s",
+                    "ms_per_step": per, "bytes_per_window": nbytes, "weight_gbs": achieved,
+                    "hbm_frac": achieved / peak, "peak_kind": kind, "gpu_launches": n_launched,
+                    "kernel": f"{job.kernel} ({args.path} path)", "clocks": clk.summary()})
+        del job
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+    return out
+
+
 def run_sdv(args, wl, S, world, rank, local):
     import torch
     from speculative_decode_verify_sdv_gb300 import build, sdv
@@ -677,23 +753,7 @@ def run_sdv(args, wl, S, world, rank, local):
     if not status_ok():
         raise RuntimeError("device status reported an error during warm-up")
 
-    # The timed region: K back-to-back windows between two events on the launching
-    # stream.  A window's GEMM is a programmatic dependent launch, so its start-up
-    # overlaps the previous window's tail; an event between windows would
-    # serialise them, so the per-launch duration is the region / K.
-    t_all0, t_all1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    barrier(world)
-    torch.cuda.synchronize()
-    with ClockSampler(local) as clk:
-        n_launch0 = sdv.sdv_launch_count()
-        t_all0.record(stream)
-        for i in range(args.steps):
-            job.step(i)
-        t_all1.record(stream)
-        n_launched = sdv.sdv_launch_count() - n_launch0  # this library's kernels in the timed region
-        torch.cuda.synchronize()
-    barrier(world)
-    elapsed_ms = t_all0.elapsed_time(t_all1)
+    elapsed_ms, n_launched, clk = timed_region(job, args.steps, world, local, sdv, torch)
     kernel_ms = elapsed_ms / args.steps
     if not status_ok():
         raise RuntimeError("device status reported an error during the timed region")
@@ -728,6 +788,7 @@ def run_sdv(args, wl, S, world, rank, local):
 
     if rank != 0:
         return 0
+    also = measure_also(args, also_specs(args, world), sdv, torch, dev, local)
     value = world * args.steps / (elapsed_ms / 1000.0)
     peak, kind = measured_peak()
     achieved = nbytes / (kernel_ms / 1000.0) / 1e9
@@ -753,6 +814,8 @@ def run_sdv(args, wl, S, world, rank, local):
         "gpu_launches": n_launched,
         "clocks": clk.summary(),
     }
+    if also:
+        line["also_measured"] = also
     print(json.dumps(line))
     return 0
 
@@ -867,6 +930,9 @@ def main(argv=None):
     ap.add_argument("--verify", choices=["greedy", "sample"], default="greedy",
                     help="head workloads: greedy verify (sdv_verify_head) or sampling verify at T = 1")
     ap.add_argument("--sweep-S", default="", help="comma-separated window sizes: verify-head time per S")
+    ap.add_argument("--also", default="auto",
+                    help="other workloads measured after the headline one, name:S comma-separated, 'none', or "
+                         f"'auto' ({ALSO_DEFAULT} on the default single-GPU run)")
     ap.add_argument("--fp4", action="store_true",
                     help="head workloads: the same head quantised to FP4 (E2M1) instead of its integer type")
     ap.add_argument("--spec-loop", action="store_true",

@@ -135,3 +135,24 @@ def test_workload_names():
 
 def test_oracle_threads_is_positive():
     assert bench.oracle_threads() >= 1
+
+
+def _args(**kw):
+    base = dict(also="auto", config="q4b", fp4=False, verify="greedy", path="auto")
+    base.update(kw)
+    return bench.argparse.Namespace(**base)
+
+
+def test_also_measured_defaults_to_the_other_full_size_workloads():
+    # the default single-GPU run also times the int4 head (S = 17 and 1), the
+    # dense MLP stack and the MoE layer; any other run measures only its own line
+    got = [(wl.name, S) for wl, S in bench.also_specs(_args(), 1)]
+    assert got == [("a3b", 17), ("a3b", 1), ("mlp27", 17), ("moe", 17)]
+    assert bench.also_specs(_args(), 2) == []
+    assert bench.also_specs(_args(config="a3b"), 1) == []
+    assert bench.also_specs(_args(fp4=True), 1) == []
+    assert bench.also_specs(_args(verify="sample"), 1) == []
+    assert bench.also_specs(_args(also="none"), 1) == []
+    assert [(wl.name, S) for wl, S in bench.also_specs(_args(also="mlp27:9, a3b"), 1)] == [("mlp27", 9), ("a3b", 17)]
+    with pytest.raises(SystemExit):
+        bench.also_specs(_args(also="nosuch:3"), 1)
