@@ -38,6 +38,7 @@
 #include <cfloat>
 #include <climits>
 #include <cstdint>
+#include <type_traits>
 
 #include "sdv_device.cuh"
 #include "sdv_kernels.h"
@@ -776,6 +777,13 @@ __global__ void __launch_bounds__(TcRoles<(QT == 8 ? 8 : 4)>::kThreads, 1)
                                 << (16 * (blk & 1));
         }
       }
+      // The stage's conversion, in one of two forms chosen once per stage (a
+      // branch per block inside the unrolled loop costs more than it saves):
+      // int4 with scale and bias in one HFMA2 per pair where every row's eight
+      // block scales s satisfy s * 2^20 <= 65504 (fp16 bits <= 0x2BFF, the
+      // common case), else the two-step form; both give the same bits.
+      auto convert = [&](auto fma_tag) {
+        constexpr bool kFma = decltype(fma_tag)::value;
 #pragma unroll
       for (int h = 0; h < kHalves; ++h) {
         uint4 wreg[kLoads];
@@ -807,6 +815,15 @@ __global__ void __launch_bounds__(TcRoles<(QT == 8 ? 8 : 4)>::kThreads, 1)
               for (int j = 0; j < 8; ++j) i8x4_to_h2x2(wv[j], cols[2 * j], cols[2 * j + 1]);
             } else if (QT == 4) {
               const uint32_t wv[4] = {wreg[blk].x, wreg[blk].y, wreg[blk].z, wreg[blk].w};
+              if constexpr (kFma) {
+                const __half2 m2 = __hmul2(__hmul2(s2, __float2half2_rn(1024.f)), __float2half2_rn(1024.f));
+                const __half2 c2 = __hmul2(s2, __float2half2_rn(-8.f));
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                  i4x8_to_h2x4_scaled(wv[j], m2, c2, cols[4 * j], cols[4 * j + 1], cols[4 * j + 2], cols[4 * j + 3]);
+                tmem_st16(tmem + lane_base + (uint32_t)(ab * 128 + sblk * 16), cols);
+                continue;
+              }
 #pragma unroll
               for (int j = 0; j < 4; ++j)
                 i4x8_to_h2x4(wv[j], cols[4 * j], cols[4 * j + 1], cols[4 * j + 2], cols[4 * j + 3]);
@@ -822,6 +839,18 @@ __global__ void __launch_bounds__(TcRoles<(QT == 8 ? 8 : 4)>::kThreads, 1)
           }
         }
       }
+      };
+      bool fma_form = false;
+      if (QT == 4 && ok) {
+        bool small = true;
+#pragma unroll
+        for (int w = 0; w < 4; ++w) small = small && (sc_w[w] & 0xFFFFu) <= 0x2BFFu && (sc_w[w] >> 16) <= 0x2BFFu;
+        fma_form = __all_sync(0xffffffffu, small);
+      }
+      if (fma_form)
+        convert(std::true_type{});
+      else
+        convert(std::false_type{});
       if (ok) {
         tmem_wait_st();
         tc_fence_before();
