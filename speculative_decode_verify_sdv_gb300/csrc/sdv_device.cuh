@@ -114,6 +114,19 @@ __device__ __forceinline__ void i8x4_to_h2x2(uint32_t w, uint32_t& lo, uint32_t&
   hi = h2_as_u32(__hsub2(u32_as_h2(t1), bias));
 }
 
+// Four signed int8 codes -> the fp16 pairs of e * s (same pairing as
+// i8x4_to_h2x2) with scale and bias in one HFMA2 per pair.  One xor of the word
+// turns each code into u = e + 128 in [0, 255], which in bits 0-7 of an fp16
+// half reads as the subnormal u * 2^-24 (exact); fma(u * 2^-24, m, c) with
+// m = s * 2^24 and c = -128 s is u * s - 128 s = e * s computed exactly and
+// rounded once: the bits of fp16(e) * s.  Valid while m is finite
+// (s <= 65504 * 2^-24); m and c in both halves.
+__device__ __forceinline__ void i8x4_to_h2x2_scaled(uint32_t w, __half2 m, __half2 c, uint32_t& lo, uint32_t& hi) {
+  const uint32_t x = w ^ 0x80808080u;
+  lo = h2_as_u32(__hfma2(u32_as_h2(x & 0x00FF00FFu), m, c));         // (e0, e2)
+  hi = h2_as_u32(__hfma2(u32_as_h2((x >> 8) & 0x00FF00FFu), m, c));  // (e1, e3)
+}
+
 // Eight signed int4 codes n0..n7 (n0 in bits 0-3) -> exact fp16 pairs
 // p0 = (n0, n4), p1 = (n1, n5), p2 = (n2, n6), p3 = (n3, n7).
 // Nibbles at bits 0-3 of each 16-bit half land as 1024 + (n + 8); nibbles at

@@ -779,9 +779,10 @@ __global__ void __launch_bounds__(TcRoles<(QT == 8 ? 8 : 4)>::kThreads, 1)
       }
       // The stage's conversion, in one of two forms chosen once per stage (a
       // branch per block inside the unrolled loop costs more than it saves):
-      // int4 with scale and bias in one HFMA2 per pair where every row's eight
-      // block scales s satisfy s * 2^20 <= 65504 (fp16 bits <= 0x2BFF, the
-      // common case), else the two-step form; both give the same bits.
+      // integer codes with scale and bias in one HFMA2 per pair where every
+      // row's eight block scales are in range -- int4: s * 2^20 <= 65504 (fp16
+      // bits <= 0x2BFF), int8: s * 2^24 <= 65504 (bits <= 0x1BFF), the common
+      // case -- else the two-step form; both give the same bits.
       auto convert = [&](auto fma_tag) {
         constexpr bool kFma = decltype(fma_tag)::value;
 #pragma unroll
@@ -811,6 +812,15 @@ __global__ void __launch_bounds__(TcRoles<(QT == 8 ? 8 : 4)>::kThreads, 1)
               const uint32_t wv[8] = {wreg[2 * blk].x, wreg[2 * blk].y, wreg[2 * blk].z, wreg[2 * blk].w,
                                       wreg[2 * blk + 1].x, wreg[2 * blk + 1].y, wreg[2 * blk + 1].z,
                                       wreg[2 * blk + 1].w};
+              if constexpr (kFma) {
+                const __half2 k12 = __float2half2_rn(4096.f);
+                const __half2 m2 = __hmul2(__hmul2(s2, k12), k12);
+                const __half2 c2 = __hmul2(s2, __float2half2_rn(-128.f));
+#pragma unroll
+                for (int j = 0; j < 8; ++j) i8x4_to_h2x2_scaled(wv[j], m2, c2, cols[2 * j], cols[2 * j + 1]);
+                tmem_st16(tmem + lane_base + (uint32_t)(ab * 128 + sblk * 16), cols);
+                continue;
+              }
 #pragma unroll
               for (int j = 0; j < 8; ++j) i8x4_to_h2x2(wv[j], cols[2 * j], cols[2 * j + 1]);
             } else if (QT == 4) {
@@ -841,10 +851,11 @@ __global__ void __launch_bounds__(TcRoles<(QT == 8 ? 8 : 4)>::kThreads, 1)
       }
       };
       bool fma_form = false;
-      if (QT == 4 && ok) {
+      if ((QT == 4 || QT == 8) && ok) {
+        constexpr uint32_t kMaxBits = (QT == 4) ? 0x2BFFu : 0x1BFFu;  // the largest scale in range
         bool small = true;
 #pragma unroll
-        for (int w = 0; w < 4; ++w) small = small && (sc_w[w] & 0xFFFFu) <= 0x2BFFu && (sc_w[w] >> 16) <= 0x2BFFu;
+        for (int w = 0; w < 4; ++w) small = small && (sc_w[w] & 0xFFFFu) <= kMaxBits && (sc_w[w] >> 16) <= kMaxBits;
         fma_form = __all_sync(0xffffffffu, small);
       }
       if (fma_form)

@@ -1,9 +1,11 @@
-"""The two int4 -> fp16 conversions of the tcgen05 converters give the same bits.
+"""The two integer-code -> fp16 conversions of the tcgen05 converters give the
+same bits.
 
-Where every row of a warp's 32-row slab has a block scale s <= 65504 * 2^-20
-(max |w| <= ~0.44 per block) the converters apply scale and bias in one fp16
-FMA on the code placed in the subnormal range; a slab with any larger scale
-takes the two-step form (exact code, then times s).  Both round n * s once, so
+Where every row of a warp's 32-row slab has its block scales in range (int4:
+s <= 65504 * 2^-20, max |w| <= ~0.44 per block; int8: s <= 65504 * 2^-24,
+max |w| <= ~0.5) the converters apply scale and bias in one fp16 FMA on the
+code placed in the subnormal range; a slab with any larger scale takes the
+two-step form (exact code, then times s).  Both round n * s once, so
 a row's logits must not depend on which form its slab took: the same head is
 run as is (every slab on the one-FMA form) and with the first row of every
 32-row slab scaled up (those slabs on the two-step form), and the logits of the
@@ -28,9 +30,10 @@ def sdv():
     return _sdv
 
 
+@pytest.mark.parametrize("bits", [4, 8])
 @pytest.mark.parametrize("S", [1, 9, 17])
 @pytest.mark.parametrize("n,k", [(4096, 2048), (1000, 512)])
-def test_int4_fma_and_two_step_forms_agree(sdv, n, k, S):
+def test_fma_and_two_step_forms_agree(sdv, bits, n, k, S):
     w = G.normal(G.stream_seed(1300, n, k), (n, k), 0.02)
     big = w.copy()
     big[::32] *= 40.0  # first row of every 32-row slab: scales around 0.3, past the one-FMA range
@@ -39,14 +42,15 @@ def test_int4_fma_and_two_step_forms_agree(sdv, n, k, S):
     keep = np.ones(n, bool)
     keep[::32] = False
     out = {}
+    limit = 65504 * 2.0 ** (-20 if bits == 4 else -24)
     with gemm_path("tc"):
         for name, wm in (("plain", w), ("big", big)):
-            codes, scales, stored = oracle_weight(wm, 4)
+            codes, scales, stored = oracle_weight(wm, bits)
             if name == "big":
-                assert float(np.max(scales[::32].astype(np.float32))) > 65504 * 2.0 ** -20
+                assert float(np.min(np.max(scales[::32].astype(np.float32), axis=1))) > limit
             if name == "plain":
-                assert float(np.max(scales.astype(np.float32))) <= 65504 * 2.0 ** -20
-            head = device_weight(stored, scales, 4, n, k)
+                assert float(np.max(scales.astype(np.float32))) <= limit
+            head = device_weight(stored, scales, bits, n, k)
             logits, am, acc, nxt = run_head(head, x, drafts, 0)
             ref = verify.verify_head(x, codes, scales, drafts, 0)
             # the parity bound is relative to the RMS of the logits it covers:
