@@ -123,8 +123,10 @@ __device__ __forceinline__ void i8x4_to_h2x2(uint32_t w, uint32_t& lo, uint32_t&
 // (s <= 65504 * 2^-24); m and c in both halves.
 __device__ __forceinline__ void i8x4_to_h2x2_scaled(uint32_t w, __half2 m, __half2 c, uint32_t& lo, uint32_t& hi) {
   const uint32_t x = w ^ 0x80808080u;
-  lo = h2_as_u32(__hfma2(u32_as_h2(x & 0x00FF00FFu), m, c));         // (e0, e2)
-  hi = h2_as_u32(__hfma2(u32_as_h2((x >> 8) & 0x00FF00FFu), m, c));  // (e1, e3)
+  // bytes 0, 2 and bytes 1, 3 into the low byte of each half, the rest zero:
+  // one byte permute each (with a zero second operand)
+  lo = h2_as_u32(__hfma2(u32_as_h2(__byte_perm(x, 0u, 0x4240u)), m, c));  // (e0, e2)
+  hi = h2_as_u32(__hfma2(u32_as_h2(__byte_perm(x, 0u, 0x4341u)), m, c));  // (e1, e3)
 }
 
 // Eight signed int4 codes n0..n7 (n0 in bits 0-3) -> exact fp16 pairs
