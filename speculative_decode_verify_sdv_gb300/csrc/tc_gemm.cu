@@ -63,6 +63,13 @@ struct TcRoles {
   static constexpr int kConv0 = 6;           // first converter warp (0 TMA, 1 MMA, 2-5 epilogue)
   static constexpr int kWarps = kConv0 + kConvWarps;
   static constexpr int kThreads = 32 * kWarps;
+  // A group converting stage i first waits (by parity) for the release of A
+  // buffer i % kABufs by the MMAs of stage i - kABufs; the wait is unambiguous
+  // only if the buffer's previous release (stage i - 2 kABufs) has completed.
+  // The group's own previous stage, i - G, waited for stage i - G - kABufs, and
+  // the MMAs complete in stage order, so that holds while G <= kABufs (with
+  // more groups a group can pass a stale phase and overwrite operands in use).
+  static_assert(G <= kABufs, "converter groups must not outnumber the A buffers");
 };
 
 struct TcPlan {
