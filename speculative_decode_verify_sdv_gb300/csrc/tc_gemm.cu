@@ -825,11 +825,10 @@ __global__ void __launch_bounds__(TcRoles<(QT == 8 ? 8 : 4)>::kThreads, 1)
                 const __half2 c2 = __hmul2(s2, __float2half2_rn(-128.f));
 #pragma unroll
                 for (int j = 0; j < 8; ++j) i8x4_to_h2x2_scaled(wv[j], m2, c2, cols[2 * j], cols[2 * j + 1]);
-                tmem_st16(tmem + lane_base + (uint32_t)(ab * 128 + sblk * 16), cols);
-                continue;
-              }
+              } else {
 #pragma unroll
-              for (int j = 0; j < 8; ++j) i8x4_to_h2x2(wv[j], cols[2 * j], cols[2 * j + 1]);
+                for (int j = 0; j < 8; ++j) i8x4_to_h2x2(wv[j], cols[2 * j], cols[2 * j + 1]);
+              }
             } else if (QT == 4) {
               const uint32_t wv[4] = {wreg[blk].x, wreg[blk].y, wreg[blk].z, wreg[blk].w};
               if constexpr (kFma) {
@@ -838,20 +837,22 @@ __global__ void __launch_bounds__(TcRoles<(QT == 8 ? 8 : 4)>::kThreads, 1)
 #pragma unroll
                 for (int j = 0; j < 4; ++j)
                   i4x8_to_h2x4_scaled(wv[j], m2, c2, cols[4 * j], cols[4 * j + 1], cols[4 * j + 2], cols[4 * j + 3]);
-                tmem_st16(tmem + lane_base + (uint32_t)(ab * 128 + sblk * 16), cols);
-                continue;
-              }
+              } else {
 #pragma unroll
-              for (int j = 0; j < 4; ++j)
-                i4x8_to_h2x4(wv[j], cols[4 * j], cols[4 * j + 1], cols[4 * j + 2], cols[4 * j + 3]);
+                for (int j = 0; j < 4; ++j)
+                  i4x8_to_h2x4(wv[j], cols[4 * j], cols[4 * j + 1], cols[4 * j + 2], cols[4 * j + 3]);
+              }
             } else {  // FP4: the hardware E2M1 -> f16x2 conversion, one byte (two codes) at a time
               const uint32_t wv[4] = {wreg[blk].x, wreg[blk].y, wreg[blk].z, wreg[blk].w};
 #pragma unroll
               for (int j = 0; j < 4; ++j)
                 e2m1x8_to_h2x4(wv[j], cols[4 * j], cols[4 * j + 1], cols[4 * j + 2], cols[4 * j + 3]);
             }
+            // the two-step form (and FP4) multiply by the scale after the conversion
+            if (!(kFma && QT != 2)) {
 #pragma unroll
-            for (int j = 0; j < 16; ++j) cols[j] = h2_as_u32(__hmul2(u32_as_h2(cols[j]), s2));
+              for (int j = 0; j < 16; ++j) cols[j] = h2_as_u32(__hmul2(u32_as_h2(cols[j]), s2));
+            }
             tmem_st16(tmem + lane_base + (uint32_t)(ab * 128 + sblk * 16), cols);
           }
         }
