@@ -356,6 +356,29 @@ __global__ void __launch_bounds__(TcRoles<(QT == 8 ? 8 : 4)>::kThreads, 1)
     }
     if (++c.ab == kABufs) { c.ab = 0; c.abphase ^= 1; }
   };
+  // advance by the G stages between a converter group's stages: the same state
+  // as G calls of advance() (G < depth and G <= kABufs, so slot and A buffer wrap
+  // at most once), in fewer instructions
+  auto advance_g = [&](Cursor& c, int G) {
+    c.i += G;
+    c.slot += G;
+    if (c.slot >= depth) {
+      c.slot -= depth;
+      c.phase ^= 1;
+    }
+    c.ks += G;
+    c.kx += G;
+    while (c.ks >= kst) {  // a new tile starts at slice rot
+      c.ks -= kst;
+      ++c.t;
+    }
+    while (c.kx >= kst) c.kx -= kst;  // kx = (ks + rot) mod kst throughout
+    c.ab += G;
+    if (c.ab >= kABufs) {
+      c.ab -= kABufs;
+      c.abphase ^= 1;
+    }
+  };
   uint64_t policy = 0;
   auto issue = [&](const Cursor& c) {  // TMA of stage c.i into ring slot c.slot
     // the timeout-path test withholds one stage: its slot never fills, and the
@@ -757,7 +780,6 @@ __global__ void __launch_bounds__(TcRoles<(QT == 8 ? 8 : 4)>::kThreads, 1)
     for (; c.i < nstages;) {
       const int slot = c.slot;
       const int ab = c.ab;
-      const int nb = max(0, min(8, nblk_total - c.kx * 8));  // blocks within the reduction length
       // the A buffer first, then the ring slot (the order tc_plan_valid relies on)
       bool ok = true;
       if (c.i >= kABufs) ok = wait_warp(bar_afree + 8 * ab, c.abphase ^ 1);
@@ -777,6 +799,7 @@ __global__ void __launch_bounds__(TcRoles<(QT == 8 ? 8 : 4)>::kThreads, 1)
         } else {
           const int row = (tile_lo + c.t) * kTileRows + r;
           const int ks = c.kx;
+          const int nb = max(0, min(8, nblk_total - ks * 8));  // blocks within the reduction length
 #pragma unroll
           for (int blk = 0; blk < 8; ++blk)
             if (blk < nb && row < p.N)
@@ -876,7 +899,7 @@ __global__ void __launch_bounds__(TcRoles<(QT == 8 ? 8 : 4)>::kThreads, 1)
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_afull + 8 * ab);
-      for (int j = 0; j < R::G; ++j) advance(c);
+      advance_g(c, R::G);
     }
   }
 
