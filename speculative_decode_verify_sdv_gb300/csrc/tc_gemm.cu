@@ -584,7 +584,7 @@ __global__ void __launch_bounds__(TcRoles<(QT == 8 ? 8 : 4)>::kThreads, 1)
     const int r = 32 * q + lane;
     const uint32_t lane_base = (uint32_t)(32 * q) << 16;
     float* const red = reinterpret_cast<float*>(sb + pl.red_off) + q * p.S * 33;  // [S][33]
-    float run_v = -FLT_MAX;  // running best of column n = lane
+    float run_v = -INFINITY;  // running best of column n = lane (no row yet: -inf, INT_MAX)
     int run_i = INT_MAX;
     // sampling verify, column n = lane: top-2 of L/T + g with their entries,
     // softmax max and sum of L/T, the logit L/T of the row's draft (NaN: not here)
@@ -659,15 +659,22 @@ __global__ void __launch_bounds__(TcRoles<(QT == 8 ? 8 : 4)>::kThreads, 1)
       }
       if (MODE == kModeHead) {
         // columns through shared memory: lane n then scans the warp's 32 rows
+        // (rows past the vocabulary as -inf, which never wins the scan below)
 #pragma unroll
         for (int n = 0; n < 32; ++n)
-          if (n < p.S) red[n * 33 + lane] = valid ? acc[n] : -FLT_MAX;
+          if (n < p.S) red[n * 33 + lane] = valid ? acc[n] : -INFINITY;
         __syncwarp();
         if (lane < p.S) {
+          // rows reach a lane in increasing index order (tiles, then rows), so a
+          // later row wins only with a strictly larger value: the argmax order
+          // (larger value, then lower index) without its tie test
           const int row0 = (tile_lo + t) * kTileRows + 32 * q;
           for (int j = 0; j < 32; ++j) {
             const float v = red[lane * 33 + j];
-            if (row0 + j < p.N) argmax_merge(run_v, run_i, v, row0 + j);
+            if (v > run_v) {
+              run_v = v;
+              run_i = row0 + j;
+            }
           }
         }
         __syncwarp();
