@@ -206,16 +206,11 @@ __device__ __forceinline__ float counter_uniform(unsigned long long key, unsigne
 // is the fast hardware one (absolute error ~1e-6, below what the draws compare).
 __device__ __forceinline__ float gumbel_of(float u) { return -__logf(-log1pf(-(1.f - u))); }
 
-// Top-2 under the argmax order (value desc, index asc).
-__device__ __forceinline__ void top2_add(float& z1, int& v1, float& z2, int& v2, float z, int v) {
+// Top 1 under the argmax order (value desc, index asc).
+__device__ __forceinline__ void top1_add(float& z1, int& v1, float z, int v) {
   if (z > z1 || (z == z1 && v < v1)) {
-    z2 = z1;
-    v2 = v1;
     z1 = z;
     v1 = v;
-  } else if (z > z2 || (z == z2 && v < v2)) {
-    z2 = z;
-    v2 = v;
   }
 }
 

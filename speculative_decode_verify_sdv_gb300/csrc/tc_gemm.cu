@@ -105,36 +105,40 @@ __host__ __device__ inline TcPlan tc_plan(int qb, int S, int kc, int depth) {
 
 // Tail of the sampling verify, run by every thread of the CTA after the
 // teardown barrier.  `stb` holds the four epilogue warps' column states
-// ([field][quarter][S] floats).  Each CTA publishes its merged partial per
-// window row; the last CTA (acquire-release ticket, as for the verify head)
-// merges all of them in CTA order and runs the accept: draft d_i is kept iff
-// u_i < p_i(d_i) = exp(L_i(d_i)/T - M_i) / sum_v exp(L_i(v)/T - M_i); at the first
-// rejection the token is the largest L/T + g of row i other than d_i (the
-// residual draw), and if every draft is kept it is row n_valid's draw.
+// ([field][quarter][S] floats: top-1 z and entry over the entries other than
+// the row's draft, the draft's z, softmax max and sum, the draft's L/T).  Each
+// CTA publishes its merged partial per window row; the last CTA (acquire-release
+// ticket, as for the verify head) merges all of them and runs the accept: draft
+// d_i is kept iff u_i < p_i(d_i) = exp(L_i(d_i)/T - M_i) / sum_v exp(L_i(v)/T - M_i);
+// at the first rejection the token is the largest L/T + g of row i other than d_i
+// (the residual draw), and if every draft is kept it is row n_valid's draw.  A
+// row's draw from its full distribution is d_i where d_i's z wins the argmax
+// order against the residual draw, else the residual draw.
 __device__ __noinline__ void sample_tail(const GemmArgs& p, uint8_t* stb, const int* s_drafts, int* s_flag,
                                          int warp, int lane, int nwarps) {
   float* const st = reinterpret_cast<float*>(stb);
   const int S = p.S, f = 4 * S;
+  auto take_number = [](float& into, float v) {  // the one CTA / quarter holding the draft reports it
+    if (v == v) into = v;
+  };
   if ((int)threadIdx.x < S) {
     const int c = threadIdx.x;
-    float z1 = st[c], z2 = st[2 * f + c], m = st[4 * f + c], s = st[5 * f + c], ld = st[6 * f + c];
-    int v1 = __float_as_int(st[f + c]), v2 = __float_as_int(st[3 * f + c]);
+    float zx = st[c], zd = st[2 * f + c], m = st[3 * f + c], s = st[4 * f + c], ld = st[5 * f + c];
+    int vx = __float_as_int(st[f + c]);
     for (int q = 1; q < 4; ++q) {
       const int o = q * S + c;
-      top2_add(z1, v1, z2, v2, st[o], __float_as_int(st[f + o]));
-      top2_add(z1, v1, z2, v2, st[2 * f + o], __float_as_int(st[3 * f + o]));
-      softmax_merge(m, s, st[4 * f + o], st[5 * f + o]);
-      const float lq = st[6 * f + o];
-      if (lq == lq) ld = lq;
+      top1_add(zx, vx, st[o], __float_as_int(st[f + o]));
+      take_number(zd, st[2 * f + o]);
+      softmax_merge(m, s, st[3 * f + o], st[4 * f + o]);
+      take_number(ld, st[5 * f + o]);
     }
     float* const out = p.part_s + ((size_t)blockIdx.x * S + c) * 8;
-    __stcg(out + 0, z1);
-    __stcg(out + 1, __int_as_float(v1));
-    __stcg(out + 2, z2);
-    __stcg(out + 3, __int_as_float(v2));
-    __stcg(out + 4, m);
-    __stcg(out + 5, s);
-    __stcg(out + 6, ld);
+    __stcg(out + 0, zx);
+    __stcg(out + 1, __int_as_float(vx));
+    __stcg(out + 2, zd);
+    __stcg(out + 3, m);
+    __stcg(out + 4, s);
+    __stcg(out + 5, ld);
   }
   __syncthreads();
   if (threadIdx.x == 0) {
@@ -144,52 +148,52 @@ __device__ __noinline__ void sample_tail(const GemmArgs& p, uint8_t* stb, const 
   }
   __syncthreads();
   if (*s_flag == 0) return;
-  // merged rows: [S][8] = v1, v2, m, s, ld
+  // merged rows: [S][8] = residual draw, full draw, m, s, ld
   for (int col = warp; col < S; col += nwarps) {
-    float z1 = -INFINITY, z2 = -INFINITY, m = -INFINITY, s = 0.f, ld = __int_as_float(0x7fc00000);
-    int v1 = INT_MAX, v2 = INT_MAX;
+    float zx = -INFINITY, zd = __int_as_float(0x7fc00000), m = -INFINITY, s = 0.f, ld = __int_as_float(0x7fc00000);
+    int vx = INT_MAX;
     for (int j = lane; j < (int)gridDim.x; j += 32) {
       const float* const in = p.part_s + ((size_t)j * S + col) * 8;
-      top2_add(z1, v1, z2, v2, __ldcg(in + 0), __float_as_int(__ldcg(in + 1)));
-      top2_add(z1, v1, z2, v2, __ldcg(in + 2), __float_as_int(__ldcg(in + 3)));
-      softmax_merge(m, s, __ldcg(in + 4), __ldcg(in + 5));
-      const float lq = __ldcg(in + 6);
-      if (lq == lq) ld = lq;
+      top1_add(zx, vx, __ldcg(in + 0), __float_as_int(__ldcg(in + 1)));
+      take_number(zd, __ldcg(in + 2));
+      softmax_merge(m, s, __ldcg(in + 3), __ldcg(in + 4));
+      take_number(ld, __ldcg(in + 5));
     }
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) {
-      const float oz1 = __shfl_xor_sync(0xffffffffu, z1, off), oz2 = __shfl_xor_sync(0xffffffffu, z2, off);
-      const int ov1 = __shfl_xor_sync(0xffffffffu, v1, off), ov2 = __shfl_xor_sync(0xffffffffu, v2, off);
+      const float oz = __shfl_xor_sync(0xffffffffu, zx, off), ozd = __shfl_xor_sync(0xffffffffu, zd, off);
+      const int ov = __shfl_xor_sync(0xffffffffu, vx, off);
       const float om = __shfl_xor_sync(0xffffffffu, m, off), os = __shfl_xor_sync(0xffffffffu, s, off);
       const float old = __shfl_xor_sync(0xffffffffu, ld, off);
-      top2_add(z1, v1, z2, v2, oz1, ov1);
-      top2_add(z1, v1, z2, v2, oz2, ov2);
+      top1_add(zx, vx, oz, ov);
+      take_number(zd, ozd);
       softmax_merge(m, s, om, os);
-      if (old == old) ld = old;
+      take_number(ld, old);
     }
     if (lane == 0) {
+      // zd is a number only where the row has a draft inside the vocabulary
+      const int d = (col < p.n_valid) ? s_drafts[col] : -1;
+      const int full = (zd == zd && (zd > zx || (zd == zx && d < vx))) ? d : vx;
       float* const r = st + col * 8;
-      r[0] = __int_as_float(v1);
-      r[1] = __int_as_float(v2);
+      r[0] = __int_as_float(vx);
+      r[1] = __int_as_float(full);
       r[2] = m;
       r[3] = s;
       r[4] = ld;
-      p.argmax[col] = v1;  // the row's draw from its full distribution
+      p.argmax[col] = full;  // the row's draw from its full distribution
     }
   }
   __syncthreads();
   if (threadIdx.x == 0) {
     int j = p.n_valid;
-    int token = __float_as_int(st[p.n_valid * 8]);
+    int token = __float_as_int(st[p.n_valid * 8 + 1]);
     for (int i = 0; i < p.n_valid; ++i) {
       const float* const r = st + i * 8;
-      const int d = s_drafts[i];
       const float pr = expf(r[4] - r[2]) / r[3];
       const float u = counter_uniform(p.rng_key, 32ull * (unsigned)p.N + (unsigned)i);
       if (!(u < pr)) {
         j = i;
-        const int a1 = __float_as_int(r[0]);
-        token = (a1 != d) ? a1 : __float_as_int(r[1]);
+        token = __float_as_int(r[0]);  // the residual draw: the best entry other than d_i
         break;
       }
     }
@@ -586,10 +590,12 @@ __global__ void __launch_bounds__(TcRoles<(QT == 8 ? 8 : 4)>::kThreads, 1)
     float* const red = reinterpret_cast<float*>(sb + pl.red_off) + q * p.S * 33;  // [S][33]
     float run_v = -INFINITY;  // running best of column n = lane (no row yet: -inf, INT_MAX)
     int run_i = INT_MAX;
-    // sampling verify, column n = lane: top-2 of L/T + g with their entries,
-    // softmax max and sum of L/T, the logit L/T of the row's draft (NaN: not here)
-    float z1 = -INFINITY, z2 = -INFINITY, sm_m = -INFINITY, sm_s = 0.f, l_d = __int_as_float(0x7fc00000);
-    int v1 = INT_MAX, v2 = INT_MAX;
+    // sampling verify, per column: the top 1 of z = L/T + g over the entries other
+    // than the row's draft (with its entry), the draft's own z and L/T (NaN: not
+    // in this CTA's rows), the softmax max and sum of L/T
+    float zx = -INFINITY, z_d = __int_as_float(0x7fc00000), sm_m = -INFINITY, sm_s = 0.f,
+          l_d = __int_as_float(0x7fc00000);
+    int vx = INT_MAX;
     // sampling scans: L lanes per column (32 over the next power of two >= S), so a
     // small window spreads each column's 32 rows over many lanes; lane cc * L owns
     // column cc's running state
@@ -597,6 +603,7 @@ __global__ void __launch_bounds__(TcRoles<(QT == 8 ? 8 : 4)>::kThreads, 1)
     const int s_lanes = 32 / s_pow2;
     const int s_col = lane / s_lanes, s_sub = lane % s_lanes;
     const bool s_act = s_col < p.S, s_own = s_act && s_sub == 0;
+    const int s_dv = (MODE == kModeSample && s_col < p.n_valid) ? s_drafts[s_col] : -1;  // the column's draft
     const int tpe = p.rows_per_expert > 0 ? p.rows_per_expert / kTileRows : 1;
     for (int t = 0; t < ntile; ++t) {
       const int tb = t & 1;
@@ -704,8 +711,7 @@ __global__ void __launch_bounds__(TcRoles<(QT == 8 ? 8 : 4)>::kThreads, 1)
           for (int o = s_lanes >> 1; o > 0; o >>= 1) e += __shfl_xor_sync(0xffffffffu, e, o);
           if (s_own) {
             softmax_merge(sm_m, sm_s, m, e);
-            const int dv = (s_col < p.n_valid) ? s_drafts[s_col] : -1;
-            if (dv >= row0 && dv < row0 + nrow) l_d = col[dv - row0];
+            if (s_dv >= row0 && s_dv < row0 + nrow) l_d = col[s_dv - row0];
           }
         }
         __syncwarp();
@@ -721,23 +727,35 @@ __global__ void __launch_bounds__(TcRoles<(QT == 8 ? 8 : 4)>::kThreads, 1)
           }
         }
         __syncwarp();
-        // (4) column s_col over its lanes: the top 2 of z over the slab, merged
-        // across the lane group by a butterfly
+        // (4) column s_col over its lanes: the draft's entry leaves the slab (its z
+        // kept aside), then the top 1 of z over the rest, merged across the lane
+        // group by a butterfly.  The draw from p without the draft is that top 1;
+        // the draw from p is the draft where its z beats it, else the same entry.
         {
-          const float* const col = red + s_col * 33;
-          float a1 = -INFINITY, a2 = -INFINITY;
-          int b1 = INT_MAX, b2 = INT_MAX;
-          if (s_act)
-            for (int j = s_sub; j < nrow; j += s_lanes) top2_add(a1, b1, a2, b2, col[j], row0 + j);
-          for (int o = s_lanes >> 1; o > 0; o >>= 1) {
-            const float oz1 = __shfl_xor_sync(0xffffffffu, a1, o), oz2 = __shfl_xor_sync(0xffffffffu, a2, o);
-            const int ob1 = __shfl_xor_sync(0xffffffffu, b1, o), ob2 = __shfl_xor_sync(0xffffffffu, b2, o);
-            top2_add(a1, b1, a2, b2, oz1, ob1);
-            top2_add(a1, b1, a2, b2, oz2, ob2);
+          float* const col = red + s_col * 33;
+          if (s_own && s_dv >= row0 && s_dv < row0 + nrow) {
+            z_d = col[s_dv - row0];
+            col[s_dv - row0] = -INFINITY;
           }
-          if (s_own) {
-            top2_add(z1, v1, z2, v2, a1, b1);
-            top2_add(z1, v1, z2, v2, a2, b2);
+          __syncwarp();
+          // a lane's rows come in increasing index order, so a later row wins
+          // only with a strictly larger z (the argmax order without its tie test)
+          float a = -INFINITY;
+          int b = INT_MAX;
+          if (s_act)
+            for (int j = s_sub; j < nrow; j += s_lanes) {
+              const float z = col[j];
+              if (z > a) {
+                a = z;
+                b = row0 + j;
+              }
+            }
+          for (int o = s_lanes >> 1; o > 0; o >>= 1)
+            top1_add(a, b, __shfl_xor_sync(0xffffffffu, a, o), __shfl_xor_sync(0xffffffffu, b, o));
+          // earlier tiles hold lower rows: again a strictly larger z wins
+          if (s_own && a > zx) {
+            zx = a;
+            vx = b;
           }
         }
         __syncwarp();
@@ -754,13 +772,12 @@ __global__ void __launch_bounds__(TcRoles<(QT == 8 ? 8 : 4)>::kThreads, 1)
       float* const st = reinterpret_cast<float*>(sb + pl.red_off);
       if (s_own) {
         const int o = q * p.S + s_col, f = 4 * p.S;
-        st[o] = z1;
-        st[f + o] = __int_as_float(v1);
-        st[2 * f + o] = z2;
-        st[3 * f + o] = __int_as_float(v2);
-        st[4 * f + o] = sm_m;
-        st[5 * f + o] = sm_s;
-        st[6 * f + o] = l_d;
+        st[o] = zx;
+        st[f + o] = __int_as_float(vx);
+        st[2 * f + o] = z_d;
+        st[3 * f + o] = sm_m;
+        st[4 * f + o] = sm_s;
+        st[5 * f + o] = l_d;
       }
     }
   } else {
