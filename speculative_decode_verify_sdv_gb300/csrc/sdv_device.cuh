@@ -158,20 +158,24 @@ __device__ __forceinline__ uint32_t and_xor(uint32_t a, uint32_t flip) {
 }
 
 // Eight signed int4 codes n0..n7 -> the fp16 pairs of n * s (same pairing as
-// i4x8_to_h2x4) with scale and bias in one HFMA2 per pair.  Each code is moved
-// to bits 4-7 of an fp16 half and its top bit flipped in the same LOP3 that
-// masks it, giving u = n + 8 in [0, 15], which reads as the subnormal
-// u * 2^-20 (exact); fma(u * 2^-20, m, c) with m = s * 2^20 and c = -8 s is
-// u * s - 8 s = n * s computed exactly and rounded once: the bits of
-// fp16(n) * s from the two-step form.  Valid while m is finite
-// (s <= 65504 * 2^-20); m and c in both halves.
-__device__ __forceinline__ void i4x8_to_h2x4_scaled(uint32_t w, __half2 m, __half2 c, uint32_t& p0, uint32_t& p1,
-                                                    uint32_t& p2, uint32_t& p3) {
+// i4x8_to_h2x4), one shift per word.  Pairs (n1, n5) and (n3, n7), at bits 4-7
+// of each half of w and of w >> 8, take scale and bias in one HFMA2: the LOP3
+// that masks a code also flips its top bit, giving u = n + 8 in [0, 15], which
+// reads as the subnormal u * 2^-20 (exact); fma(u * 2^-20, m, c) with
+// m = s * 2^20 and c = -8 s is u * s - 8 s = n * s computed exactly and rounded
+// once.  Pairs (n0, n4) and (n2, n6), at bits 0-3, take the exponent-bias form
+// of i4x8_to_h2x4 (exact n, then times s, rounded once).  Every pair gets the
+// bits of fp16(n) * s from the two-step form.  Valid while m is finite
+// (s <= 65504 * 2^-20); m, c and s in both halves.
+__device__ __forceinline__ void i4x8_to_h2x4_scaled(uint32_t w, __half2 m, __half2 c, __half2 s, uint32_t& p0,
+                                                    uint32_t& p1, uint32_t& p2, uint32_t& p3) {
   const uint32_t flip = 0x00800080u;  // the top bit of a code placed at bits 4-7 of each half
-  p0 = h2_as_u32(__hfma2(u32_as_h2(and_xor<0x00F000F0u>(w << 4, flip)), m, c));  // (n0, n4)
-  p1 = h2_as_u32(__hfma2(u32_as_h2(and_xor<0x00F000F0u>(w, flip)), m, c));       // (n1, n5)
-  p2 = h2_as_u32(__hfma2(u32_as_h2(and_xor<0x00F000F0u>(w >> 4, flip)), m, c));  // (n2, n6)
-  p3 = h2_as_u32(__hfma2(u32_as_h2(and_xor<0x00F000F0u>(w >> 8, flip)), m, c));  // (n3, n7)
+  const __half2 b_lo = u32_as_h2(0x64086408u);  // (1032, 1032)
+  const uint32_t y = w >> 8;
+  p0 = h2_as_u32(__hmul2(__hsub2(u32_as_h2(and_xor<0x000F000Fu>(w, 0x64086408u)), b_lo), s));  // (n0, n4)
+  p1 = h2_as_u32(__hfma2(u32_as_h2(and_xor<0x00F000F0u>(w, flip)), m, c));                      // (n1, n5)
+  p2 = h2_as_u32(__hmul2(__hsub2(u32_as_h2(and_xor<0x000F000Fu>(y, 0x64086408u)), b_lo), s));  // (n2, n6)
+  p3 = h2_as_u32(__hfma2(u32_as_h2(and_xor<0x00F000F0u>(y, flip)), m, c));                      // (n3, n7)
 }
 
 // Counter stream of the sampling verify: SplitMix64 (Steele, Lea & Flood,

@@ -883,7 +883,7 @@ __global__ void __launch_bounds__(TcRoles<(QT == 8 ? 8 : 4)>::kThreads, 1)
                 const __half2 c2 = __hmul2(s2, __float2half2_rn(-8.f));
 #pragma unroll
                 for (int j = 0; j < 4; ++j)
-                  i4x8_to_h2x4_scaled(wv[j], m2, c2, cols[4 * j], cols[4 * j + 1], cols[4 * j + 2], cols[4 * j + 3]);
+                  i4x8_to_h2x4_scaled(wv[j], m2, c2, s2, cols[4 * j], cols[4 * j + 1], cols[4 * j + 2], cols[4 * j + 3]);
               } else {
 #pragma unroll
                 for (int j = 0; j < 4; ++j)
