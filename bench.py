@@ -498,27 +498,30 @@ class HeadJob:
                                  self.acc[j], self.nxt[j], self.ws)
 
     def e2e_setup(self):
+        # one pinned host record per window (hidden states, then drafts) and one
+        # device record it lands in: one H2D copy per step; the results (ids,
+        # accepted, next token) are one device record read back by one D2H copy
         t, S, dev = self.torch, self.S, self.dev
-        self.x_host = t.from_numpy(self.xs.view(np.int16)).view(t.float16).pin_memory()
-        self.d_host = t.from_numpy(self.dr).pin_memory()
-        self.x_stage = t.empty_like(self.x_dev[0])
-        self.d_stage = t.empty_like(self.d_dev[0])
+        xb, db = S * self.wl.h * 2, self.dr.shape[1] * 4
+        rec = np.zeros((self.nwin, xb + db), dtype=np.uint8)
+        rec[:, :xb] = self.xs.reshape(self.nwin, -1).view(np.uint8)
+        rec[:, xb:] = self.dr.view(np.uint8).reshape(self.nwin, -1)
+        self.in_host = t.from_numpy(rec).pin_memory()
+        self.in_dev = t.empty(xb + db, dtype=t.uint8, device=dev)
+        self.x_stage = self.in_dev[:xb].view(t.float16).view(S, self.wl.h)
+        self.d_stage = self.in_dev[xb:].view(t.int32)
+        self.out_dev = t.empty(S + 2, dtype=t.int32, device=dev)
+        self.am1, self.acc1, self.nxt1 = self.out_dev[:S], self.out_dev[S:S + 1], self.out_dev[S + 1:]
         self.out_host = t.empty((self.nwin, S + 2), dtype=t.int32).pin_memory()
-        self.am1 = t.empty(S, dtype=t.int32, device=dev)
-        self.acc1 = t.empty(1, dtype=t.int32, device=dev)
-        self.nxt1 = t.empty(1, dtype=t.int32, device=dev)
-        self.h2d = S * self.wl.h * 2 + self.dr.shape[1] * 4
+        self.h2d = xb + db
         self.d2h = (S + 2) * 4
 
     def e2e_step(self, i):
         j, S = i % self.nwin, self.S
-        self.x_stage.copy_(self.x_host[j], non_blocking=True)
-        self.d_stage.copy_(self.d_host[j], non_blocking=True)
+        self.in_dev.copy_(self.in_host[j], non_blocking=True)
         self.sdv.sdv_verify_head(self.head, self.x_stage, S, self.d_stage, self.n_valid, None, self.am1,
                                  self.acc1, self.nxt1, self.ws)
-        self.out_host[j, :S].copy_(self.am1, non_blocking=True)
-        self.out_host[j, S:S + 1].copy_(self.acc1, non_blocking=True)
-        self.out_host[j, S + 1:].copy_(self.nxt1, non_blocking=True)
+        self.out_host[j].copy_(self.out_dev, non_blocking=True)
 
 
 class SampleJob(HeadJob):
@@ -538,13 +541,10 @@ class SampleJob(HeadJob):
 
     def e2e_step(self, i):
         j, S = i % self.nwin, self.S
-        self.x_stage.copy_(self.x_host[j], non_blocking=True)
-        self.d_stage.copy_(self.d_host[j], non_blocking=True)
+        self.in_dev.copy_(self.in_host[j], non_blocking=True)
         self.sdv.sdv_verify_sample(self.head, self.x_stage, S, self.d_stage, self.n_valid, 1.0, 1, i, None,
                                    self.am1, self.acc1, self.nxt1, self.ws)
-        self.out_host[j, :S].copy_(self.am1, non_blocking=True)
-        self.out_host[j, S:S + 1].copy_(self.acc1, non_blocking=True)
-        self.out_host[j, S + 1:].copy_(self.nxt1, non_blocking=True)
+        self.out_host[j].copy_(self.out_dev, non_blocking=True)
 
 
 class MlpJob:
@@ -633,20 +633,25 @@ class MoeJob:
         self._call(self.x_dev[j], self.l_dev[j], self.out[j])
 
     def e2e_setup(self):
-        t = self.torch
-        self.x_host = t.from_numpy(self.xs.view(np.int16)).view(t.float16).pin_memory()
-        self.l_host = t.from_numpy(self.ls).pin_memory()
-        self.x_stage = t.empty_like(self.x_dev[0])
-        self.l_stage = t.empty_like(self.l_dev[0])
+        # one pinned host record per window (hidden states, then router logits)
+        # and one device record it lands in: one H2D copy and one D2H per step
+        t, S, dev = self.torch, self.S, self.dev
+        xb, lb = S * self.wl.h * 2, S * self.wl.experts * 4
+        rec = np.zeros((self.nwin, xb + lb), dtype=np.uint8)
+        rec[:, :xb] = self.xs.reshape(self.nwin, -1).view(np.uint8)
+        rec[:, xb:] = self.ls.astype(np.float32).reshape(self.nwin, -1).view(np.uint8)
+        self.in_host = t.from_numpy(rec).pin_memory()
+        self.in_dev = t.empty(xb + lb, dtype=t.uint8, device=dev)
+        self.x_stage = self.in_dev[:xb].view(t.float16).view(S, self.wl.h)
+        self.l_stage = self.in_dev[xb:].view(t.float32).view(S, self.wl.experts)
         self.o1 = t.empty_like(self.out[0])
         self.out_host = t.empty((self.nwin,) + tuple(self.o1.shape), dtype=t.float32).pin_memory()
-        self.h2d = self.S * self.wl.h * 2 + self.S * self.wl.experts * 4
-        self.d2h = self.S * self.wl.h * 4
+        self.h2d = xb + lb
+        self.d2h = S * self.wl.h * 4
 
     def e2e_step(self, i):
         j = i % self.nwin
-        self.x_stage.copy_(self.x_host[j], non_blocking=True)
-        self.l_stage.copy_(self.l_host[j], non_blocking=True)
+        self.in_dev.copy_(self.in_host[j], non_blocking=True)
         self._call(self.x_stage, self.l_stage, self.o1)
         self.out_host[j].copy_(self.o1, non_blocking=True)
 
