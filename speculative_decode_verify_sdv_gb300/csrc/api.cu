@@ -183,7 +183,7 @@ void apply_debug(GemmArgs& a) {
 // stages (a stage is one 128 x 256 code tile; every SM streams at the same rate)
 // plus the split partials' write and read-back; the cheapest wins, ties to fewer
 // splits.  `unit` tiles move together (2: the gate/up pairs of the fused SwiGLU).
-GemmPlan plan_tc(int qbits, int n, int k, int S, bool allow_split, int unit = 1) {
+GemmPlan plan_tc(int qbits, int n, int k, int S, bool allow_split, int unit = 1, bool route = false) {
   GemmPlan best;
   const int sms = device_sms();
   const int limit = device_smem_optin();
@@ -200,7 +200,7 @@ GemmPlan plan_tc(int qbits, int n, int k, int S, bool allow_split, int unit = 1)
     if (splits != want) continue;  // the same chunk as a smaller split count
     int depth = 0, bytes = 0;
     for (int d = kMaxDepth; d >= 4 && depth == 0; --d) {  // tc_plan_valid rejects shallower rings
-      const int b = sdv::tc_smem_bytes(qbits, S, k_chunk, d);
+      const int b = sdv::tc_smem_bytes(qbits, S, k_chunk, d, route);
       if (b <= limit && sdv::tc_plan_valid(qbits, S, k_chunk, d)) {
         depth = d;
         bytes = b;
@@ -414,6 +414,7 @@ size_t swiglu_ws_bytes(int qbits, int n, int k, int S) {
 // Gathered-expert MoE workspace layout (all offsets 256-aligned).
 struct MoeLayout {
   int n_cap = 0;       // most experts a window can hit: min(E, S * top_k)
+  bool route = false;  // the gate/up launch routes the window itself (no routing launch)
   int gx = 0, ys = 0;  // down projection: CTAs per split, splits (expert-segment slots)
   GemmPlan gu, dn;     // gate/up and down launch plans
   size_t ids, w, offsets, pair_rows, n_hit, hit, row_w, hbuf, dn_part, total;
@@ -425,8 +426,14 @@ MoeLayout plan_moe(int qbits, int E, int I, int H, int top_k, int S) {
   const int limit = device_smem_optin();
   if (sms <= 0 || limit <= 0) return L;
   L.n_cap = E < S * top_k ? E : S * top_k;
-  // gate/up: both matrices of the hit experts, full reduction H, no split
-  L.gu = plan_tc(qbits, 2 * L.n_cap * I, H, S, false);
+  // gate/up: both matrices of the hit experts, full reduction H, no split; it
+  // routes the window in its prologue where the routing fits its limits and
+  // shared memory, else a routing launch runs first
+  if (E <= sdv::kRouteMaxE && top_k <= sdv::kRouteMaxTopK && S <= sdv::kRouteMaxS) {
+    L.gu = plan_tc(qbits, 2 * L.n_cap * I, H, S, false, 1, true);
+    L.route = L.gu.splits == 1;
+  }
+  if (!L.route) L.gu = plan_tc(qbits, 2 * L.n_cap * I, H, S, false);
   if (L.gu.splits != 1) return MoeLayout{};
   L.gu.grid = sms;
   // down: the reduction is the hit experts' I-column segments; gx CTAs share one
@@ -807,11 +814,15 @@ sdv_status sdv_moe_gather_qmm(const sdv_qweight* gate, const sdv_qweight* up, co
   __half* const hb = reinterpret_cast<__half*>(w8 + L.hbuf);
   float* const dn = reinterpret_cast<float*>(w8 + L.dn_part);
   const int ncap_i = L.n_cap * I;
-  // a7 + a8: route and group
-  cudaError_t e = sdv::launch_moe_route(router_logits, S, E, top_k, ids, rw8,
-                                        reinterpret_cast<int32_t*>(w8 + L.offsets),
-                                        reinterpret_cast<int32_t*>(w8 + L.pair_rows), n_hit, hit, row_w, L.n_cap, st);
-  if (e != cudaSuccess) return cuda_status(e);
+  // a7 + a8: route and group -- in the gate/up launch's prologue where it fits
+  // (each CTA routes the window itself, CTA 0 publishes the picks and the hit
+  // list), else a routing launch first
+  cudaError_t e = cudaSuccess;
+  if (!L.route) {
+    e = sdv::launch_moe_route(router_logits, S, E, top_k, ids, rw8, reinterpret_cast<int32_t*>(w8 + L.offsets),
+                              reinterpret_cast<int32_t*>(w8 + L.pair_rows), n_hit, hit, row_w, L.n_cap, st);
+    if (e != cudaSuccess) return cuda_status(e);
+  }
   // a9, gate and up: every window row through each hit expert's rows (gate/up
   // tile pairs over the hit list) with the SwiGLU epilogue writing
   // h'[s][j * I + c] = fp16(w(s, hit j) * SiLU(g) * u), zero where row s did not pick hit j
@@ -822,13 +833,23 @@ sdv_status sdv_moe_gather_qmm(const sdv_qweight* gate, const sdv_qweight* up, co
     a.N = ncap_i;
     a.K = H;
     a.dual = 2;
-    a.n_hit = n_hit;
-    a.hit = hit;
     a.rows_per_expert = I;
     a.h = hb;
     a.ldh = ncap_i;
-    a.row_w = row_w;
-    a.ldw = L.n_cap;
+    if (L.route) {
+      a.route_logits = router_logits;
+      a.route_E = E;
+      a.route_top_k = top_k;
+      a.route_ids = ids;
+      a.route_w = rw8;
+      a.route_n_hit = n_hit;
+      a.route_hit = hit;
+    } else {
+      a.n_hit = n_hit;
+      a.hit = hit;
+      a.row_w = row_w;
+      a.ldw = L.n_cap;
+    }
     sdv_status s = launch_tc_y(gate, up, L.gu, a, ws, st);
     if (s != SDV_OK) return s;
   }

@@ -66,8 +66,9 @@ struct GemmArgs {
   unsigned* ticket;
   int* status;
   // sampling verify (kModeSample): p_i = softmax(L_i * inv_temp); draws from the
-  // counter stream rng_key; per-CTA partials [grid][S][8] (top-2 of L/T + g with
-  // their entries, softmax max and sum of L/T, the draft's L/T)
+  // counter stream rng_key; per-CTA partials [grid][S][8] (top 1 of L/T + g over
+  // the entries other than the row's draft, with its entry; the draft's z;
+  // softmax max and sum of L/T; the draft's L/T)
   float inv_temp;
   unsigned long long rng_key;
   float* part_s;
@@ -90,6 +91,18 @@ struct GemmArgs {
   int ldh;
   const float* row_w;
   int ldw;
+  // MoE gate/up that routes the window in its own prologue (dual == 2, hit-list
+  // tiles; n_hit and hit null): every CTA selects the top route_top_k of each
+  // row's route_E router logits ([S][route_E] fp32) and takes the hit list and
+  // the routing weights from its own selection; CTA 0 publishes the picks
+  // (route_ids, route_w: [S][route_top_k]) and the hit list (route_n_hit,
+  // route_hit, experts ascending) for the down projection.  Null: off.
+  const float* route_logits;
+  int route_E, route_top_k;
+  int32_t* route_ids;
+  float* route_w;
+  int32_t* route_n_hit;
+  int32_t* route_hit;
   // ---- timeout-path test hooks of the tcgen05 path (zero = off) ----
   unsigned long long wait_ns;  // limit of every bounded wait (0: kWaitLimitNs)
   int debug_withhold;          // 1 + the stage index whose weight copy the producer never
@@ -103,8 +116,10 @@ cudaError_t launch_dq_gemm(int qbits, int mode, const CUtensorMap& tm_codes,
                            const CUtensorMap& tm_scales, const GemmArgs& a, int grid, int smem,
                            cudaStream_t st);
 
-int tc_smem_bytes(int qbits, int S, int k_chunk, int depth);
+int tc_smem_bytes(int qbits, int S, int k_chunk, int depth, bool route = false);
 bool tc_plan_valid(int qbits, int S, int k_chunk, int depth);
+// The in-prologue MoE routing of the tcgen05 GEMM: its limits
+constexpr int kRouteMaxE = 256, kRouteMaxTopK = 8, kRouteMaxS = 32;
 cudaError_t launch_tc_gemm(int qbits, int mode, const CUtensorMap& tm_codes,
                            const CUtensorMap& tm_scales, const CUtensorMap& tm_codes2,
                            const CUtensorMap& tm_scales2, const GemmArgs& a, int grid, int smem,

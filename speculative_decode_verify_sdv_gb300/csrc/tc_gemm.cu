@@ -40,6 +40,7 @@
 #include <cstdint>
 #include <type_traits>
 
+#include "moe_route.cuh"
 #include "sdv_device.cuh"
 #include "sdv_kernels.h"
 
@@ -74,12 +75,16 @@ struct TcRoles {
 
 struct TcPlan {
   int depth, nmma, xrows, kpad, code_stage, sc_stage;
-  int x_off, ring_off, sc_off, red_off, bar_off, best_off, misc_off, total;
+  int x_off, ring_off, sc_off, red_off, bar_off, best_off, misc_off, route_off, total;
 };
+
+// The in-prologue MoE routing's region: hit count (16 bytes), hit list
+// [kRouteMaxE], picks [kRouteMaxS][kRouteMaxTopK] and their weights.
+constexpr int kRouteBytes = 16 + 4 * kRouteMaxE + 2 * 4 * kRouteMaxS * kRouteMaxTopK;
 
 __host__ __device__ inline int rup(int a, int b) { return (a + b - 1) / b * b; }
 
-__host__ __device__ inline TcPlan tc_plan(int qb, int S, int kc, int depth) {
+__host__ __device__ inline TcPlan tc_plan(int qb, int S, int kc, int depth, bool route = false) {
   TcPlan p;
   p.depth = depth;
   p.nmma = S <= 16 ? 16 : 32;
@@ -99,7 +104,8 @@ __host__ __device__ inline TcPlan tc_plan(int qb, int S, int kc, int depth) {
   // ring full/empty, A buffers afull/afree, tiles tfull/tfree, row slices xready, drain
   p.best_off = p.bar_off + (2 * depth + 2 * kABufs + 4 + p.kpad / 256 + 1) * 8;
   p.misc_off = p.best_off + 4 * 32 * 8;
-  p.total = p.misc_off + 16 + 32 * 4 + 32 * 4;  // flags, argmax [32], drafts [32]
+  p.route_off = rup(p.misc_off + 16 + 32 * 4 + 32 * 4, 16);  // after flags, argmax [32], drafts [32]
+  p.total = p.route_off + (route ? kRouteBytes : 0);
   return p;
 }
 
@@ -205,6 +211,58 @@ __device__ __noinline__ void sample_tail(const GemmArgs& p, uint8_t* stb, const 
 
 // QT: the weight type -- 8 int8, 4 int4, 2 FP4 (E2M1); QB below is its code
 // width in bits (8 or 4), which sets the byte layout of a stage.
+// The MoE window's routing in the prologue of its gate/up launch (GemmArgs
+// route_*): the rows over the CTA's warps (route_row), then a flag per hit
+// expert and one warp's prefix count over the flags give the hit list, experts
+// ascending -- the grouping of moe_route_kernel without its per-expert row
+// lists, which no GEMM reads.  `rt` is the plan's routing region, `scratch`
+// kRouteMaxE ints that are free until the weight stream starts.  CTA 0
+// publishes the picks and the hit list for the down projection.
+__device__ __forceinline__ void route_prologue(const GemmArgs& p, int* rt, int* scratch, int warp, int lane,
+                                               int nwarps) {
+  int* const s_hit = rt + 4;
+  int* const s_ids = s_hit + kRouteMaxE;
+  float* const s_w = reinterpret_cast<float*>(s_ids + kRouteMaxS * kRouteMaxTopK);
+  const int E = p.route_E, K = p.route_top_k;
+  for (int e = threadIdx.x; e < kRouteMaxE; e += blockDim.x) scratch[e] = 0;
+  for (int s = warp; s < p.S; s += nwarps)
+    route_row<kRouteMaxE / 32>(p.route_logits + (size_t)s * E, E, K, lane, s_ids + s * kRouteMaxTopK,
+                               s_w + s * kRouteMaxTopK);
+  __syncthreads();
+  for (int v = threadIdx.x; v < p.S * K; v += blockDim.x) scratch[s_ids[(v / K) * kRouteMaxTopK + v % K]] = 1;
+  __syncthreads();
+  if (warp == 0) {
+    constexpr int kPer = kRouteMaxE / 32;  // experts lane * kPer .. of each lane
+    int f[kPer], c = 0;
+#pragma unroll
+    for (int m = 0; m < kPer; ++m) {
+      f[m] = scratch[lane * kPer + m];
+      c += f[m];
+    }
+    int incl = c;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int o = __shfl_up_sync(0xffffffffu, incl, off);
+      if (lane >= off) incl += o;
+    }
+    int pos = incl - c;
+#pragma unroll
+    for (int m = 0; m < kPer; ++m)
+      if (f[m]) s_hit[pos++] = lane * kPer + m;
+    if (lane == 31) rt[0] = incl;
+  }
+  __syncthreads();
+  if (blockIdx.x == 0 && blockIdx.y == 0) {
+    for (int v = threadIdx.x; v < p.S * K; v += blockDim.x) {
+      const int o = (v / K) * kRouteMaxTopK + v % K;
+      p.route_ids[v] = s_ids[o];
+      p.route_w[v] = s_w[o];
+    }
+    for (int j = threadIdx.x; j < rt[0]; j += blockDim.x) p.route_hit[j] = s_hit[j];
+    if (threadIdx.x == 0) *p.route_n_hit = rt[0];
+  }
+}
+
 template <int QT, int MODE, int NM>
 __global__ void __launch_bounds__(TcRoles<(QT == 8 ? 8 : 4)>::kThreads, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_codes,
@@ -227,8 +285,18 @@ __global__ void __launch_bounds__(TcRoles<(QT == 8 ? 8 : 4)>::kThreads, 1)
   // nothing in global memory is read or written before that grid has completed.
   // Only the MoE mappings need global data (the hit count) up front; other
   // launches set up barriers and tensor memory first, overlapping its tail.
-  const bool dep_early = (p.n_hit != nullptr);
+  const bool routed = (MODE == kModeY) && (p.route_logits != nullptr);  // Y mode only
+  const bool listed = routed || (p.n_hit != nullptr);  // hit-list mappings (MoE)
+  const bool dep_early = listed;
   if (dep_early) griddep_wait();
+  const TcPlan pl = tc_plan(QB, p.S, p.k_chunk, p.depth, routed);
+  int* const s_route = reinterpret_cast<int*>(sb + pl.route_off);  // hit count, hit list, picks, weights
+  if (routed) route_prologue(p, s_route, reinterpret_cast<int*>(sb + pl.ring_off), threadIdx.x >> 5,
+                             threadIdx.x & 31, blockDim.x >> 5);
+  const int* const s_hit = s_route + 4;
+  const int* const s_rids = s_hit + kRouteMaxE;  // [kRouteMaxS][kRouteMaxTopK]
+  const float* const s_rw = reinterpret_cast<const float*>(s_rids + kRouteMaxS * kRouteMaxTopK);
+  auto hit_of = [&](int j) -> int { return routed ? s_hit[j] : __ldg(p.hit + j); };
   // Row and reduction mappings (all uniform over the CTA):
   //  * plain: tile t covers weight rows 128t.., the reduction [k_begin, k_begin + k_len);
   //  * dual: tiles [0, T) read the first matrix, [T, 2T) the second (T tiles each);
@@ -236,9 +304,9 @@ __global__ void __launch_bounds__(TcRoles<(QT == 8 ? 8 : 4)>::kThreads, 1)
   //    experts' row blocks, rows_per_expert rows each;
   //  * expert segments (n_hit and seg_k): the reduction runs over the hit experts'
   //    seg_k columns, segment j reading expert hit[j]'s rows.
-  const bool segs = (p.n_hit != nullptr) && p.seg_k > 0;
-  const bool hit_tiles = (p.n_hit != nullptr) && p.seg_k == 0;
-  const int n_hit = (p.n_hit != nullptr) ? *p.n_hit : 0;
+  const bool segs = listed && p.seg_k > 0;
+  const bool hit_tiles = listed && p.seg_k == 0;
+  const int n_hit = routed ? s_route[0] : (p.n_hit != nullptr) ? *p.n_hit : 0;
   int k_begin, k_len;
   if (segs) {
     const int s_lo = (int)((long)blockIdx.y * n_hit / gridDim.y);
@@ -268,7 +336,7 @@ __global__ void __launch_bounds__(TcRoles<(QT == 8 ? 8 : 4)>::kThreads, 1)
     if (hit_tiles) {
       const int tpe = p.rows_per_expert / kTileRows;
       const int j = lt / tpe;
-      return __ldg(p.hit + j) * p.rows_per_expert + (lt - j * tpe) * kTileRows;
+      return hit_of(j) * p.rows_per_expert + (lt - j * tpe) * kTileRows;
     }
     return lt * kTileRows;
   };
@@ -291,7 +359,6 @@ __global__ void __launch_bounds__(TcRoles<(QT == 8 ? 8 : 4)>::kThreads, 1)
     }
     return;
   }
-  const TcPlan pl = tc_plan(QB, p.S, p.k_chunk, p.depth);
   const int depth = pl.depth;
 
   const uint32_t x_base = base + pl.x_off;
@@ -397,7 +464,7 @@ __global__ void __launch_bounds__(TcRoles<(QT == 8 ? 8 : 4)>::kThreads, 1)
     if (segs) {  // expert segment of this stage (seg_k is a multiple of 256)
       const int kk = k_begin + ks * 256;
       const int j = kk / p.seg_k, col = kk - j * p.seg_k;
-      row0 = __ldg(p.hit + j) * p.rows_per_expert + lt * kTileRows;
+      row0 = hit_of(j) * p.rows_per_expert + lt * kTileRows;
       xb = (QB == 8) ? col : col / 2;
       sc_col = col / 32;
       all_boxes = true;
@@ -640,21 +707,36 @@ __global__ void __launch_bounds__(TcRoles<(QT == 8 ? 8 : 4)>::kThreads, 1)
 #pragma unroll
           for (int n = 0; n < 32; ++n)
             if (n < p.S) red[n * 33 + lane] = acc[n];
-        } else if (valid) {
-          // the routing weights of this tile's expert slot (written by the router
-          // before this grid started): all loaded before the first store of h,
-          // which the compiler could not otherwise move them past
-          const float* const rw = (p.row_w != nullptr) ? p.row_w + lt / tpe : nullptr;
+        } else {
+          // the routing weights of this tile's expert slot, all in registers before
+          // the first store of h (which the compiler could not otherwise move them
+          // past): written by the router before this grid started, or, routed in
+          // this launch, lane n's weight of row n for the slot's expert (zero where
+          // row n did not pick it), passed round the warp
+          const bool weighted = routed || p.row_w != nullptr;
           float wv[32];
+          if (routed) {
+            const int e = s_hit[lt / tpe];
+            float mine = 0.f;
+            if (lane < p.S)
+              for (int i = 0; i < p.route_top_k; ++i)
+                if (s_rids[lane * kRouteMaxTopK + i] == e) mine = s_rw[lane * kRouteMaxTopK + i];
 #pragma unroll
-          for (int n = 0; n < 32; ++n) wv[n] = (rw != nullptr && n < p.S) ? __ldg(rw + (size_t)n * p.ldw) : 1.f;
+            for (int n = 0; n < 32; ++n) wv[n] = __shfl_sync(0xffffffffu, mine, n);
+          } else {
+            const float* const rw = (p.row_w != nullptr) ? p.row_w + lt / tpe : nullptr;
 #pragma unroll
-          for (int n = 0; n < 32; ++n) {
-            if (n < p.S) {
-              const float g = red[n * 33 + lane];
-              float v = g / (1.f + expf(-g)) * acc[n];
-              if (rw != nullptr) v *= wv[n];
-              p.h[(size_t)n * p.ldh + lrow] = __float2half_rn(v);
+            for (int n = 0; n < 32; ++n) wv[n] = (rw != nullptr && n < p.S) ? __ldg(rw + (size_t)n * p.ldw) : 1.f;
+          }
+          if (valid) {
+#pragma unroll
+            for (int n = 0; n < 32; ++n) {
+              if (n < p.S) {
+                const float g = red[n * 33 + lane];
+                float v = g / (1.f + expf(-g)) * acc[n];
+                if (weighted) v *= wv[n];
+                p.h[(size_t)n * p.ldh + lrow] = __float2half_rn(v);
+              }
             }
           }
         }
@@ -1029,8 +1111,8 @@ cudaError_t tc_launch_nm(const TcMaps& m, const GemmArgs& a, int grid, int smem,
 
 }  // namespace
 
-int tc_smem_bytes(int qbits, int S, int k_chunk, int depth) {
-  return tc_plan(qbits, S, k_chunk, depth).total + 1024;
+int tc_smem_bytes(int qbits, int S, int k_chunk, int depth, bool route) {
+  return tc_plan(qbits, S, k_chunk, depth, route).total + 1024;
 }
 
 // The aliased 8-row groups of N read up to one group stride past the staged

@@ -132,9 +132,11 @@ cudaError_t cudaLaunchKernelExC(const cudaLaunchConfig_t* c, const void* fn, voi
   if (name.find("tc_gemm_kernel") != std::string::npos) {
     const sdv::GemmArgs& a = *static_cast<const sdv::GemmArgs*>(args[4]);
     std::printf(" S=%d N=%d K=%d k_chunk=%d splits=%d depth=%d scales_tma=%d n_valid=%d dual=%d seg_k=%d"
-                " rows_per_expert=%d y=%llx h=%llx part_v=%llx part_s=%llx x=%llx",
+                " rows_per_expert=%d y=%llx h=%llx part_v=%llx part_s=%llx x=%llx route=%d route_E=%d"
+                " route_top_k=%d listed=%d",
                 a.S, a.N, a.K, a.k_chunk, a.splits, a.depth, a.scales_tma, a.n_valid, a.dual, a.seg_k,
-                a.rows_per_expert, low(a.y), low(a.h), low(a.part_v), low(a.part_s), low(a.x));
+                a.rows_per_expert, low(a.y), low(a.h), low(a.part_v), low(a.part_s), low(a.x),
+                a.route_logits != nullptr ? 1 : 0, a.route_E, a.route_top_k, a.n_hit != nullptr ? 1 : 0);
   }
   if (name.find("splitk_reduce_kernel") != std::string::npos ||
       name.find("swiglu_reduce_kernel") != std::string::npos)  // first argument: the partials

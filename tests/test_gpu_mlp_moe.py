@@ -253,3 +253,27 @@ def test_moe_identical_experts(sdv):
     x = G.normal(G.stream_seed(721, 902, S), (S, H), 1.0, dtype=np.float64).astype(np.float16)
     one = mlp.expert_swiglu64(x, 0, I, H, T["gate"][0], T["up"][0], T["down"][0])
     assert _rel_l2(out, one) <= 1e-3
+
+
+def test_moe_prologue_routing_matches_router(sdv):
+    """Up to 256 experts and 8 picks the gate/up launch routes the window in its
+    own prologue: its picks and weights (the call's top-k outputs) equal the
+    routing kernel's bit for bit, on logits full of ties."""
+    E, I, H, S, top_k = 256, 256, 256, 17, 8
+    rng = np.random.default_rng(11)
+    logits = rng.integers(0, 3, (S, E)).astype(np.float32)
+    T = _moe_tensors(sdv, 903, E, I, H, 4)
+    x = G.normal(G.stream_seed(721, 903, S), (S, H), 1.0, dtype=np.float64).astype(np.float16)
+    out, ids, wts = _run_moe(sdv, T, E, I, H, top_k, x, logits)
+    rids, rwts = _route_dev(sdv, logits, top_k)[:2]
+    np.testing.assert_array_equal(ids, rids)
+    np.testing.assert_array_equal(wts, rwts)
+    ref = mlp.moe_forward(x, logits, T["gate"][0], T["up"][0], T["down"][0], E, I, H, top_k)[0]
+    assert _rel_l2(out, ref) <= 1e-3
+
+
+@pytest.mark.parametrize("E,top_k", [(320, 4), (64, 12)])
+def test_moe_routing_launch_beyond_prologue_limits(sdv, E, top_k):
+    """More than 256 experts or 8 picks: the routing launch runs first and the
+    gate/up launch reads its hit list."""
+    _moe_case(sdv, 4, 9, E, 256, 256, top_k, seed=904 + E + top_k)

@@ -107,15 +107,26 @@ def test_launch_counter_counts_every_launch(tracer):
 
 
 def test_moe_plan(tracer):
-    # profiles/moe_s17_launches.md: route (one block), gate/up over the hit list
-    # with the SwiGLU epilogue, down over 38 expert-segment slots x 4 CTAs, split sum
+    # gate/up over the hit list with the SwiGLU epilogue, routing the window in
+    # its own prologue (no routing launch), down over 38 expert-segment slots x 4
+    # CTAs reading the hit list gate/up's CTA 0 wrote, split sum
     (c,) = trace(tracer, "moe 4 256 512 2048 8 17")
-    route, gu, dn, red = c["launches"]
-    assert "moe_route_kernel" in route["name"] and grid(route) == (1, 1) and route["block"] == "1024"
+    gu, dn, red = c["launches"]
     assert tc_args(gu) == (4, 0, 32) and grid(gu) == (152, 1) and gu["dual"] == "2"
     assert gu["rows_per_expert"] == "512" and gu["seg_k"] == "0"
+    assert gu["route"] == "1" and gu["route_E"] == "256" and gu["route_top_k"] == "8" and gu["listed"] == "0"
     assert tc_args(dn) == (4, 0, 32) and grid(dn) == (4, 38) and dn["seg_k"] == "512"
+    assert dn["route"] == "0" and dn["listed"] == "1"
     assert "splitk_reduce" in red["name"]
+
+
+def test_moe_plan_beyond_prologue_routing(tracer):
+    # more experts or picks than the prologue routing takes: the routing launch
+    # (one block) runs first and gate/up reads the hit list it wrote
+    (c,) = trace(tracer, "moe 4 1024 256 256 32 9")
+    route, gu = c["launches"][:2]
+    assert "moe_route_kernel" in route["name"] and grid(route) == (1, 1) and route["block"] == "1024"
+    assert tc_args(gu) == (4, 0, 16) and gu["route"] == "0" and gu["listed"] == "1"
 
 
 def test_q4b_head_beyond_one_launch_splits_the_reduction(tracer):
