@@ -455,17 +455,19 @@ __global__ void splitk_reduce_kernel(const float* __restrict__ part, int splits,
   griddep_wait();
   griddep_launch_dependents();
   for (long i = (long)blockIdx.x * blockDim.x + threadIdx.x; i < count; i += (long)gridDim.x * blockDim.x) {
-    // loads in batches of 8 (independent), sums in split order
-    float v = part[i];
-    int sp = 1;
-    for (; sp + 8 <= splits; sp += 8) {
-      float b[8];
+    // loads in batches of 16 (independent, one L2 round trip per batch), sums
+    // in split order
+    float v = 0.f;
+    for (int sp0 = 0; sp0 < splits; sp0 += 16) {
+      float b[16];
 #pragma unroll
-      for (int j = 0; j < 8; ++j) b[j] = __ldcg(part + (long)(sp + j) * count + i);
+      for (int j = 0; j < 16; ++j) b[j] = sp0 + j < splits ? __ldcg(part + (long)(sp0 + j) * count + i) : 0.f;
 #pragma unroll
-      for (int j = 0; j < 8; ++j) v += b[j];
+      for (int j = 0; j < 16; ++j) {
+        if (sp0 + j >= splits) break;
+        v = (sp0 + j == 0) ? b[j] : v + b[j];
+      }
     }
-    for (; sp < splits; ++sp) v += __ldcg(part + (long)sp * count + i);
     y[i] = v;
   }
 }
