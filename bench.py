@@ -682,11 +682,12 @@ def timed_region(job, steps, world, local, sdv, torch):
     return t0.elapsed_time(t1), n_launched, clk
 
 
-# The other full-size workloads a default single-GPU run measures beside the
-# headline one (name:S), so that one driver run records every config's number
-# with its own clocks: the int4 head at the window the pages' cliff is quoted on
-# and at one row, the dense MLP stack and the MoE layer.
-ALSO_DEFAULT = "a3b:17,a3b:1,mlp27:17,moe:17"
+# The other workloads a default single-GPU run measures beside the headline one
+# (name:S), so that one driver run records every config's number with its own
+# clocks: the int4 head at the window the pages' cliff is quoted on and at one
+# row, the dense MLP stack, the MoE layer, and the L2-resident tiny head (with
+# its CUDA-graph number).
+ALSO_DEFAULT = "a3b:17,a3b:1,mlp27:17,moe:17,tiny:9"
 
 
 def also_specs(args, world) -> list:
@@ -708,6 +709,41 @@ def also_specs(args, world) -> list:
     return out
 
 
+L2_BYTES = 129e6  # the GB300's L2
+
+
+def l2_label(nbytes: float) -> str:
+    if nbytes > L2_BYTES:
+        return "inputs larger than L2 (weight stream %.0f MB > 129 MB)" % (nbytes / 1e6)
+    return "L2-warm: the working set (%.2f MB) fits the 129 MB L2; not an HBM number" % (nbytes / 1e6)
+
+
+def graph_record(job, steps, nbytes, torch, replays=10) -> dict:
+    """The secondary back-to-back number: `steps` windows captured once as a CUDA
+    graph (the library's launches keep their programmatic dependencies as graph
+    edges) and replayed `replays` times between two events on the stream."""
+    try:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for i in range(steps):
+                job.step(i)
+        g.replay()
+        torch.cuda.synchronize()
+        stream = torch.cuda.current_stream()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(replays):
+            g.replay()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        per = e0.elapsed_time(e1) / (replays * steps)
+        del g
+    except Exception as exc:  # a capture the runtime refuses: say why, keep the line
+        return {"unavailable": f"{type(exc).__name__}: {exc}"[:200]}
+    return {"value": 1000.0 / per, "unit": "windows/s", "ms_per_step": per, "windows_per_graph": steps,
+            "replays": replays, "l2": l2_label(nbytes)}
+
+
 def measure_also(args, specs, sdv, torch, dev, local) -> list:
     """Each (workload, S): warm-up, the timed region (as the headline line),
     a status check; one compact record per workload."""
@@ -725,10 +761,15 @@ def measure_also(args, specs, sdv, torch, dev, local) -> list:
         nbytes = float(np.mean([job.bytes(i) for i in range(args.steps)]))
         per = ms / args.steps
         achieved = nbytes / (per / 1000.0) / 1e9
-        out.append({"workload": workload_name(wl, S), "S": S, "value": 1000.0 / per, "unit": "windows/s",
-                    "ms_per_step": per, "bytes_per_window": nbytes, "weight_gbs": achieved,
-                    "hbm_frac": achieved / peak, "peak_kind": kind, "gpu_launches": n_launched,
-                    "kernel": f"{job.kernel} ({args.path} path)", "clocks": clk.summary()})
+        rec = {"workload": workload_name(wl, S), "S": S, "value": 1000.0 / per, "unit": "windows/s",
+               "ms_per_step": per, "bytes_per_window": nbytes, "l2": l2_label(nbytes), "weight_gbs": achieved,
+               "hbm_frac": achieved / peak, "peak_kind": kind, "gpu_launches": n_launched,
+               "kernel": f"{job.kernel} ({args.path} path)", "clocks": clk.summary()}
+        if wl.kind == "head":
+            rec["graph"] = graph_record(job, args.steps, nbytes, torch)
+            if not all(sdv.sdv_last_device_status(w) == sdv.SDV_OK for w in job.ws_list):
+                raise RuntimeError(f"device status reported an error in the graph replays of {wl.name} S={S}")
+        out.append(rec)
         del job
         torch.cuda.synchronize()
         torch.cuda.empty_cache()
@@ -806,7 +847,7 @@ def run_sdv(args, wl, S, world, rank, local):
         "scaling": "weak", "vs_baseline": None, "dtype": "f16 x %s -> f32" % wtype(wl.bits), "data": "synthetic",
         "config": {"workload": workload_name(wl, S) + (", sampling verify T=1" if sampling else ""), "S": S,
                    "windows": nwin, "bytes_per_window": nbytes,
-                   "l2": "inputs larger than L2 (weight stream %.0f MB > 129 MB)" % (nbytes / 1e6),
+                   "l2": l2_label(nbytes),
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "weight_gbs": achieved, "hbm_frac": achieved / peak,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
@@ -819,6 +860,10 @@ def run_sdv(args, wl, S, world, rank, local):
         "gpu_launches": n_launched,
         "clocks": clk.summary(),
     }
+    if wl.kind == "head":
+        line["graph"] = graph_record(job, args.steps, nbytes, torch)
+        if not status_ok():
+            raise RuntimeError("device status reported an error in the graph replays")
     if also:
         line["also_measured"] = also
     print(json.dumps(line))

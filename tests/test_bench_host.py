@@ -143,11 +143,12 @@ def _args(**kw):
     return bench.argparse.Namespace(**base)
 
 
-def test_also_measured_defaults_to_the_other_full_size_workloads():
+def test_also_measured_defaults_to_the_other_workloads():
     # the default single-GPU run also times the int4 head (S = 17 and 1), the
-    # dense MLP stack and the MoE layer; any other run measures only its own line
+    # dense MLP stack, the MoE layer and the L2-resident tiny head; any other run
+    # measures only its own line
     got = [(wl.name, S) for wl, S in bench.also_specs(_args(), 1)]
-    assert got == [("a3b", 17), ("a3b", 1), ("mlp27", 17), ("moe", 17)]
+    assert got == [("a3b", 17), ("a3b", 1), ("mlp27", 17), ("moe", 17), ("tiny", 9)]
     assert bench.also_specs(_args(), 2) == []
     assert bench.also_specs(_args(config="a3b"), 1) == []
     assert bench.also_specs(_args(fp4=True), 1) == []
@@ -156,3 +157,10 @@ def test_also_measured_defaults_to_the_other_full_size_workloads():
     assert [(wl.name, S) for wl, S in bench.also_specs(_args(also="mlp27:9, a3b"), 1)] == [("mlp27", 9), ("a3b", 17)]
     with pytest.raises(SystemExit):
         bench.also_specs(_args(also="nosuch:3"), 1)
+
+
+def test_l2_label_separates_l2_warm_from_hbm():
+    # the tiny head's 1.12 MB fits the 129 MB L2: its numbers are labelled
+    # L2-warm, never HBM; the full-size weight streams are larger than L2
+    assert bench.l2_label(1.12e6).startswith("L2-warm")
+    assert bench.l2_label(286e6).startswith("inputs larger than L2")
