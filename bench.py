@@ -914,7 +914,8 @@ def run_spec_loop(args, wl, S):
         "E_alpha_K": specdec.expected_tokens_per_round(alpha, K), "K": K, "ngram": args.ngram,
         "gen": args.gen, "p_echo": args.p_echo,
         "config": {"workload": workload_name(wl, S), "S": S, "model_body": "synth.toy_model.ToyHidden (period 5)"},
-        "timing": "host wall clock around each whole decode (H2D of the window, the call, D2H, sync per round)",
+        "timing": "host wall clock around each whole decode (per round: H2D of the window, the call, D2H, "
+                  "one stream sync; the round's GPU work replayed as a CUDA graph per window size)",
     }
     print(json.dumps(line), flush=True)
     return 0 if line["lossless"] else 1

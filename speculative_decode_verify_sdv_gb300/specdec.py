@@ -82,11 +82,20 @@ class HeadVerifier:
     ``x [S, k]`` and the drafts through pinned host buffers, runs the fused
     head GEMM + argmax + accept on ``stream`` and returns
     ``(argmax int32 [S], accepted, next_a0)`` once the stream has finished.
+
+    With ``graph`` (the default) a round's GPU work -- the two host-to-device
+    copies, the verify launch, the copy of the results back -- is captured once
+    per window size as a CUDA graph and replayed: a round then costs the host
+    one replay and one stream synchronisation instead of the per-call work of
+    the copies and the library call.  The graph bakes in n_valid = S - 1: the
+    drafts past the real n_valid are -1, which no argmax equals, so the accept
+    stops at the same place.
     """
 
-    def __init__(self, head: sdv.QWeight, s_max: int, device="cuda", stream: torch.cuda.Stream | None = None):
-        self.head, self.s_max = head, s_max
-        self.stream = stream if stream is not None else torch.cuda.current_stream(device)
+    def __init__(self, head: sdv.QWeight, s_max: int, device="cuda", stream: torch.cuda.Stream | None = None,
+                 graph: bool = True):
+        self.head, self.s_max, self.graph = head, s_max, graph
+        self.stream = stream if stream is not None else torch.cuda.Stream(device)
         self.ws = sdv.workspace(sdv.SDV_OP_VERIFY_HEAD, head.n, head.k, s_max, device=device)
         self.x_d = torch.empty((s_max, head.k), dtype=torch.float16, device=device)
         self.dr_d = torch.zeros(max(s_max - 1, 1), dtype=torch.int32, device=device)
@@ -94,7 +103,17 @@ class HeadVerifier:
         self.x_h = torch.empty((s_max, head.k), dtype=torch.float16).pin_memory()
         self.dr_h = torch.zeros(max(s_max - 1, 1), dtype=torch.int32).pin_memory()
         self.out_h = torch.empty(s_max + 2, dtype=torch.int32).pin_memory()
+        self.graphs: dict[int, torch.cuda.CUDAGraph] = {}
         self.calls = 0
+
+    def _round(self, S: int, n_valid: int) -> None:
+        """The GPU work of one round, on the current stream."""
+        self.x_d[:S].copy_(self.x_h[:S], non_blocking=True)
+        if S > 1:
+            self.dr_d[:S - 1].copy_(self.dr_h[:S - 1], non_blocking=True)
+        am, acc, nxt = self.out_d[:S], self.out_d[self.s_max:self.s_max + 1], self.out_d[self.s_max + 1:]
+        sdv.sdv_verify_head(self.head, self.x_d[:S], S, self.dr_d, n_valid, None, am, acc, nxt, self.ws)
+        self.out_h.copy_(self.out_d, non_blocking=True)
 
     def __call__(self, x: np.ndarray, drafts: Sequence[int], n_valid: int):
         S = x.shape[0]
@@ -102,15 +121,23 @@ class HeadVerifier:
             raise ValueError(f"window of {S} rows, at most {self.s_max}")
         self.x_h[:S].numpy()[...] = np.asarray(x, dtype=np.float16)
         if S > 1:
-            self.dr_h[:S - 1].numpy()[...] = np.asarray(drafts, dtype=np.int32)[:S - 1]
+            d = self.dr_h[:S - 1].numpy()
+            d[...] = np.asarray(drafts, dtype=np.int32)[:S - 1]
+            if self.graph:
+                d[n_valid:] = -1
         with torch.cuda.stream(self.stream):
-            self.x_d[:S].copy_(self.x_h[:S], non_blocking=True)
-            if S > 1:
-                self.dr_d[:S - 1].copy_(self.dr_h[:S - 1], non_blocking=True)
-            am, acc, nxt = self.out_d[:S], self.out_d[self.s_max:self.s_max + 1], self.out_d[self.s_max + 1:]
-            sdv.sdv_verify_head(self.head, self.x_d[:S], S, self.dr_d, n_valid, None, am, acc, nxt, self.ws,
-                                stream=self.stream)
-            self.out_h.copy_(self.out_d, non_blocking=True)
+            if not self.graph:
+                self._round(S, n_valid)
+            else:
+                g = self.graphs.get(S)
+                if g is None:
+                    self._round(S, S - 1)  # outside the capture first: plans, tensor maps, attributes
+                    self.stream.synchronize()
+                    g = torch.cuda.CUDAGraph()
+                    with torch.cuda.graph(g, stream=self.stream):
+                        self._round(S, S - 1)
+                    self.graphs[S] = g
+                g.replay()
         self.stream.synchronize()
         self.calls += 1
         o = self.out_h.numpy()

@@ -77,3 +77,26 @@ def test_row_logits_independent_of_window(sdv, bits, k):
     ref = verify.dequant_gemm64(x[:17], codes, scales)
     rms = float(np.sqrt(np.mean(ref ** 2)))
     assert float(np.max(np.abs(got - alone))) <= 2e-3 * np.sqrt(k / 256.0) * rms
+
+
+@pytest.mark.parametrize("bits,k", [(8, 2560), (4, 2048)])
+def test_graph_rounds_match_direct_calls(sdv, bits, k):
+    """The verifier's replayed CUDA graph (n_valid baked in as S - 1, drafts past
+    the real n_valid set to -1) returns what a direct call with the real n_valid
+    returns, over windows whose drafts partly match the argmax chain."""
+    n, S = 3000, 9
+    _, codes, scales, qw = _head(n, k, bits, 11)
+    direct = specdec.HeadVerifier(qw, S, graph=False)
+    graphed = specdec.HeadVerifier(qw, S, graph=True)
+    rng = np.random.default_rng(12)
+    for case in range(24):
+        x = G.normal(G.stream_seed(964, case, k), (S, k), 1.0, dtype=np.float64).astype(np.float16)
+        chain = direct(x, [0] * (S - 1), 0)[0]
+        drafts = list(chain[:S - 1])
+        cut = int(rng.integers(0, S))
+        if cut < S - 1:
+            drafts[cut] = (drafts[cut] + 1) % n  # a miss at `cut`
+        n_valid = int(rng.integers(0, S))
+        a = direct(x, drafts, n_valid)
+        b = graphed(x, drafts, n_valid)
+        assert np.array_equal(a[0], b[0]) and a[1:] == b[1:], (case, n_valid, a[1:], b[1:])
