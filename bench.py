@@ -486,6 +486,9 @@ class HeadJob:
         self.dr = np.ascontiguousarray(dr.reshape(nwin, -1))
         self.d_dev = torch.from_numpy(self.dr).to(dev)
         self.n_valid = S - 1
+        # each window's argument views, made once (a view per call costs the host
+        # more than the tiny head's kernel)
+        self.win = [(self.x_dev[j], self.d_dev[j], self.am[j], self.acc[j], self.nxt[j]) for j in range(nwin)]
         self.kernel = "verify-head GEMM + argmax + accept (one launch)"
         self.ws_list = [self.ws]
 
@@ -493,9 +496,8 @@ class HeadJob:
         return head_bytes(self.wl, self.S)
 
     def step(self, i):
-        j = i % self.nwin
-        self.sdv.sdv_verify_head(self.head, self.x_dev[j], self.S, self.d_dev[j], self.n_valid, None, self.am[j],
-                                 self.acc[j], self.nxt[j], self.ws)
+        x, d, am, acc, nxt = self.win[i % self.nwin]
+        self.sdv.sdv_verify_head(self.head, x, self.S, d, self.n_valid, None, am, acc, nxt, self.ws)
 
     def e2e_setup(self):
         # one pinned host record per window (hidden states, then drafts) and one
@@ -535,9 +537,8 @@ class SampleJob(HeadJob):
         self.kernel = "sampling verify: GEMM + Gumbel-max draws + softmax + accept (one launch)"
 
     def step(self, i):
-        j = i % self.nwin
-        self.sdv.sdv_verify_sample(self.head, self.x_dev[j], self.S, self.d_dev[j], self.n_valid, 1.0, 1, i, None,
-                                   self.am[j], self.acc[j], self.nxt[j], self.ws)
+        x, d, am, acc, nxt = self.win[i % self.nwin]
+        self.sdv.sdv_verify_sample(self.head, x, self.S, d, self.n_valid, 1.0, 1, i, None, am, acc, nxt, self.ws)
 
     def e2e_step(self, i):
         j, S = i % self.nwin, self.S
@@ -578,7 +579,9 @@ class MlpJob:
 
     def step(self, i):
         j = i % self.nwin
-        self._call(self.x_dev[j], self.y[j])
+        if not hasattr(self, "win"):
+            self.win = [(self.x_dev[w], self.y[w]) for w in range(self.nwin)]
+        self._call(*self.win[j])
 
     def e2e_setup(self):
         t = self.torch
@@ -630,7 +633,9 @@ class MoeJob:
 
     def step(self, i):
         j = i % self.nwin
-        self._call(self.x_dev[j], self.l_dev[j], self.out[j])
+        if not hasattr(self, "win"):
+            self.win = [(self.x_dev[w], self.l_dev[w], self.out[w]) for w in range(self.nwin)]
+        self._call(*self.win[j])
 
     def e2e_setup(self):
         # one pinned host record per window (hidden states, then router logits)
