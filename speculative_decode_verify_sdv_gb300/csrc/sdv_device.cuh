@@ -157,25 +157,45 @@ __device__ __forceinline__ uint32_t and_xor(uint32_t a, uint32_t flip) {
   return d;
 }
 
-// Eight signed int4 codes n0..n7 -> the fp16 pairs of n * s (same pairing as
-// i4x8_to_h2x4), one shift per word.  Pairs (n1, n5) and (n3, n7), at bits 4-7
-// of each half of w and of w >> 8, take scale and bias in one HFMA2: the LOP3
-// that masks a code also flips its top bit, giving u = n + 8 in [0, 15], which
-// reads as the subnormal u * 2^-20 (exact); fma(u * 2^-20, m, c) with
-// m = s * 2^20 and c = -8 s is u * s - 8 s = n * s computed exactly and rounded
-// once.  Pairs (n0, n4) and (n2, n6), at bits 0-3, take the exponent-bias form
-// of i4x8_to_h2x4 (exact n, then times s, rounded once).  Every pair gets the
-// bits of fp16(n) * s from the two-step form.  Valid while m is finite
-// (s <= 65504 * 2^-20); m, c and s in both halves.
-__device__ __forceinline__ void i4x8_to_h2x4_scaled(uint32_t w, __half2 m, __half2 c, __half2 s, uint32_t& p0,
-                                                    uint32_t& p1, uint32_t& p2, uint32_t& p3) {
-  const uint32_t flip = 0x00800080u;  // the top bit of a code placed at bits 4-7 of each half
-  const __half2 b_lo = u32_as_h2(0x64086408u);  // (1032, 1032)
+// The tcgen05 converters' int4 forms.  Eight signed int4 codes n0..n7 of a
+// 32-bit word give the fp16 pairs (n0, n4), (n1, n5), (n2, n6), (n3, n7) -- the
+// pairing of i4x8_to_h2x4 -- with (n0, n4) and (n2, n6) scaled by 2^-4: those
+// codes sit at bits 0-3 of each half of w and of w >> 8, and taking them there
+// needs the 2^-4 (their accumulators are scaled back by 16 in the epilogue).
+// The LOP3 that masks a code also flips its top bit, giving u = n + 8 in
+// [0, 15].  One-FMA form: a code at bits 4-7 reads as the subnormal u * 2^-20,
+// one at bits 0-3 as u * 2^-24 (both exact); fma with m = s * 2^20 and
+// c = -8 s, resp. c_lo = -s / 2, gives n * s, resp. n * s / 16, computed
+// exactly and rounded once.  Valid while m is finite (s <= 65504 * 2^-20) and
+// s / 2 is exact (s = 0 or s >= 2^-13); m, c, c_lo in both halves.
+__device__ __forceinline__ void i4x8_to_h2x4_split(uint32_t w, __half2 m, __half2 c, __half2 c_lo, uint32_t& p0,
+                                                   uint32_t& p1, uint32_t& p2, uint32_t& p3) {
+  const uint32_t flip_hi = 0x00800080u, flip_lo = 0x00080008u;  // the top bit of a code at bits 4-7 / 0-3
   const uint32_t y = w >> 8;
-  p0 = h2_as_u32(__hmul2(__hsub2(u32_as_h2(and_xor<0x000F000Fu>(w, 0x64086408u)), b_lo), s));  // (n0, n4)
-  p1 = h2_as_u32(__hfma2(u32_as_h2(and_xor<0x00F000F0u>(w, flip)), m, c));                      // (n1, n5)
-  p2 = h2_as_u32(__hmul2(__hsub2(u32_as_h2(and_xor<0x000F000Fu>(y, 0x64086408u)), b_lo), s));  // (n2, n6)
-  p3 = h2_as_u32(__hfma2(u32_as_h2(and_xor<0x00F000F0u>(y, flip)), m, c));                      // (n3, n7)
+  p0 = h2_as_u32(__hfma2(u32_as_h2(and_xor<0x000F000Fu>(w, flip_lo)), m, c_lo));  // (n0, n4) / 16
+  p1 = h2_as_u32(__hfma2(u32_as_h2(and_xor<0x00F000F0u>(w, flip_hi)), m, c));     // (n1, n5)
+  p2 = h2_as_u32(__hfma2(u32_as_h2(and_xor<0x000F000Fu>(y, flip_lo)), m, c_lo));  // (n2, n6) / 16
+  p3 = h2_as_u32(__hfma2(u32_as_h2(and_xor<0x00F000F0u>(y, flip_hi)), m, c));     // (n3, n7)
+}
+
+// The same pairs as exact fp16 values before the scale, (n0, n4) and (n2, n6)
+// as n / 16: the exponent-bias form of i4x8_to_h2x4 with (1024 + u) / 16 - 64.5
+// = n / 16 (exact) for those two pairs; times s (HMUL2) they round once, to the
+// bits of the one-FMA form.
+__device__ __forceinline__ void i4x8_to_h2x4_split_exact(uint32_t w, uint32_t& p0, uint32_t& p1, uint32_t& p2,
+                                                         uint32_t& p3) {
+  const __half2 sixteenth = u32_as_h2(0x2C002C00u);  // (1/16, 1/16)
+  const __half2 b_lo = u32_as_h2(0xD408D408u);       // (-64.5, -64.5)
+  const __half2 b_hi = u32_as_h2(0xD480D480u);       // (-72, -72)
+  const uint32_t y = w >> 8;
+  const uint32_t t0 = (w & 0x000F000Fu) ^ 0x64086408u;
+  const uint32_t t1 = (w & 0x00F000F0u) ^ 0x64806480u;
+  const uint32_t t2 = (y & 0x000F000Fu) ^ 0x64086408u;
+  const uint32_t t3 = (y & 0x00F000F0u) ^ 0x64806480u;
+  p0 = h2_as_u32(__hfma2(u32_as_h2(t0), sixteenth, b_lo));
+  p1 = h2_as_u32(__hfma2(u32_as_h2(t1), sixteenth, b_hi));
+  p2 = h2_as_u32(__hfma2(u32_as_h2(t2), sixteenth, b_lo));
+  p3 = h2_as_u32(__hfma2(u32_as_h2(t3), sixteenth, b_hi));
 }
 
 // Counter stream of the sampling verify: SplitMix64 (Steele, Lea & Flood,

@@ -575,11 +575,20 @@ __global__ void __launch_bounds__(TcRoles<(QT == 8 ? 8 : 4)>::kThreads, 1)
             o.y = __byte_perm(x4.x, x4.y, 0x7632);
             o.z = __byte_perm(x4.z, x4.w, 0x5410);
             o.w = __byte_perm(x4.z, x4.w, 0x7632);
-          } else {  // per 8 elements: (k0, k4, k1, k5, k2, k6, k3, k7)
+          } else {  // int4, per 8 elements (word j of a 32-block): pairs (k0, k4), (k1, k5), (k2, k6), (k3, k7)
             o.x = __byte_perm(x4.x, x4.z, 0x5410);
             o.y = __byte_perm(x4.x, x4.z, 0x7632);
             o.z = __byte_perm(x4.y, x4.w, 0x5410);
             o.w = __byte_perm(x4.y, x4.w, 0x7632);
+            // the converters put a block's (k0, k4) and (k2, k6) pairs in its first
+            // eight columns (the first MMA of the block) and (k1, k5), (k3, k7) in
+            // the last eight: word j's pairs go to columns 2j, 2j + 1 and 8 + 2j,
+            // 9 + 2j, 4 columns (16 bytes) per core-matrix row
+            const int j = g8 & 3, blk0 = g8 - j;
+            uint8_t* const row = sb + pl.x_off + (n >> 3) * sbo + (n & 7) * 16 + (j & 1) * 8;
+            *reinterpret_cast<uint2*>(row + (blk0 + (j >> 1)) * 128) = make_uint2(o.x, o.z);
+            *reinterpret_cast<uint2*>(row + (blk0 + 2 + (j >> 1)) * 128) = make_uint2(o.y, o.w);
+            continue;
           }
           *reinterpret_cast<uint4*>(sb + pl.x_off + (n >> 3) * sbo + g8 * 128 + (n & 7) * 16) = o;
         }
@@ -679,19 +688,23 @@ __global__ void __launch_bounds__(TcRoles<(QT == 8 ? 8 : 4)>::kThreads, 1)
       float acc[32];
 #pragma unroll
       for (int n = 0; n < 32; ++n) acc[n] = 0.f;
+      // int4: the even MMAs of a block (into the even accumulators) carry the
+      // pairs the converters scaled by 2^-4, so those accumulators count 16-fold
+      // (an exact power of two)
 #pragma unroll
       for (int j = 0; j < kAcc; ++j) {
         const uint32_t col = (uint32_t)(kACols + (tb * kAcc + j) * NM);
+        const float wj = (QT == 4 && (j & 1) == 0) ? 16.f : 1.f;
         uint32_t v[16];
         tmem_ld16(tmem + lane_base + col, v);
         tmem_wait_ld();
 #pragma unroll
-        for (int n = 0; n < 16; ++n) acc[n] += __uint_as_float(v[n]);
+        for (int n = 0; n < 16; ++n) acc[n] = fmaf(wj, __uint_as_float(v[n]), acc[n]);
         if (NM == 32) {
           tmem_ld16(tmem + lane_base + col + 16, v);
           tmem_wait_ld();
 #pragma unroll
-          for (int n = 0; n < 16; ++n) acc[16 + n] += __uint_as_float(v[n]);
+          for (int n = 0; n < 16; ++n) acc[16 + n] = fmaf(wj, __uint_as_float(v[n]), acc[16 + n]);
         }
       }
       tc_fence_before();
@@ -962,17 +975,22 @@ __global__ void __launch_bounds__(TcRoles<(QT == 8 ? 8 : 4)>::kThreads, 1)
                 for (int j = 0; j < 8; ++j) i8x4_to_h2x2(wv[j], cols[2 * j], cols[2 * j + 1]);
               }
             } else if (QT == 4) {
+              // word j's (n0, n4), (n2, n6) pairs (scaled by 2^-4) to columns 2j,
+              // 2j + 1 (the block's first MMA, accumulated into the accumulators
+              // the epilogue scales by 16), (n1, n5), (n3, n7) to 8 + 2j, 9 + 2j
               const uint32_t wv[4] = {wreg[blk].x, wreg[blk].y, wreg[blk].z, wreg[blk].w};
               if constexpr (kFma) {
                 const __half2 m2 = __hmul2(__hmul2(s2, __float2half2_rn(1024.f)), __float2half2_rn(1024.f));
                 const __half2 c2 = __hmul2(s2, __float2half2_rn(-8.f));
+                const __half2 clo2 = __hmul2(s2, __float2half2_rn(-0.5f));
 #pragma unroll
                 for (int j = 0; j < 4; ++j)
-                  i4x8_to_h2x4_scaled(wv[j], m2, c2, s2, cols[4 * j], cols[4 * j + 1], cols[4 * j + 2], cols[4 * j + 3]);
+                  i4x8_to_h2x4_split(wv[j], m2, c2, clo2, cols[2 * j], cols[8 + 2 * j], cols[2 * j + 1],
+                                     cols[9 + 2 * j]);
               } else {
 #pragma unroll
                 for (int j = 0; j < 4; ++j)
-                  i4x8_to_h2x4(wv[j], cols[4 * j], cols[4 * j + 1], cols[4 * j + 2], cols[4 * j + 3]);
+                  i4x8_to_h2x4_split_exact(wv[j], cols[2 * j], cols[8 + 2 * j], cols[2 * j + 1], cols[9 + 2 * j]);
               }
             } else {  // FP4: the hardware E2M1 -> f16x2 conversion, one byte (two codes) at a time
               const uint32_t wv[4] = {wreg[blk].x, wreg[blk].y, wreg[blk].z, wreg[blk].w};
@@ -993,9 +1011,13 @@ __global__ void __launch_bounds__(TcRoles<(QT == 8 ? 8 : 4)>::kThreads, 1)
       bool fma_form = false;
       if ((QT == 4 || QT == 8) && ok) {
         constexpr uint32_t kMaxBits = (QT == 4) ? 0x2BFFu : 0x1BFFu;  // the largest scale in range
+        // int4 also needs s / 2 exact: s = 0 or s >= 2^-13 (fp16 bits 0x0800)
+        auto in_range = [](uint32_t b) {
+          return b <= kMaxBits && (QT != 4 || b == 0u || b >= 0x0800u);
+        };
         bool small = true;
 #pragma unroll
-        for (int w = 0; w < 4; ++w) small = small && (sc_w[w] & 0xFFFFu) <= kMaxBits && (sc_w[w] >> 16) <= kMaxBits;
+        for (int w = 0; w < 4; ++w) small = small && in_range(sc_w[w] & 0xFFFFu) && in_range(sc_w[w] >> 16);
         fma_form = __all_sync(0xffffffffu, small);
       }
       if (fma_form)

@@ -2,10 +2,12 @@
 same bits.
 
 Where every row of a warp's 32-row slab has its block scales in range (int4:
-s <= 65504 * 2^-20, max |w| <= ~0.44 per block; int8: s <= 65504 * 2^-24,
-max |w| <= ~0.5) the converters apply scale and bias in one fp16 FMA on the
-code placed in the subnormal range; a slab with any larger scale takes the
-two-step form (exact code, then times s).  Both round n * s once, so
+2^-13 <= s <= 65504 * 2^-20 or s = 0, i.e. max |w| <= ~0.44 per block; int8:
+s <= 65504 * 2^-24, max |w| <= ~0.5) the converters apply scale and bias in one
+fp16 FMA on the code placed in the subnormal range; a slab with any scale out
+of range takes the two-step form (exact code, then times s).  (int4 holds the
+codes at bits 0-3 of a half as fp16(n * s / 16) in both forms; their
+accumulators are scaled back by 16.)  Both round n * s once, so
 a row's logits must not depend on which form its slab took: the same head is
 run as is (every slab on the one-FMA form) and with the first row of every
 32-row slab scaled up (those slabs on the two-step form), and the logits of the
@@ -78,3 +80,33 @@ def test_int4_y_mode_large_scales(sdv):
         sdv.sdv_qlinear(qw, to_dev_f16(x), S, y, ws)
         assert sdv.sdv_last_device_status(ws) == sdv.SDV_OK
     assert_gemm_close(y.cpu().numpy(), verify.dequant_gemm64(x, codes, scales), k, "Y, large scales")
+
+
+@pytest.mark.parametrize("S", [1, 17])
+def test_int4_small_scales_take_the_two_step_form(sdv, S):
+    """int4 slabs with a block scale below 2^-13 (s / 2 not exact) take the
+    two-step form; both forms hold the pairs at bits 0-3 as fp16(n * s / 16),
+    so the rows the two runs share agree bit for bit.  The tiny rows' own
+    values carry the fp16 subnormal spacing of n * s / 16 (2^-24, i.e. 2^-20
+    once the accumulator is scaled back): within the parity bound relative to
+    the logits of the whole head, as the contract states it."""
+    n, k = 4096, 2048
+    w = G.normal(G.stream_seed(1320, n, k), (n, k), 0.02)
+    small = w.copy()
+    small[::32] /= 300.0  # first row of every 32-row slab: scales ~2e-5, below 2^-13
+    x = G.normal(G.stream_seed(1321, n, k, S), (S, k), 1.0, dtype=np.float64).astype(np.float16)
+    drafts = np.zeros(max(S - 1, 0), np.int32)
+    keep = np.ones(n, bool)
+    keep[::32] = False
+    out = {}
+    with gemm_path("tc"):
+        for name, wm in (("plain", w), ("small", small)):
+            codes, scales, stored = oracle_weight(wm, 4)
+            if name == "small":
+                assert float(np.max(scales[::32].astype(np.float32))) < 2.0 ** -13
+            head = device_weight(stored, scales, 4, n, k)
+            logits, am, acc, nxt = run_head(head, x, drafts, 0)
+            ref = verify.verify_head(x, codes, scales, drafts, 0)
+            assert_gemm_close(logits, ref["logits"], k, f"{name} logits (whole head)")
+            out[name] = logits
+    np.testing.assert_array_equal(out["plain"][:, keep], out["small"][:, keep])
