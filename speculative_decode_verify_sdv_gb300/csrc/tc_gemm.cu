@@ -11,26 +11,26 @@
 //   warp 0        TMA producer: 128-row x 256-element stages of codes (128-byte
 //                 swizzled boxes) and their fp16 scales into a shared-memory ring;
 //   warp 1        allocates tensor memory and issues every tcgen05.mma (one
-//                 thread), committing completion to mbarriers;
+//                 elected thread per stage), committing completion to mbarriers;
 //   warps 2-5     tile epilogue, one per tensor-memory lane quarter;
-//   warps 6..     4*G converter warps: group g (warps 6+4g .. 9+4g) converts blocks
-//                 [8g/G, 8(g+1)/G) of every stage; warp w serves tensor-memory lane
+//   warps 6..     4*G converter warps: group g (warps 6+4g .. 9+4g) converts the
+//                 whole stages g, g+G, g+2G, ...; warp w serves tensor-memory lane
 //                 quarter w % 4 (rows 32q..32q+31 of the tile) and each thread owns
-//                 one weight row.  Codes become exact fp16 integers, are multiplied
-//                 by the block's fp16 scale (one rounding: q*s to fp16) and stored
-//                 into tensor memory as the A operand (M = 128 rows, K = 16 per
-//                 MMA).  The window rows are the B operand (N = 16 or 32), staged
-//                 once in shared memory in the K-major core-matrix layout with the
-//                 reduction index permuted like the converted codes.
+//                 one weight row.  Codes become fp16 n*s, rounded once (one-FMA or
+//                 two-step form, the same bits; int4 codes at bits 0-3 of a half
+//                 as n*s/16), stored into tensor memory as the A operand (M = 128
+//                 rows, K = 16 per MMA).  The window rows are the B operand (N = 16
+//                 or 32), staged once in shared memory in the K-major core-matrix
+//                 layout, the reduction index permuted like the converted codes.
 //   The MMAs of a 128-row tile accumulate in fp32 tensor memory (double-buffered
 //   across tiles); the epilogue warps load the result (tcgen05.ld) while the next
 //   tile streams and write Y, or reduce the verify head's per-row
 //   (max, lowest index) through shared memory.  The MMA warp runs a
-//   warp-uniform loop and one elected lane issues each MMA.
-// Tensor memory: columns 0-255 hold A (2 stage buffers x 8 blocks x 16 columns),
-// columns 256.. two tile buffers of 4 accumulators (N columns each): the MMAs of
-// a tile rotate over the 4 so that consecutive MMAs do not depend on each other,
-// and the epilogue adds the 4.
+//   warp-uniform loop and one elected lane issues each stage's MMAs.
+// Tensor memory: columns 0-383 hold A (3 stage buffers x 8 blocks x 16 columns),
+// columns 384.. two tile buffers of kAcc accumulators (N columns each): a tile's
+// MMAs rotate over them so that consecutive MMAs do not depend on each other,
+// and the epilogue adds them (int4: the even ones 16-fold).
 #include <cuda.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -933,8 +933,8 @@ __global__ void __launch_bounds__(TcRoles<(QT == 8 ? 8 : 4)>::kThreads, 1)
       // branch per block inside the unrolled loop costs more than it saves):
       // integer codes with scale and bias in one HFMA2 per pair where every
       // row's eight block scales are in range -- int4: s * 2^20 <= 65504 (fp16
-      // bits <= 0x2BFF), int8: s * 2^24 <= 65504 (bits <= 0x1BFF), the common
-      // case -- else the two-step form; both give the same bits.
+      // bits <= 0x2BFF) and s / 2 exact, int8: s * 2^24 <= 65504 (bits <=
+      // 0x1BFF), the common case -- else the two-step form; the same bits.
       auto convert = [&](auto fma_tag) {
         constexpr bool kFma = decltype(fma_tag)::value;
 #pragma unroll
