@@ -209,8 +209,6 @@ __device__ __noinline__ void sample_tail(const GemmArgs& p, uint8_t* stb, const 
   }
 }
 
-// QT: the weight type -- 8 int8, 4 int4, 2 FP4 (E2M1); QB below is its code
-// width in bits (8 or 4), which sets the byte layout of a stage.
 // The MoE window's routing in the prologue of its gate/up launch (GemmArgs
 // route_*): the rows over the CTA's warps (route_row), then a flag per hit
 // expert and one warp's prefix count over the flags give the hit list, experts
@@ -263,6 +261,8 @@ __device__ __forceinline__ void route_prologue(const GemmArgs& p, int* rt, int* 
   }
 }
 
+// QT: the weight type -- 8 int8, 4 int4, 2 FP4 (E2M1); QB below is its code
+// width in bits (8 or 4), which sets the byte layout of a stage.
 template <int QT, int MODE, int NM>
 __global__ void __launch_bounds__(TcRoles<(QT == 8 ? 8 : 4)>::kThreads, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_codes,
