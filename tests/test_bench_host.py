@@ -1,6 +1,7 @@
 """Host logic of bench.py (CPU only): the algorithmic byte counts behind the
 roofline, the committed DRAM-traffic summaries it reads, the clock-record
-summary and the peak lookup."""
+summary, the peak lookup, and the order the end-to-end loop imposes on its
+copies and calls."""
 import dataclasses
 import os
 
@@ -164,3 +165,174 @@ def test_l2_label_separates_l2_warm_from_hbm():
     # L2-warm, never HBM; the full-size weight streams are larger than L2
     assert bench.l2_label(1.12e6).startswith("L2-warm")
     assert bench.l2_label(286e6).startswith("inputs larger than L2")
+
+
+# ---- the end-to-end loop's stream ordering, on a model of streams and events ----
+
+class _Op:
+    def __init__(self, kind, stream, **kw):
+        self.kind, self.stream, self.deps, self.kw = kind, stream, set(), kw
+
+
+class _FakeCuda:
+    """Streams as ordered op lists and events as 'the op recorded last', enough
+    to decide what the device may run before what: an op follows the previous
+    op of its stream and every event record its stream waited for."""
+
+    def __init__(self):
+        self.ops = []
+        self.main = self.Stream()
+        self.cur = self.main
+
+    def _add(self, kind, stream=None, **kw):
+        s = stream or self.cur
+        op = _Op(kind, s, **kw)
+        if s.last is not None:
+            op.deps.add(s.last)
+        op.deps |= s.pending
+        s.pending = set()
+        s.last = op
+        self.ops.append(op)
+        return op
+
+    def Stream(self, device=None):
+        class S:
+            last, device = None, "cuda:0"
+
+            def __init__(s):
+                s.pending = set()
+
+            def wait_event(s, ev):
+                if ev.op is not None:
+                    s.pending.add(ev.op)
+
+            def wait_stream(s, other):
+                if other.last is not None:
+                    s.pending.add(other.last)
+        return S()
+
+    def Event(self, enable_timing=False):
+        cuda = self
+
+        class E:
+            op = None
+
+            def record(e, stream=None):
+                e.op = cuda._add("record", stream)
+
+            def elapsed_time(e, other):
+                return 1.0
+        return E()
+
+    def current_stream(self):
+        return self.cur
+
+    def stream(self, s):
+        cuda = self
+
+        class Ctx:
+            def __enter__(c):
+                c.prev, cuda.cur = cuda.cur, s
+
+            def __exit__(c, *a):
+                cuda.cur = c.prev
+        return Ctx()
+
+    def synchronize(self):
+        self._add("sync", self.main)
+        for s in {op.stream for op in self.ops}:
+            s.pending = set()
+
+
+class _FakeTorch:
+    def __init__(self):
+        self.cuda = _FakeCuda()
+
+
+class _Slot:
+    def __init__(self, cuda, kind, idx):
+        self.cuda, self.kind, self.idx = cuda, kind, idx
+
+    def copy_(self, src, non_blocking=False):
+        if self.kind == "in":      # H2D into device record idx
+            self.cuda._add("h2d", slot=self.idx, win=src.idx)
+        else:                      # D2H into host row idx from device record src
+            self.cuda._add("d2h", slot=src.idx, win=self.idx)
+
+
+class _FakeJob:
+    def __init__(self, cuda, slots, nwin):
+        self.cuda, self.nwin = cuda, nwin
+        self.e2e_in = [_Slot(cuda, "in", r) for r in range(slots)]
+        self.e2e_out = [_Slot(cuda, "dev", r) for r in range(slots)]
+        self.in_rows = [_Slot(cuda, "host", j) for j in range(nwin)]
+        self.out_rows = [_Slot(cuda, "out", j) for j in range(nwin)]
+
+    def e2e_call(self, r, i):
+        self.cuda._add("call", slot=r, step=i)
+
+
+def _before(a, b):
+    """Whether op a must finish before op b may start."""
+    seen, todo = set(), [b]
+    while todo:
+        op = todo.pop()
+        for d in op.deps:
+            if d is a:
+                return True
+            if id(d) not in seen:
+                seen.add(id(d))
+                todo.append(d)
+    return False
+
+
+@pytest.mark.parametrize("overlap", [True, False])
+def test_e2e_region_orders_copies_and_calls(overlap):
+    torch = _FakeTorch()
+    cuda = torch.cuda
+    steps, warmup, nwin = 11, 3, 4
+    job = _FakeJob(cuda, bench.E2E_SLOTS, nwin)
+    assert bench.e2e_region(job, steps, warmup, 1, torch, overlap) == 1.0
+    # the timed steps: the ops after the last synchronize
+    last_sync = max(i for i, op in enumerate(cuda.ops) if op.kind == "sync" and i < len(cuda.ops) - 1)
+    ops = cuda.ops[last_sync + 1:]
+    calls = [op for op in ops if op.kind == "call"]
+    h2d = [op for op in ops if op.kind == "h2d"]
+    d2h = [op for op in ops if op.kind == "d2h"]
+    assert len(calls) == len(h2d) == len(d2h) == steps
+    assert all(c.stream is cuda.main for c in calls)
+    if overlap:
+        assert all(o.stream is not cuda.main for o in h2d + d2h)
+        assert h2d[0].stream is not d2h[0].stream
+    R = bench.E2E_SLOTS
+    for i in range(steps):
+        r = i % R
+        assert calls[i].kw == {"slot": r, "step": i}
+        assert h2d[i].kw == {"slot": r, "win": i % nwin} and d2h[i].kw == {"slot": r, "win": i % nwin}
+        # the call reads its inputs after they land and before its result is read
+        assert _before(h2d[i], calls[i]) and _before(calls[i], d2h[i])
+        if i + R < steps:
+            # record r is refilled only after the call that read it, and
+            # rewritten only after its result went back to the host
+            assert _before(calls[i], h2d[i + R])
+            assert _before(d2h[i], calls[i + R])
+    # the end event follows every read-back
+    end = [op for op in ops if op.kind == "record" and op.stream is cuda.main][-1]
+    assert all(_before(o, end) for o in d2h)
+    if overlap:
+        # and the copies are free to overlap other windows' calls: the next
+        # window's inputs do not wait for this window's call
+        assert not _before(calls[0], h2d[1])
+
+
+def test_e2e_record_reports_the_faster_ordering():
+    rec = lambda v, ok: {"value": v, "unit": "windows/s", "copies": "...", "outputs_match_resident": ok}
+    r = bench.e2e_record({"overlapped": rec(14000.0, True), "in_line": rec(12000.0, True)}, 100, 8)
+    assert (r["value"], r["ordering"], r["outputs_match_resident"]) == (14000.0, "overlapped", True)
+    assert r["in_line"]["value"] == 12000.0 and r["h2d_bytes_per_step"] == 100 and r["d2h_bytes_per_step"] == 8
+    r = bench.e2e_record({"overlapped": rec(9000.0, True), "in_line": rec(24000.0, False)}, 100, 8)
+    assert (r["value"], r["ordering"], r["outputs_match_resident"]) == (24000.0, "in_line", False)
+    # results that depend on the step (sampling draws) are not compared
+    r = bench.e2e_record({"overlapped": rec(1.0, None), "in_line": rec(2.0, None)}, 1, 1)
+    assert r["outputs_match_resident"] is None
+    assert [name for name, _, _ in bench.E2E_ORDERINGS] == ["overlapped", "in_line"]
