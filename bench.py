@@ -998,6 +998,8 @@ def run_spec_loop(args, wl, S):
     stats = {}
     spec = specdec.spec_decode(verS, hidden, prompt, args.gen, K, args.ngram, stats)
     t2 = time.perf_counter()
+    if ver1.status() != sdv.SDV_OK or verS.status() != sdv.SDV_OK:
+        raise RuntimeError("device status reported an error in the spec loop")
     alpha = specdec.alpha_estimate(stats)
     per_round = (stats["accepted"] + stats["rounds"]) / max(1, stats["rounds"])
     line = {

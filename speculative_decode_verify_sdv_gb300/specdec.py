@@ -143,6 +143,14 @@ class HeadVerifier:
         o = self.out_h.numpy()
         return o[:S].copy(), int(o[self.s_max]), int(o[self.s_max + 1])
 
+    def status(self) -> int:
+        """The device status of the verify calls since the last read: SDV_OK, or
+        SDV_ERR_TIMEOUT where a bounded device wait gave up (the results of that
+        call are then not to be trusted).  Read and cleared once the verifier's
+        stream has finished; a caller checks it after a decode, or as often as
+        it wants to pay a read-back for."""
+        return sdv.sdv_last_device_status(self.ws, self.stream)
+
 
 def greedy_decode(verify: Callable, hidden: Callable, prompt: Sequence[int], gen: int) -> list[int]:
     """Plain greedy decoding: one S = 1 forward per token."""

@@ -53,8 +53,10 @@ def test_spec_loop_lossless(sdv, bits, n, k, K, m):
     prompt = [int(t) for t in G.randint(G.stream_seed(962, K, m), 16, n)]
     gen = 160
     stats = {}
-    spec = specdec.spec_decode(specdec.HeadVerifier(qw, K + 1), hidden, prompt, gen, K, m, stats)
-    greedy = specdec.greedy_decode(specdec.HeadVerifier(qw, 1), hidden, prompt, gen)
+    ver_s, ver_1 = specdec.HeadVerifier(qw, K + 1), specdec.HeadVerifier(qw, 1)
+    spec = specdec.spec_decode(ver_s, hidden, prompt, gen, K, m, stats)
+    greedy = specdec.greedy_decode(ver_1, hidden, prompt, gen)
+    assert ver_s.status() == sdv.SDV_OK and ver_1.status() == sdv.SDV_OK
     assert spec == greedy
     ref, safe = _oracle_greedy(codes, scales, hidden, prompt, gen)
     assert spec[:safe] == ref[:safe]
@@ -100,3 +102,4 @@ def test_graph_rounds_match_direct_calls(sdv, bits, k):
         a = direct(x, drafts, n_valid)
         b = graphed(x, drafts, n_valid)
         assert np.array_equal(a[0], b[0]) and a[1:] == b[1:], (case, n_valid, a[1:], b[1:])
+    assert direct.status() == sdv.SDV_OK and graphed.status() == sdv.SDV_OK
