@@ -336,3 +336,16 @@ def test_e2e_record_reports_the_faster_ordering():
     r = bench.e2e_record({"overlapped": rec(1.0, None), "in_line": rec(2.0, None)}, 1, 1)
     assert r["outputs_match_resident"] is None
     assert [name for name, _, _ in bench.E2E_ORDERINGS] == ["overlapped", "in_line"]
+
+
+def test_oracle_sample_runs_successive_windows_until_the_budget():
+    import re
+    # the tiny head: a window takes the oracle well under the budget, so the
+    # sample goes on to the windows after window 0
+    rate, desc = bench.oracle_sample(W.TINY, 9, 0.3, 1)
+    n_win = int(re.search(r"of (\d+) successive window", desc).group(1))
+    work = float(re.search(r"([\d.]+) windows of work", desc).group(1))
+    assert n_win > 1 and rate > 0 and abs(work - n_win) <= 1.0
+    # one window at most (the reference arm's step)
+    rate1, desc1 = bench.oracle_sample(W.TINY, 9, 30.0, 1, max_windows=1)
+    assert "of 1 successive window" in desc1 and "1.00 windows of work" in desc1 and rate1 > 0
