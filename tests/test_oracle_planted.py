@@ -85,7 +85,22 @@ def argmax_tail_dropped(real):
     return lambda l: real(np.ascontiguousarray(np.asarray(l)[:, :-1]))
 
 
+def top2_second_distinct(real):
+    # the second largest taken over the values below the maximum, so a
+    # duplicated maximum no longer gives a gap of 0
+    def f(l):
+        l = np.asarray(l, np.float64)
+        out = []
+        for row in l:
+            m = row.max()
+            below = row[row < m]
+            out.append(m - below.max() if below.size else 0.0)
+        return np.array(out)
+    return f
+
+
 ARGMAX_PINS = [pins_gemm.test_argmax_brute_force_and_ties]
+TOP2_PINS = [pins_gemm.test_top2_gap]
 
 # ---- greedy accept ------------------------------------------------------------------
 
@@ -194,6 +209,26 @@ def route_softmax_over_all_experts(real):
     return f
 
 
+def group_rows_reversed(real):
+    # an expert's selections listed in decreasing row order
+    def f(ids, e):
+        off, rows, slots = real(ids, e)
+        rows, slots = rows.copy(), slots.copy()
+        for x in range(e):
+            a, b = int(off[x]), int(off[x + 1])
+            rows[a:b], slots[a:b] = rows[a:b][::-1], slots[a:b][::-1]
+        return off, rows, slots
+    return f
+
+
+def group_offsets_inclusive(real):
+    # the offsets taken from an inclusive scan of the counts
+    def f(ids, e):
+        off, rows, slots = real(ids, e)
+        return np.append(off[1:], off[-1]).astype(np.int32), rows, slots
+    return f
+
+
 # ---- quantisers ---------------------------------------------------------------------
 
 
@@ -279,6 +314,11 @@ def sample_residual_may_return_draft(real):
     return f
 
 
+def mix_state_off_by_one(real):
+    # the finaliser applied to the state before its increment
+    return lambda z: real(np.asarray(z, np.uint64) - sample.G)
+
+
 SAMPLE_PINS = [pins_sample.test_low_temperature_reduces_to_greedy,
                functools.partial(pins_sample.test_first_token_follows_target, 2)]
 
@@ -291,6 +331,7 @@ PLANTS = [
     ("gemm: activation row off by one", verify, "dequant_gemm", gemm_row_off_by_one, GEMM_PINS),
     ("argmax: ties to the last index", verify, "argmax_rows", argmax_ties_to_last, ARGMAX_PINS),
     ("argmax: last entry not scanned", verify, "argmax_rows", argmax_tail_dropped, ARGMAX_PINS),
+    ("top2: second largest below the maximum", verify, "top2_gap", top2_second_distinct, TOP2_PINS),
     ("accept: next token off by one", verify, "greedy_accept", accept_next_off_by_one, ACCEPT_PINS),
     ("accept: pads accepted", verify, "greedy_accept", accept_pads, ACCEPT_PINS),
     ("accept: shifted compare", verify, "greedy_accept", accept_shifted_compare, ACCEPT_PINS),
@@ -304,12 +345,16 @@ PLANTS = [
      [pins_mlp.test_route_topk_brute_force_and_ties]),
     ("route: softmax over every expert", mlp, "route_topk", route_softmax_over_all_experts,
      [pins_mlp.test_route_topk_brute_force_and_ties]),
+    ("group: rows in decreasing order", mlp, "group_by_expert", group_rows_reversed, [pins_mlp.test_group_by_expert]),
+    ("group: inclusive offsets", mlp, "group_by_expert", group_offsets_inclusive, [pins_mlp.test_group_by_expert]),
     ("quant: ties away from zero", quant, "quantize_block32", quant_ties_away_from_zero, QUANT_PINS),
     ("quant: scale not rounded to fp16", quant, "quantize_block32", quant_scale_not_rounded_to_fp16, QUANT_PINS),
     ("int4: nibbles swapped", quant, "pack_int4", pack_nibbles_swapped,
      [pins_quant.test_int4_pack_roundtrip_and_nibble_order]),
     ("e2m1: ties to the larger magnitude", quant, "encode_e2m1", e2m1_ties_up, FP4_PINS),
     ("e2m1: negative zero", quant, "encode_e2m1", e2m1_negative_zero, FP4_PINS),
+    ("splitmix: state off by one increment", sample, "mix", mix_state_off_by_one,
+     [pins_sample.test_splitmix64_published_stream]),
     ("sample: temperature ignored", sample, "verify_sample", sample_temperature_ignored, SAMPLE_PINS),
     ("sample: residual draw may be the draft", sample, "verify_sample", sample_residual_may_return_draft,
      SAMPLE_PINS),
